@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the sliced tensor-parallel MLP layer on GB300.
+
+One step = one domino_mlp_fwd over one batch of the workload (GEMM1 + GEMM2 +
+shard-sum for every chunk and slice), inputs resident in HBM.  Prints ONE JSON
+line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mu MU]
+                  [--schedule streams|serial] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run, one independent replica per GPU (the
+workload has no exchange between GPUs: weak scaling, no data-path collective;
+the only collectives are the timing barrier and the max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "communication_overlap_domino_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_kind, workload):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    entry = rec.get("kernels", {}).get(f"{workload}/{kernel_kind}")
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_row_sample(w, t, target_s):
+    """Times the fp64 oracle's forward on a row sample sized for about target_s.
+
+    Rows are independent in the block, so the sample's flops scale exactly with
+    its row count.  Returns (rows, seconds, flops)."""
+    import oracle
+    f64 = {k: v.to("cpu").double().numpy() for k, v in t.items() if k != "X"}
+    A = (f64["Wg"], f64["Wu"]) if w.act == "swiglu" else f64["A"]
+    rows = min(w.M, 32)
+    while True:
+        X = t["X"][:rows].double().numpy()
+        t0 = time.perf_counter()
+        oracle.mlp_fwd(X, A, f64["B"], w.act)
+        dt = time.perf_counter() - t0
+        flops = w.fwd_flops() * rows / w.M
+        if dt >= 0.5 * target_s or rows >= w.M:
+            return rows, dt, flops
+        rows = int(min(w.M, max(rows * 2, rows * target_s / max(dt, 1e-3))))
+
+
+# ---------------------------------------------------------------- our arm
+
+def timeline_stats(records):
+    """Per call: span of all launches, GEMM-busy time, exposed (non-GEMM) time."""
+    calls = {}
+    for r in records:
+        calls.setdefault(r["call"], []).append(r)
+    spans, exposed = [], []
+    for recs in calls.values():
+        lo = min(r["start_ms"] for r in recs)
+        hi = max(r["end_ms"] for r in recs)
+        ivs = sorted((r["start_ms"], r["end_ms"]) for r in recs if r["kind"] in ("gemm1", "gemm2"))
+        busy, cur_s, cur_e = 0.0, None, None
+        for s, e in ivs:
+            if cur_e is None or s > cur_e:
+                if cur_e is not None:
+                    busy += cur_e - cur_s
+                cur_s, cur_e = s, e
+            else:
+                cur_e = max(cur_e, e)
+        if cur_e is not None:
+            busy += cur_e - cur_s
+        spans.append(hi - lo)
+        exposed.append(max(0.0, (hi - lo) - busy))
+    return statistics.mean(spans), statistics.mean(exposed)
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from communication_overlap_domino_gb300 import binding as b
+    from communication_overlap_domino_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    t = wl.generate(w, seed=0)
+    A = (t["Wg"].to(dev), t["Wu"].to(dev)) if w.act == "swiglu" else t["A"].to(dev)
+    A_sh, B_sh = b.shard_weights(A, t["B"].to(dev), w.P)
+    del A
+    X = t["X"].to(dev)
+    Y = torch.empty((w.M, w.d), dtype=torch.bfloat16, device=dev)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, args.schedule)
+    ws = torch.zeros(b.workspace_size(desc), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(timed=False, x=X):
+        b.mlp_fwd(x, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices,
+                  schedule=args.schedule, Y=Y, workspace=ws, kernel_times=timed)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier(device_ids=[local_rank])
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+    st = b.query_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {b.STATUS.get(st)}")
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the step events)
+    b.kernel_times_reset()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[local_rank]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local_rank
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(timed=True)
+        ev[i][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    st = b.query_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {b.STATUS.get(st)}")
+    step_ms = [s.elapsed_time(e) for s, e in ev]
+    mean_ms = statistics.mean(step_ms)
+    records = b.kernel_times()
+    if world > 1:
+        tt = torch.tensor([mean_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_ms = float(tt.item())
+
+    # ---- end to end: pinned host X in, Y out, copies inside the timed region
+    e2e_steps = max(3, min(args.steps, 200))
+    Xh = t["X"].pin_memory()
+    Yh = torch.empty((w.M, w.d), dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(X)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        ev2[i][0].record(stream)
+        Xd.copy_(Xh, non_blocking=True)
+        step(x=Xd)
+        Yh.copy_(Y, non_blocking=True)
+        ev2[i][1].record(stream)
+    barrier()
+    e2e_ms = statistics.mean(s.elapsed_time(e) for s, e in ev2)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    if not torch.equal(Yh, Y.cpu()):
+        raise RuntimeError("end-to-end output differs from the device result")
+
+    if rank != 0:
+        return None
+
+    # ---- per-kernel durations from the live events of the timed region
+    peaks, peak_src = load_peaks()
+    by_kind = {}
+    for r in records:
+        by_kind.setdefault(r["kind"], []).append(r["end_ms"] - r["start_ms"])
+    nact = 2 if w.act == "swiglu" else 1
+    flops_per_launch = {
+        "gemm1": 2.0 * w.Mc * w.d * w.F * nact,
+        "gemm2": 2.0 * w.Mc * w.F * (w.d // w.slices),
+    }
+    psize = 4 if w.partial == "f32" else 2
+    ss_bytes = (w.P * psize + 2) * w.Mc * (w.d // w.slices)
+    kinds = {k: {"launches": len(v), "avg_us": 1e3 * statistics.mean(v), "total_ms": sum(v)}
+             for k, v in by_kind.items()}
+    dominant = max((k for k in kinds if k.startswith("gemm")), key=lambda k: kinds[k]["total_ms"])
+    dom_tflops = flops_per_launch[dominant] / (kinds[dominant]["avg_us"] * 1e-6) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    ss_gbs = ss_bytes / (kinds["shard_sum"]["avg_us"] * 1e-6) / 1e9
+    span_ms, exposed_ms = timeline_stats(records)
+
+    flops = w.fwd_flops()
+    value = world * flops / (mean_ms * 1e-3) / 1e12
+    line = {
+        "metric": "sliced TP-MLP layer TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights, bf16",
+        "config": {"workload": w.name, "M": w.M, "d": w.d, "F": w.F, "P": w.P, "mu": w.mu, "act": w.act,
+                   "partials": w.partial, "out_slices": w.slices, "schedule": args.schedule,
+                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+        "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
+        "exposed_reduce_us_per_layer": round(1e3 * exposed_ms, 2),
+        "exposed_reduce_frac": round(exposed_ms / span_ms, 4) if span_ms > 0 else None,
+        "roofline": {
+            "kernel": f"gemm_bf16_tcgen05 ({dominant})",
+            "bound": "tensor",
+            "achieved": round(dom_tflops, 2),
+            "peak": peak_tf,
+            "unit": "TFLOP/s",
+            "frac": round(dom_tflops / peak_tf, 4),
+            "peak_source": f"{peak_src} bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
+            else f"{peak_src} bf16_tflops",
+            "frac_of_burst": round(dom_tflops / float(peaks.get("bf16_tflops", peak_tf)), 4),
+            "flops_per_launch": flops_per_launch[dominant],
+            "traffic": ncu_traffic(dominant, w.name),
+        },
+        "shard_sum": {
+            "bound": "hbm",
+            "achieved": round(ss_gbs, 1),
+            "peak": float(peaks.get("hbm_gbs")),
+            "unit": "GB/s",
+            "frac": round(ss_gbs / float(peaks.get("hbm_gbs")), 4),
+            "bytes_per_launch": ss_bytes,
+            "traffic": ncu_traffic("shard_sum", w.name),
+        },
+        "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
+                        "share": round(v["total_ms"] / sum(x["total_ms"] for x in kinds.values()), 4)}
+                    for k, v in kinds.items()},
+        "gpu_launches": len(records),
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": w.M * w.d * 2, "d2h_bytes_per_step": w.M * w.d * 2,
+                "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rows, dt, fl = oracle_row_sample(w, t, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 5), "unit": "TFLOP/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"fp64 oracle forward on {rows} of {w.M} rows ({dt:.1f} s; rows are "
+                                          f"independent, flops scale with rows)"}
+    return line
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, w):
+    """The fp64 CPU oracle as it stands, on the host cores: each step runs the
+    oracle forward on a bounded row sample of the workload."""
+    from communication_overlap_domino_gb300 import workloads as wl
+    t = wl.generate(w, seed=0)
+    budget_s = 150.0
+    rows, dt, _ = oracle_row_sample(w, t, target_s=min(5.0, budget_s / max(1, args.steps + args.warmup)))
+    import oracle
+    f64 = {k: v.double().numpy() for k, v in t.items() if k != "X"}
+    A = (f64["Wg"], f64["Wu"]) if w.act == "swiglu" else f64["A"]
+    X = t["X"][:rows].double().numpy()
+    for _ in range(args.warmup):
+        oracle.mlp_fwd(X, A, f64["B"], w.act)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.mlp_fwd(X, A, f64["B"], w.act)
+        times.append(time.perf_counter() - t0)
+    mean_s = statistics.mean(times)
+    flops = w.fwd_flops() * rows / w.M
+    value = flops / mean_s / 1e12
+    sample = f"fp64 oracle forward on {rows} of {w.M} rows per step"
+    return {
+        "impl": "reference",
+        "metric": "sliced TP-MLP layer TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",
+        "value": round(value, 5),
+        "unit": "TFLOP/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * mean_s, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights, bf16 values widened to fp64",
+        "config": {"workload": w.name, "M": w.M, "d": w.d, "F": w.F, "P": w.P, "mu": w.mu, "act": w.act,
+                   "partials": w.partial, "out_slices": w.slices, "rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--mu", type=int, default=None)
+    ap.add_argument("--schedule", choices=("streams", "serial"), default="streams")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from communication_overlap_domino_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload or wl.BENCH_WORKLOAD]
+    if args.mu is not None:
+        w = w.with_(mu=args.mu)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    import __graft_entry__
+    __graft_entry__.build()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        line = run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

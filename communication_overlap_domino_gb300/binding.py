@@ -1,0 +1,240 @@
+"""ctypes binding of libdomino_gb300.so (include/domino.h), same names as the C ABI.
+
+Argument marshalling only: torch tensors are passed as device pointers, streams
+as cudaStream_t handles; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU or PyTorch fallback: if the library is missing
+or the device is not a GB300, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence, Tuple
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libdomino_gb300.so")
+
+# enums of include/domino.h
+STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTED", 3: "DOMINO_ERR_ALIGNMENT",
+          4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
+ACT = {"gelu": 0, "gelu_tanh": 1, "swiglu": 2, "identity": 3}
+PARTIAL = {"f32": 0, "bf16": 1}
+SCHEDULE = {"serial": 0, "streams": 1}
+KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw"}
+FLAG_KERNEL_TIMES = 1
+MAX_SHARDS = 16
+
+
+class DominoError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {detail}")
+
+
+class MlpDesc(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int64),
+        ("d", ctypes.c_int64),
+        ("F", ctypes.c_int64),
+        ("P", ctypes.c_int32),
+        ("mu", ctypes.c_int32),
+        ("out_slices", ctypes.c_int32),
+        ("act", ctypes.c_int32),
+        ("partial_dtype", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+        ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [
+        ("call", ctypes.c_int32),
+        ("kind", ctypes.c_int32),
+        ("chunk", ctypes.c_int32),
+        ("slice", ctypes.c_int32),
+        ("stream", ctypes.c_int32),
+        ("start_ms", ctypes.c_float),
+        ("end_ms", ctypes.c_float),
+    ]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+_VP = ctypes.c_void_p
+_VPP = ctypes.POINTER(ctypes.c_void_p)
+
+# (name, restype, argtypes) for every entry point of include/domino.h
+SIGNATURES = [
+    ("domino_mlp_workspace_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc), ctypes.c_int32]),
+    ("domino_mlp_saved_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc)]),
+    ("domino_mlp_fwd", ctypes.c_int, [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    ("domino_mlp_bwd", ctypes.c_int,
+     [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP, _VP, _VPP, _VPP, _VP, ctypes.c_size_t, _VP]),
+    ("domino_shard_sum", ctypes.c_int,
+     [_VPP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int64, _VP]),
+    ("domino_query_device_status", ctypes.c_int, [_VP, _VP]),
+    ("domino_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("domino_last_error", ctypes.c_char_p, []),
+    ("domino_kernel_times", ctypes.c_int32, [ctypes.POINTER(KernelTime), ctypes.c_int32]),
+    ("domino_kernel_times_reset", None, []),
+]
+
+
+def lib() -> ctypes.CDLL:
+    """Loads the library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(this package has no CPU or PyTorch fallback)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        detail = lib().domino_last_error().decode(errors="replace")
+        raise DominoError(status, where, detail)
+
+
+def _ptr_array(ptrs: Sequence[int]):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for i, p in enumerate(ptrs):
+        arr[i] = p
+    return arr
+
+
+def make_desc(M: int, d: int, F: int, P: int, mu: int, act: str, partial: str, out_slices: int = 1,
+              schedule: str = "streams", kernel_times: bool = False, timeout_ns: int = 0) -> MlpDesc:
+    return MlpDesc(M=M, d=d, F=F, P=P, mu=mu, out_slices=out_slices, act=ACT[act], partial_dtype=PARTIAL[partial],
+                   schedule=SCHEDULE[schedule], flags=FLAG_KERNEL_TIMES if kernel_times else 0, reserved=0,
+                   timeout_ns=timeout_ns)
+
+
+def workspace_size(desc: MlpDesc, with_bwd: bool = False) -> int:
+    return int(lib().domino_mlp_workspace_size(ctypes.byref(desc), 1 if with_bwd else 0))
+
+
+def saved_size(desc: MlpDesc) -> int:
+    return int(lib().domino_mlp_saved_size(ctypes.byref(desc)))
+
+
+# ------------------------------------------------------------------ torch side
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+_WS_CACHE: Dict[Tuple[int, int], object] = {}
+
+
+def _workspace(nbytes: int, device):
+    """A cached uint8 device buffer of at least nbytes (256-byte aligned by torch)."""
+    torch = _torch()
+    dev = torch.device(device)
+    key = (dev.index if dev.index is not None else torch.cuda.current_device(), nbytes)
+    buf = _WS_CACHE.get(key)
+    if buf is None:
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _WS_CACHE[key] = buf
+    return buf
+
+
+def shard_weights(A, B, P: int):
+    """Splits mathematical-layout weights into the ABI's per-shard layout.
+
+    A: [d, F] (or a pair (Wg, Wu), each [d, F]); B: [F, d].  Returns
+    (A_shards, B_shards): A_shards[p] = A[:, cols_p]^T ([F/P, d]; SwiGLU:
+    Wg[:, cols_p]^T stacked over Wu[:, cols_p]^T, [2F/P, d]) and
+    B_shards[p] = B[cols_p, :]^T ([d, F/P]), each contiguous.  A one-time
+    parameter re-layout (like loading a checkpoint into a tensor-parallel
+    layout), not part of the forward pass.
+    """
+    torch = _torch()
+    if isinstance(A, (tuple, list)):
+        Wg, Wu = A
+        F = Wg.shape[1]
+    else:
+        Wg, Wu = A, None
+        F = A.shape[1]
+    Fp = F // P
+    A_sh, B_sh = [], []
+    for p in range(P):
+        cols = slice(p * Fp, (p + 1) * Fp)
+        if Wu is not None:
+            A_sh.append(torch.cat([Wg[:, cols].t(), Wu[:, cols].t()], dim=0).contiguous())
+        else:
+            A_sh.append(Wg[:, cols].t().contiguous())
+        B_sh.append(B[cols, :].t().contiguous())
+    return A_sh, B_sh
+
+
+def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str, out_slices: int = 1,
+            schedule: str = "streams", Y=None, saved=None, workspace=None, stream=None, kernel_times: bool = False,
+            timeout_ns: int = 0):
+    """domino_mlp_fwd on torch tensors; returns Y [M, d] bf16."""
+    torch = _torch()
+    M, d = X.shape
+    P = len(A_shards)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns)
+    if Y is None:
+        Y = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
+    need = workspace_size(desc)
+    if need == 0:
+        _check(lib().domino_mlp_fwd(ctypes.byref(desc), None, None, None, None, None, None, 0, None), "domino_mlp_fwd")
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    st = lib().domino_mlp_fwd(
+        ctypes.byref(desc), X.data_ptr(), _ptr_array([a.data_ptr() for a in A_shards]),
+        _ptr_array([b.data_ptr() for b in B_shards]), Y.data_ptr(), saved.data_ptr() if saved is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "domino_mlp_fwd")
+    return Y
+
+
+def shard_sum(partials: List, Y, *, stream=None):
+    """domino_shard_sum: Y = bf16(sum of the fp32 or bf16 partials)."""
+    torch = _torch()
+    P = len(partials)
+    rows, cols = partials[0].shape
+    dt = {torch.float32: 0, torch.bfloat16: 1}[partials[0].dtype]
+    st = lib().domino_shard_sum(_ptr_array([z.data_ptr() for z in partials]), P, dt, rows, cols,
+                                partials[0].stride(0), Y.data_ptr(), Y.stride(0), _stream_handle(stream))
+    _check(st, "domino_shard_sum")
+    return Y
+
+
+def query_device_status(workspace, stream=None) -> int:
+    """Synchronises, returns and clears the device status word (0 = OK)."""
+    return int(lib().domino_query_device_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+def kernel_times_reset() -> None:
+    lib().domino_kernel_times_reset()
+
+
+def kernel_times() -> List[dict]:
+    """Per-launch event times logged by calls made with kernel_times=True since the last reset."""
+    n = lib().domino_kernel_times(None, 0)
+    if n <= 0:
+        return []
+    buf = (KernelTime * n)()
+    n = lib().domino_kernel_times(buf, n)
+    if n < 0:
+        raise DominoError(5, "domino_kernel_times", "event synchronisation failed")
+    return [{"call": r.call, "kind": KERNEL_KIND.get(r.kind, r.kind), "chunk": r.chunk, "slice": r.slice,
+             "stream": r.stream, "start_ms": r.start_ms, "end_ms": r.end_ms} for r in buf[:n]]

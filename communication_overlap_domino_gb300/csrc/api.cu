@@ -1,0 +1,496 @@
+// C-ABI layer: argument validation, workspace layout, and the schedule that
+// orders the per-piece GEMMs and shard-sums (declared in include/domino.h).
+//
+// Schedule (Domino page, "Domino: Eliminating Communication in LLM Training via
+// Generic Tensor Slicing and Overlapping", Abstract: independent pieces are
+// pipelined so that one piece's communication overlaps another's computation):
+// for every row chunk k, one grouped GEMM1 launch computes H_{k,p} for all P
+// shards; for every output slice s one grouped GEMM2 launch writes the shard
+// partials Z_{k,p,s}; the shard-sum of (k, s) then runs
+//   SERIAL : next on the caller's stream (fully exposed), or
+//   STREAMS: on the library's reduction stream, released by an event recorded
+//            after GEMM2(k, s), so that it runs while GEMM1/GEMM2 of the next
+//            piece occupy the tensor cores.  The reduction stream is joined back
+//            into the caller's stream at the end of the call.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "gemm.h"
+
+using namespace domino;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+domino_status_t fail(domino_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+constexpr size_t kHeaderBytes = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// --------------------------------------------------------------- per device
+
+struct TimedLaunch {
+  int32_t call, kind, chunk, slice, stream;
+  cudaEvent_t origin, begin, end;
+};
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  cudaStream_t reduce_stream = nullptr;
+  cudaEvent_t ev_fork = nullptr;
+  cudaEvent_t ev_join = nullptr;
+  cudaEvent_t ev_piece[DOMINO_MAX_PIECES] = {};
+  std::vector<cudaEvent_t> timing_pool;  // events with timing, reused after a log reset
+  size_t timing_next = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[64];
+
+// Log of launches made by calls with DOMINO_FLAG_KERNEL_TIMES (guarded by g_mutex).
+struct TimingLog {
+  int32_t calls = 0;
+  std::vector<TimedLaunch> launches;
+};
+TimingLog g_timing;
+
+domino_status_t device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(DOMINO_ERR_DEVICE, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& ds = g_devices[dev];
+  if (!ds.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      char buf[128];
+      snprintf(buf, sizeof buf, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev, major, minor);
+      return fail(DOMINO_ERR_DEVICE, buf);
+    }
+    e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = prepare_gemm_kernels();
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ds.reduce_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_join, cudaEventDisableTiming);
+    for (int i = 0; i < DOMINO_MAX_PIECES && e == cudaSuccess; ++i)
+      e = cudaEventCreateWithFlags(&ds.ev_piece[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("device setup: ") + cudaGetErrorString(e));
+    ds.ready = true;
+  }
+  *out = &ds;
+  return DOMINO_OK;
+}
+
+// ---------------------------------------------------------------- validation
+
+struct Shape {
+  int64_t M, d, F, Fp, Mc, ds;
+  int P, mu, S;
+  int act, partial, schedule;
+  size_t psize;  // bytes per partial element
+  int nact;      // pre-activation matrices per shard (2 for SwiGLU)
+};
+
+domino_status_t check_desc(const domino_mlp_desc_t* desc, Shape* s) {
+  if (desc == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "desc is NULL");
+  const domino_mlp_desc_t& d = *desc;
+  if (d.M < 0 || d.d <= 0 || d.F <= 0) return fail(DOMINO_ERR_INVALID_ARG, "M must be >= 0 and d, F > 0");
+  if (d.P < 1 || d.P > DOMINO_MAX_SHARDS) return fail(DOMINO_ERR_INVALID_ARG, "P must be in 1..DOMINO_MAX_SHARDS");
+  if (d.mu < 1 || d.out_slices < 1) return fail(DOMINO_ERR_INVALID_ARG, "mu and out_slices must be >= 1");
+  if (d.act < DOMINO_ACT_GELU || d.act > DOMINO_ACT_IDENTITY) return fail(DOMINO_ERR_INVALID_ARG, "unknown act");
+  if (d.partial_dtype != DOMINO_PARTIAL_F32 && d.partial_dtype != DOMINO_PARTIAL_BF16)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown partial_dtype");
+  if (d.schedule != DOMINO_SCHEDULE_SERIAL && d.schedule != DOMINO_SCHEDULE_STREAMS)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
+  if (d.reserved != 0) return fail(DOMINO_ERR_INVALID_ARG, "reserved must be 0");
+  if ((d.flags & ~DOMINO_FLAG_KERNEL_TIMES) != 0) return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
+  if (static_cast<int64_t>(d.mu) * d.out_slices > DOMINO_MAX_PIECES)
+    return fail(DOMINO_ERR_UNSUPPORTED, "mu * out_slices exceeds DOMINO_MAX_PIECES");
+  if (d.F % d.P) return fail(DOMINO_ERR_UNSUPPORTED, "P must divide F");
+  if (d.M % d.mu) return fail(DOMINO_ERR_UNSUPPORTED, "mu must divide M");
+  if (d.d % d.out_slices) return fail(DOMINO_ERR_UNSUPPORTED, "out_slices must divide d");
+  const int64_t Fp = d.F / d.P;
+  if (d.d % 8 || Fp % 8 || (d.d / d.out_slices) % 8)
+    return fail(DOMINO_ERR_ALIGNMENT, "d, F/P and d/out_slices must be multiples of 8 (16-byte rows)");
+  const int64_t lim = int64_t(1) << 30;
+  if (d.M >= lim || d.d >= lim || Fp >= lim) return fail(DOMINO_ERR_UNSUPPORTED, "dimension too large");
+  s->M = d.M;
+  s->d = d.d;
+  s->F = d.F;
+  s->P = d.P;
+  s->mu = d.mu;
+  s->S = d.out_slices;
+  s->Fp = Fp;
+  s->Mc = d.M / d.mu;
+  s->ds = d.d / d.out_slices;
+  s->act = d.act;
+  s->partial = d.partial_dtype;
+  s->schedule = d.schedule;
+  s->psize = d.partial_dtype == DOMINO_PARTIAL_F32 ? 4 : 2;
+  s->nact = d.act == DOMINO_ACT_SWIGLU ? 2 : 1;
+  return DOMINO_OK;
+}
+
+struct WsLayout {
+  size_t h_off, h_shard;  // hidden activations [P][M][Fp] bf16
+  size_t z_off, z_shard;  // partials [P][M][d]
+  size_t total;
+};
+
+WsLayout ws_layout(const Shape& s, bool with_bwd) {
+  WsLayout L;
+  size_t off = kHeaderBytes;
+  L.h_shard = static_cast<size_t>(s.M) * s.Fp * 2;
+  L.h_off = off;
+  off = align_up(off + L.h_shard * s.P, 256);
+  L.z_shard = static_cast<size_t>(s.M) * s.d * s.psize;
+  L.z_off = off;
+  off = align_up(off + L.z_shard * s.P, 256);
+  if (with_bwd) {
+    // gradient of the hidden layer [P][M][nact*Fp] bf16
+    off = align_up(off + static_cast<size_t>(s.M) * s.Fp * s.nact * 2 * s.P, 256);
+  }
+  L.total = off;
+  return L;
+}
+
+size_t saved_shard_bytes(const Shape& s) { return static_cast<size_t>(s.M) * s.Fp * (s.nact + 1) * 2; }
+
+// ------------------------------------------------------------------- timing
+
+struct Timer {
+  bool on = false;
+  DeviceState* ds = nullptr;
+  int32_t call = 0;
+  cudaEvent_t origin = nullptr;
+  cudaEvent_t take() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (ds->timing_next == ds->timing_pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      ds->timing_pool.push_back(e);
+    }
+    return ds->timing_pool[ds->timing_next++];
+  }
+  bool start(cudaStream_t s0) {
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      call = g_timing.calls++;
+    }
+    origin = take();
+    if (!origin) return false;
+    cudaEventRecord(origin, s0);
+    return true;
+  }
+};
+
+template <typename F>
+domino_status_t timed(Timer& T, cudaStream_t st, int32_t stream_id, int32_t kind, int32_t chunk, int32_t slice,
+                      F&& launch) {
+  if (!T.on) return launch();
+  bool room;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    room = g_timing.launches.size() < DOMINO_MAX_TIMED_LAUNCHES;
+  }
+  if (!room) return launch();
+  cudaEvent_t b = T.take(), e = T.take();
+  if (!b || !e) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
+  cudaEventRecord(b, st);
+  domino_status_t r = launch();
+  cudaEventRecord(e, st);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_timing.launches.push_back({T.call, kind, chunk, slice, stream_id, T.origin, b, e});
+  return r;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+const char* domino_status_string(domino_status_t status) {
+  switch (status) {
+    case DOMINO_OK: return "DOMINO_OK";
+    case DOMINO_ERR_INVALID_ARG: return "DOMINO_ERR_INVALID_ARG";
+    case DOMINO_ERR_UNSUPPORTED: return "DOMINO_ERR_UNSUPPORTED";
+    case DOMINO_ERR_ALIGNMENT: return "DOMINO_ERR_ALIGNMENT";
+    case DOMINO_ERR_WORKSPACE: return "DOMINO_ERR_WORKSPACE";
+    case DOMINO_ERR_CUDA: return "DOMINO_ERR_CUDA";
+    case DOMINO_ERR_TIMEOUT: return "DOMINO_ERR_TIMEOUT";
+    case DOMINO_ERR_DEVICE: return "DOMINO_ERR_DEVICE";
+    default: return "DOMINO_ERR_UNKNOWN";
+  }
+}
+
+const char* domino_last_error(void) { return g_last_error.c_str(); }
+
+size_t domino_mlp_workspace_size(const domino_mlp_desc_t* desc, int32_t with_bwd) {
+  Shape s;
+  if (check_desc(desc, &s) != DOMINO_OK) return 0;
+  return ws_layout(s, with_bwd != 0).total;
+}
+
+size_t domino_mlp_saved_size(const domino_mlp_desc_t* desc) {
+  Shape s;
+  if (check_desc(desc, &s) != DOMINO_OK) return 0;
+  return saved_shard_bytes(s) * s.P;
+}
+
+domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                               const void* const* B_shards, void* Y, void* saved, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  Shape s;
+  domino_status_t st = check_desc(desc, &s);
+  if (st != DOMINO_OK) return st;
+  if (!X || !A_shards || !B_shards || !Y || !workspace)
+    return fail(DOMINO_ERR_INVALID_ARG, "X, A_shards, B_shards, Y and workspace must be non-NULL");
+  for (int p = 0; p < s.P; ++p) {
+    if (!A_shards[p] || !B_shards[p]) return fail(DOMINO_ERR_INVALID_ARG, "NULL shard pointer");
+    if (!aligned16(A_shards[p]) || !aligned16(B_shards[p]))
+      return fail(DOMINO_ERR_ALIGNMENT, "shard pointers must be 16-byte aligned");
+  }
+  if (!aligned16(X) || !aligned16(Y) || (saved && !aligned16(saved)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(DOMINO_ERR_ALIGNMENT, "X, Y, saved must be 16-byte and workspace 256-byte aligned");
+  const WsLayout W = ws_layout(s, false);
+  if (workspace_bytes < W.total) return fail(DOMINO_ERR_WORKSPACE, "workspace smaller than domino_mlp_workspace_size()");
+  if (s.M == 0) return DOMINO_OK;
+
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != DOMINO_OK) return st;
+
+  cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
+  const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DeviceStatus* dstat = reinterpret_cast<DeviceStatus*>(ws);
+
+  Timer T;
+  T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
+  T.ds = ds;
+  if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
+
+  // Where H and the saved pre-activations go.
+  void* H[kMaxShards];
+  void* pre[kMaxShards];
+  for (int p = 0; p < s.P; ++p) {
+    if (saved) {
+      uint8_t* blk = static_cast<uint8_t*>(saved) + saved_shard_bytes(s) * p;
+      pre[p] = blk;
+      H[p] = blk + static_cast<size_t>(s.M) * s.Fp * s.nact * 2;
+    } else {
+      pre[p] = nullptr;
+      H[p] = ws + W.h_off + W.h_shard * p;
+    }
+  }
+  void* Z[kMaxShards];
+  for (int p = 0; p < s.P; ++p) Z[p] = ws + W.z_off + W.z_shard * p;
+
+  static const int kEpiOfAct[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_SWIGLU, EPI_H_IDENTITY};
+  const bool swiglu = s.act == DOMINO_ACT_SWIGLU;
+  std::string err;
+
+  if (sr != s0) {
+    cudaEventRecord(ds->ev_fork, s0);
+    cudaStreamWaitEvent(sr, ds->ev_fork, 0);
+  }
+
+  for (int k = 0; k < s.mu; ++k) {
+    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
+    // ---- GEMM1: H_{k,p} = act(X_k A_p), all shards in one launch
+    {
+      GemmLaunch L;
+      L.epi = kEpiOfAct[s.act];
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {X, s.M, s.d, s.d};
+        const uint8_t* Ap = static_cast<const uint8_t*>(A_shards[p]);
+        if (swiglu) {
+          L.b0[p] = {Ap, s.Fp, s.d, s.d};
+          L.b1[p] = {Ap + static_cast<size_t>(s.Fp) * s.d * 2, s.Fp, s.d, s.d};
+        } else {
+          L.b0[p] = {Ap, s.Fp, s.d, s.d};
+          L.b1[p] = L.b0[p];
+        }
+        L.out[p] = H[p];
+        L.aux[p] = pre[p];
+      }
+      L.n_tile = swiglu ? kBN / 2 : kBN;
+      L.b1_off = swiglu ? 0 : kBN / 2;
+      L.ldo = s.Fp;
+      L.ld_aux = s.Fp * s.nact;
+      L.aux_u_off = s.Fp;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = 0;
+      L.n_end = static_cast<int32_t>(s.Fp);
+      L.K = s.d;
+      L.status = dstat;
+      L.timeout_ns = tmo;
+      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      if (st != DOMINO_OK) return fail(st, err);
+    }
+    for (int sl = 0; sl < s.S; ++sl) {
+      const int32_t col0 = static_cast<int32_t>(sl * s.ds);
+      // ---- GEMM2: Z_{k,p,s} = H_{k,p} B_p[:, slice s]
+      GemmLaunch L;
+      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {H[p], s.M, s.Fp, s.Fp};
+        L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};
+        L.b1[p] = L.b0[p];
+        L.out[p] = Z[p];
+      }
+      L.n_tile = kBN;
+      L.b1_off = kBN / 2;
+      L.ldo = s.d;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = col0;
+      L.n_end = static_cast<int32_t>(col0 + s.ds);
+      L.K = s.Fp;
+      L.status = dstat;
+      L.timeout_ns = tmo;
+      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      if (st != DOMINO_OK) return fail(st, err);
+
+      // ---- shard-sum of piece (k, s)
+      if (sr != s0) {
+        cudaEvent_t ev = ds->ev_piece[k * s.S + sl];
+        cudaEventRecord(ev, s0);
+        cudaStreamWaitEvent(sr, ev, 0);
+      }
+      ShardSumParams q;
+      memset(&q, 0, sizeof q);
+      const size_t zoff = (static_cast<size_t>(row0) * s.d + col0) * s.psize;
+      for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
+      q.rows = s.Mc;
+      q.cols = s.ds;
+      q.ld_part = s.d;
+      q.ld_y = s.d;
+      q.y = static_cast<uint8_t*>(Y) + (static_cast<size_t>(row0) * s.d + col0) * 2;
+      q.P = s.P;
+      q.f32 = s.partial == DOMINO_PARTIAL_F32;
+      st = timed(T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
+                 [&] { return launch_shard_sum(q, ds->num_sms, sr, &err); });
+      if (st != DOMINO_OK) return fail(st, err);
+    }
+  }
+
+  if (sr != s0) {
+    cudaEventRecord(ds->ev_join, sr);
+    cudaStreamWaitEvent(s0, ds->ev_join, 0);
+  }
+  return DOMINO_OK;
+}
+
+domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                               const void* const* B_shards, const void* dY, const void* saved, void* dX,
+                               void* const* dA_shards, void* const* dB_shards, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  Shape s;
+  domino_status_t st = check_desc(desc, &s);
+  if (st != DOMINO_OK) return st;
+  if (!X || !A_shards || !B_shards || !dY || !saved || !dX || !dA_shards || !dB_shards || !workspace)
+    return fail(DOMINO_ERR_INVALID_ARG, "NULL argument");
+  (void)workspace_bytes;
+  (void)stream;
+  return fail(DOMINO_ERR_UNSUPPORTED, "backward kernels are not built yet");
+}
+
+domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t partial_dtype, int64_t rows,
+                                 int64_t cols, int64_t ld_partial, void* Y, int64_t ld_y, void* stream) {
+  if (!partials || !Y) return fail(DOMINO_ERR_INVALID_ARG, "partials and Y must be non-NULL");
+  if (P < 1 || P > DOMINO_MAX_SHARDS) return fail(DOMINO_ERR_INVALID_ARG, "P must be in 1..DOMINO_MAX_SHARDS");
+  if (partial_dtype != DOMINO_PARTIAL_F32 && partial_dtype != DOMINO_PARTIAL_BF16)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown partial_dtype");
+  if (rows < 0 || cols < 0 || ld_partial < cols || ld_y < cols)
+    return fail(DOMINO_ERR_INVALID_ARG, "bad rows/cols/leading dimensions");
+  if (cols % 8 || ld_partial % 8 || ld_y % 8)
+    return fail(DOMINO_ERR_ALIGNMENT, "cols and leading dimensions must be multiples of 8");
+  for (int p = 0; p < P; ++p) {
+    if (!partials[p]) return fail(DOMINO_ERR_INVALID_ARG, "NULL partial pointer");
+    if (!aligned16(partials[p])) return fail(DOMINO_ERR_ALIGNMENT, "partials must be 16-byte aligned");
+  }
+  if (!aligned16(Y)) return fail(DOMINO_ERR_ALIGNMENT, "Y must be 16-byte aligned");
+  if (rows == 0 || cols == 0) return DOMINO_OK;
+  DeviceState* ds = nullptr;
+  domino_status_t st = device_state(&ds);
+  if (st != DOMINO_OK) return st;
+  ShardSumParams q;
+  memset(&q, 0, sizeof q);
+  for (int p = 0; p < P; ++p) q.part[p] = partials[p];
+  q.rows = rows;
+  q.cols = cols;
+  q.ld_part = ld_partial;
+  q.ld_y = ld_y;
+  q.y = Y;
+  q.P = P;
+  q.f32 = partial_dtype == DOMINO_PARTIAL_F32;
+  std::string err;
+  st = launch_shard_sum(q, ds->num_sms, static_cast<cudaStream_t>(stream), &err);
+  if (st != DOMINO_OK) return fail(st, err);
+  return DOMINO_OK;
+}
+
+domino_status_t domino_query_device_status(void* workspace, void* stream) {
+  if (!workspace) return fail(DOMINO_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("stream sync: ") + cudaGetErrorString(e));
+  DeviceStatus h;
+  e = cudaMemcpy(&h, workspace, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(e));
+  if (h.code == 0) return DOMINO_OK;
+  e = cudaMemset(workspace, 0, sizeof h);
+  if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("status clear: ") + cudaGetErrorString(e));
+  char buf[160];
+  snprintf(buf, sizeof buf, "device wait gave up: site %u, block %u, detail %u", h.where, h.block, h.aux);
+  return fail(static_cast<domino_status_t>(h.code), buf);
+}
+
+int32_t domino_kernel_times(domino_kernel_time_t* out, int32_t max_records) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  const int32_t n = static_cast<int32_t>(g_timing.launches.size());
+  for (int32_t i = 0; i < n && out && i < max_records; ++i) {
+    const TimedLaunch& t = g_timing.launches[i];
+    float b = 0.f, e = 0.f;
+    if (cudaEventSynchronize(t.end) != cudaSuccess) return -1;
+    cudaEventElapsedTime(&b, t.origin, t.begin);
+    cudaEventElapsedTime(&e, t.origin, t.end);
+    out[i] = {t.call, t.kind, t.chunk, t.slice, t.stream, b, e};
+  }
+  return n;
+}
+
+void domino_kernel_times_reset(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_timing.calls = 0;
+  g_timing.launches.clear();
+  for (DeviceState& ds : g_devices) ds.timing_next = 0;
+}
+
+}  // extern "C"

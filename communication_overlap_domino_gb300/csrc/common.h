@@ -1,0 +1,90 @@
+// Structures shared by the host launch code and the device kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "domino.h"
+
+namespace domino {
+
+constexpr int kMaxShards = DOMINO_MAX_SHARDS;
+
+// Device status words, first 16 bytes of the caller's workspace.
+struct DeviceStatus {
+  uint32_t code;   // first error code recorded (0 = none)
+  uint32_t where;  // which wait gave up (site id, see kSite*)
+  uint32_t block;  // blockIdx.x of the CTA that recorded it
+  uint32_t aux;    // site-defined detail (tile index)
+};
+
+// Wait sites reported in DeviceStatus::where.
+enum : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaFull = 2,
+  kSiteMmaTmemEmpty = 3,
+  kSiteEpilogueTmemFull = 4,
+  kSiteDrain = 5,
+};
+
+// Epilogue of the tcgen05 GEMM: what is done with each fp32 accumulator tile.
+enum Epi : int {
+  EPI_H_GELU = 0,       // H = gelu(acc) -> bf16            (GEMM1, GeLU)
+  EPI_H_GELU_TANH = 1,  // H = gelu_tanh(acc) -> bf16
+  EPI_H_IDENTITY = 2,   // H = acc -> bf16
+  EPI_H_SWIGLU = 3,     // H = silu(acc[:, :128]) * acc[:, 128:] -> bf16 (gate | up in one N=256 tile)
+  EPI_Z_F32 = 4,        // partial Z = acc, fp32             (GEMM2)
+  EPI_Z_BF16 = 5,       // partial Z = acc -> bf16
+  EPI_COUNT = 6
+};
+
+// GEMM tile shape: one CTA computes a 128 x 256 fp32 accumulator (tcgen05
+// M=128, N=256) over K in blocks of 64 bf16 (one 128-byte swizzle row).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kAStageBytes = kBM * kBK * 2;
+constexpr int kBStageBytes = kBN * kBK * 2;
+constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint32_t kTmemCols = 2 * kBN;  // double-buffered accumulator
+
+// One grouped, persistent GEMM launch: C_s = A_s * B_s^T for every shard s,
+// A_s [rows, K] and B_s [N, K] bf16 K-major, through TMA tensor maps.
+struct GemmParams {  // CUtensorMap members carry 64-byte alignment
+  CUtensorMap map_a[kMaxShards];   // A operand, box 64 x 128
+  CUtensorMap map_b0[kMaxShards];  // B operand rows [n0, n0+128), box 64 x 128
+  CUtensorMap map_b1[kMaxShards];  // B operand rows for accumulator columns 128..255
+  void* out[kMaxShards];           // output matrix per shard
+  void* aux[kMaxShards];           // optional copy of the pre-activation(s) (bf16), or null
+  int64_t ldo;                     // leading dimension of out (elements)
+  int64_t ld_aux;                  // leading dimension of aux (elements)
+  int64_t aux_u_off;               // SwiGLU: column offset of u inside aux
+  int32_t a_row0;                  // first row of A read by tile row 0
+  int32_t out_row0;                // first output row written by tile row 0
+  int32_t rows;                    // valid rows (tile rows >= rows are not stored)
+  int32_t n_base;                  // output column of tile column 0 (and B row of map_b0)
+  int32_t n_end;                   // output columns >= n_end are not stored
+  int32_t n_tile;                  // output columns per tile (256, or 128 for SwiGLU)
+  int32_t b1_off;                  // B row of the second 128-row box relative to the first
+  int32_t num_kb;                  // K blocks of 64
+  int32_t tiles_m, tiles_n, num_shards, num_tiles;
+  DeviceStatus* status;
+  uint64_t timeout_ns;
+};
+
+// The shard-sum: y[r, c] = bf16(sum_p part[p][r, c]).
+struct ShardSumParams {
+  const void* part[kMaxShards];
+  int64_t rows, cols;  // cols multiple of 8
+  int64_t ld_part;     // elements
+  int64_t ld_y;        // elements
+  void* y;
+  int32_t P;
+  int32_t f32;  // 1: fp32 partials, 0: bf16 partials
+};
+
+}  // namespace domino

@@ -1,0 +1,435 @@
+// Grouped persistent tcgen05 GEMM for the two projections of the sliced MLP.
+//
+// One launch covers every tensor-parallel shard of one row chunk (and one
+// output column slice): C_s = A_s B_s^T for s = 0..P-1, with A_s and B_s bf16,
+// K-major, read by TMA into a 4-stage shared-memory ring, multiplied by
+// tcgen05.mma (M=128, N=256, K=16 per instruction) into an fp32 accumulator in
+// tensor memory, and drained by a fused epilogue:
+//   GEMM1 (column-parallel, Megatron-LM MLP): H = act(X_k A_p), act = GeLU,
+//         tanh-GeLU, identity, or SwiGLU (gate and up accumulated side by side
+//         in one N=256 tile, H = silu(gate) * up);
+//   GEMM2 (row-parallel): the partial Z_{k,p} = H_{k,p} B_p of shard p, in
+//         fp32 or bf16, into that shard's own partial buffer -- the operand of
+//         the shard-sum that stands in for the tensor-parallel all-reduce
+//         (Domino page, Abstract: each piece's communication is issued as soon
+//         as the piece is computed).
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0 lane 0: TMA producer     warp 1: TMEM allocator; lane 0 issues MMAs
+//   warps 2..5   : epilogue (warp w reads TMEM lanes 32*(w%4) .. +31)
+// The accumulator is double-buffered in TMEM (2 x 256 columns), so the
+// epilogue of tile i overlaps the main loop of tile i+1.
+// Every wait is bounded (see mbar_wait); a wait that runs out records
+// DOMINO_ERR_TIMEOUT in the status words and the CTA unwinds cleanly.
+#include <cuda_bf16.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "gemm.h"
+#include "ptx.cuh"
+
+namespace domino {
+
+// ------------------------------------------------------------------ epilogue
+
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_tanh(float x) {
+  return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
+}
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+template <int EPI>
+__device__ __forceinline__ float activate(float x) {
+  if constexpr (EPI == EPI_H_GELU) return gelu_erf(x);
+  else if constexpr (EPI == EPI_H_GELU_TANH) return gelu_tanh(x);
+  else return x;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Stores v[0..n) (n <= 32) as bf16 at dst (16-byte aligned when n == 32).
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (&v)[32], int n) {
+  if (n >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      d4[q] = w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) dst[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], int n) {
+  if (n >= 32) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) dst[j] = v[j];
+  }
+}
+
+// Drains one accumulator tile (this thread: one row) through the epilogue.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int shard, int mb, int nb,
+                                              int row_in_tile) {
+  const int64_t grow = static_cast<int64_t>(mb) * kBM + row_in_tile;
+  const bool row_ok = grow < p.rows;
+  const int64_t orow = p.out_row0 + grow;
+  const int col0 = p.n_base + nb * p.n_tile;
+  constexpr int kChunks = (EPI == EPI_H_SWIGLU) ? (kBN / 2) / 32 : kBN / 32;
+#pragma unroll 1
+  for (int c = 0; c < kChunks; ++c) {
+    const int col = col0 + c * 32;
+    if (col >= p.n_end) break;  // uniform across the warp
+    const int n = p.n_end - col;
+    uint32_t r0[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, r0);
+    if constexpr (EPI == EPI_H_SWIGLU) {
+      uint32_t r1[32];
+      tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
+      tmem_ld_wait();
+      if (row_ok) {
+        float h[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float g = __uint_as_float(r0[j]);
+          const float u = __uint_as_float(r1[j]);
+          h[j] = silu(g) * u;
+        }
+        store_row_bf16(static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col, h, n);
+        if (p.aux[shard] != nullptr) {
+          float g[32], u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            g[j] = __uint_as_float(r0[j]);
+            u[j] = __uint_as_float(r1[j]);
+          }
+          __nv_bfloat16* a = static_cast<__nv_bfloat16*>(p.aux[shard]) + orow * p.ld_aux + col;
+          store_row_bf16(a, g, n);
+          store_row_bf16(a + p.aux_u_off, u, n);
+        }
+      }
+    } else {
+      tmem_ld_wait();
+      if (row_ok) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+        if constexpr (EPI == EPI_Z_F32) {
+          store_row_f32(static_cast<float*>(p.out[shard]) + orow * p.ldo + col, v, n);
+        } else if constexpr (EPI == EPI_Z_BF16) {
+          store_row_bf16(static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col, v, n);
+        } else {
+          if (p.aux[shard] != nullptr)
+            store_row_bf16(static_cast<__nv_bfloat16*>(p.aux[shard]) + orow * p.ld_aux + col, v, n);
+          float h[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(v[j]);
+          store_row_bf16(static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col, h, n);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& shard, int& mb, int& nb) {
+  const int per = p.tiles_m * p.tiles_n;
+  shard = t / per;
+  const int r = t - shard * per;
+  nb = r / p.tiles_m;
+  mb = r - nb * p.tiles_m;
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem_a = smem;
+  uint8_t* smem_b = smem + kStages * kAStageBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + kStages * kBStageBytes);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* final_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4 * 32);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < p.num_shards; ++s) {
+      prefetch_tmap(&p.map_a[s]);
+      prefetch_tmap(&p.map_b0[s]);
+      prefetch_tmap(&p.map_b1[s]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.num_tiles;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load was issued / its phase parity
+    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+      int shard, mb, nb;
+      tile_coords(p, t, shard, mb, nb);
+      const int ya = p.a_row0 + mb * kBM;
+      const int yb0 = p.n_base + nb * p.n_tile;
+      const int yb1 = yb0 + p.b1_off;
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, tmo, p.status, kSiteProducerEmpty, t)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem_a + stage * kAStageBytes;
+        uint8_t* sb = smem_b + stage * kBStageBytes;
+        mbar_arrive_expect_tx(&full_bar[stage], kAStageBytes + kBStageBytes);
+        const int x = kb * kBK;
+        tma_load_2d(sa, &p.map_a[shard], &full_bar[stage], x, ya);
+        tma_load_2d(sb, &p.map_b0[shard], &full_bar[stage], x, yb0);
+        tma_load_2d(sb + kBStageBytes / 2, &p.map_b1[shard], &full_bar[stage], x, yb1);
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+    // Drain: every issued copy must have landed before shared memory is released.
+    for (int s = 0; s < kStages; ++s) {
+      if (issued_mask & (1u << s)) {
+        volatile int no_abort = 0;
+        mbar_wait(&full_bar[s], (issued_parity >> s) & 1u, &no_abort, tmo, p.status, kSiteDrain, s);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+    uint32_t stage = 0, phase = 0;
+    int i = 0;
+    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++i) {
+      const uint32_t acc = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag, tmo, p.status, kSiteMmaTmemEmpty, t)) break;
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + acc * kBN;
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, abort_flag, tmo, p.status, kSiteMmaFull, t)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t adesc = smem_desc_k128(smem_u32(smem_a + stage * kAStageBytes));
+        const uint64_t bdesc = smem_desc_k128(smem_u32(smem_b + stage * kBStageBytes));
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          // advancing K by 16 bf16 = 32 bytes = 2 in the (address >> 4) field
+          mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty_bar[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      mma_commit(&tfull_bar[acc]);
+    }
+    // All MMAs issued by this thread complete before TMEM is released.
+    mma_commit(final_bar);
+    volatile int no_abort = 0;
+    mbar_wait(final_bar, 0, &no_abort, tmo, p.status, kSiteDrain, 99);
+  } else if (warp >= 2) {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int i = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
+      const uint32_t acc = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, tmo, p.status, kSiteEpilogueTmemFull, t)) break;
+      tc_fence_after_sync();
+      int shard, mb, nb;
+      tile_coords(p, t, shard, mb, nb);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+      epilogue_tile<EPI>(p, tacc, shard, mb, nb, row_in_tile);
+      tc_fence_before_sync();
+      mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------- host
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn(std::string* err) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (status == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  if (fn == nullptr && err) *err = "cuTensorMapEncodeTiled entry point unavailable";
+  return fn;
+}
+
+template <int EPI>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(&gemm_bf16_tcgen05_kernel<EPI>);
+}
+
+void* kernel_for(int epi) {
+  switch (epi) {
+    case EPI_H_GELU: return kernel_ptr<EPI_H_GELU>();
+    case EPI_H_GELU_TANH: return kernel_ptr<EPI_H_GELU_TANH>();
+    case EPI_H_IDENTITY: return kernel_ptr<EPI_H_IDENTITY>();
+    case EPI_H_SWIGLU: return kernel_ptr<EPI_H_SWIGLU>();
+    case EPI_Z_F32: return kernel_ptr<EPI_Z_F32>();
+    case EPI_Z_BF16: return kernel_ptr<EPI_Z_BF16>();
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+bool encode_bf16_kmajor(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err) {
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (err) {
+      char buf[256];
+      snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) rows=%lld cols=%lld ld=%lld", (int)r,
+               (long long)op.rows, (long long)op.cols, (long long)op.ld);
+      *err = buf;
+    }
+    return false;
+  }
+  return true;
+}
+
+cudaError_t prepare_gemm_kernels() {
+  for (int e = 0; e < EPI_COUNT; ++e) {
+    cudaError_t st = cudaFuncSetAttribute(kernel_for(e), cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    if (st != cudaSuccess) return st;
+  }
+  return cudaSuccess;
+}
+
+domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stream, std::string* err) {
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  if (L.num_shards < 1 || L.num_shards > kMaxShards) {
+    if (err) *err = "launch_gemm: bad shard count";
+    return DOMINO_ERR_INVALID_ARG;
+  }
+  for (int s = 0; s < L.num_shards; ++s) {
+    if (!encode_bf16_kmajor(&p.map_a[s], L.a[s], kBM, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_kmajor(&p.map_b0[s], L.b0[s], kBN / 2, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_kmajor(&p.map_b1[s], L.b1[s], kBN / 2, err)) return DOMINO_ERR_CUDA;
+    p.out[s] = L.out[s];
+    p.aux[s] = L.aux[s];
+  }
+  p.ldo = L.ldo;
+  p.ld_aux = L.ld_aux;
+  p.aux_u_off = L.aux_u_off;
+  p.a_row0 = L.a_row0;
+  p.out_row0 = L.out_row0;
+  p.rows = L.rows;
+  p.n_base = L.n_base;
+  p.n_end = L.n_end;
+  p.n_tile = L.n_tile;
+  p.b1_off = L.b1_off;
+  p.num_kb = static_cast<int32_t>((L.K + kBK - 1) / kBK);
+  p.tiles_m = (L.rows + kBM - 1) / kBM;
+  p.tiles_n = (L.n_end - L.n_base + L.n_tile - 1) / L.n_tile;
+  p.num_shards = L.num_shards;
+  p.num_tiles = p.tiles_m * p.tiles_n * p.num_shards;
+  p.status = L.status;
+  p.timeout_ns = L.timeout_ns;
+  if (p.num_tiles == 0) return DOMINO_OK;
+  const int grid = p.num_tiles < max_ctas ? p.num_tiles : max_ctas;
+  void* fn = kernel_for(L.epi);
+  if (!fn) {
+    if (err) *err = "launch_gemm: bad epilogue";
+    return DOMINO_ERR_INVALID_ARG;
+  }
+  void* args[] = {&p};
+  cudaError_t st = cudaLaunchKernel(fn, dim3(grid), dim3(kGemmThreads), args, kGemmSmemBytes, stream);
+  if (st != cudaSuccess) {
+    if (err) *err = std::string("gemm launch: ") + cudaGetErrorString(st);
+    return DOMINO_ERR_CUDA;
+  }
+  return DOMINO_OK;
+}
+
+}  // namespace domino

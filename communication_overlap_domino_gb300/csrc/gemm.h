@@ -1,0 +1,45 @@
+// Host-side interface of the grouped tcgen05 GEMM (gemm.cu) and the shard-sum
+// (shard_sum.cu), used by the C-ABI layer (api.cu).
+#pragma once
+
+#include <string>
+
+#include "common.h"
+
+namespace domino {
+
+// A bf16 row-major matrix [rows, cols] with leading dimension ld (elements).
+struct Operand2D {
+  const void* base = nullptr;
+  int64_t rows = 0;
+  int64_t cols = 0;
+  int64_t ld = 0;
+};
+
+// One grouped GEMM launch: for every shard s, out_s = epi(A_s B_s^T), where
+// A_s = a[s] rows [a_row0, a_row0 + rows), B_s = rows [n_base + nb*n_tile, ...)
+// of b0[s] (accumulator columns 0..127) and b1[s] (columns 128..255, at row
+// offset b1_off from the b0 box), contraction length K.
+struct GemmLaunch {
+  int epi = 0;
+  int num_shards = 0;
+  Operand2D a[kMaxShards];
+  Operand2D b0[kMaxShards];
+  Operand2D b1[kMaxShards];
+  void* out[kMaxShards] = {};
+  void* aux[kMaxShards] = {};
+  int64_t ldo = 0, ld_aux = 0, aux_u_off = 0;
+  int32_t a_row0 = 0, out_row0 = 0, rows = 0;
+  int32_t n_base = 0, n_end = 0, n_tile = kBN, b1_off = kBN / 2;
+  int64_t K = 0;
+  DeviceStatus* status = nullptr;
+  uint64_t timeout_ns = 0;
+};
+
+cudaError_t prepare_gemm_kernels();
+domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
+
+// Shard-sum launch (shard_sum.cu).
+domino_status_t launch_shard_sum(const ShardSumParams& p, int num_sms, cudaStream_t stream, std::string* err);
+
+}  // namespace domino

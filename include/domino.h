@@ -1,0 +1,209 @@
+/*
+ * domino.h -- C ABI of the GB300 (sm_103a) sliced tensor-parallel MLP library.
+ *
+ * The operation
+ * -------------
+ * The transformer MLP block  Y = act(X A) B  (GeLU), or
+ *                            Y = (silu(X Wg) * (X Wu)) Wd  (SwiGLU),
+ * computed the way Domino slices a tensor-parallel layer ("Domino: Eliminating
+ * Communication in LLM Training via Generic Tensor Slicing and Overlapping",
+ * Abstract: the data dependency of one batch is broken into independent pieces
+ * whose communication overlaps the next piece's computation):
+ *
+ *   - the hidden dimension F is split into P tensor-parallel shards (the
+ *     Megatron-LM column-parallel / row-parallel MLP, listed under "Builds on" on
+ *     the Domino page): shard p owns columns [p F/P, (p+1) F/P) of A (of Wg and
+ *     Wu) and the same rows of B;
+ *   - the tokens X are split into mu independent row chunks;
+ *   - the output columns can be split into out_slices column slices, a
+ *     decomposition finer than a shard ("Design Space Exploration of DMA based
+ *     Finer-Grain Compute Communication Overlap", Abstract);
+ *   - each shard's row-parallel product is materialised as a partial output and
+ *     a separate memory-bound shard-sum adds the P partials -- the stand-in, on
+ *     one GPU, for the tensor-parallel all-reduce.  The shard-sum of chunk k
+ *     overlaps the GEMMs of chunk k+1.
+ *
+ * All P shards live on the calling GPU as separate buffers; there are no peers
+ * and no collectives.  The result equals the unsharded block up to rounding.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Arrays are row-major, bf16 unless stated, in device memory of the current
+ *    CUDA device.  Weights use the nn.Linear layout (out-features x in-features),
+ *    which makes both forward contractions K-major:
+ *        A_shards[p]  GeLU/identity: A_p^T  [F_p, d]
+ *                     SwiGLU:        [2 F_p, d] = Wg_p^T rows then Wu_p^T rows
+ *        B_shards[p]  B_p^T [d, F_p]   (B = Wd for SwiGLU)
+ *    with F_p = F / P.  A_shards and B_shards themselves are HOST arrays of P
+ *    device pointers.
+ *  - Every device pointer must be 16-byte aligned (TMA); the workspace 256-byte.
+ *  - The caller owns every buffer.  The library allocates no device memory.
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Internally the library may fork work onto its own
+ *    streams; it always joins them back into `stream` before returning.
+ *  - One call in flight per workspace.
+ *  - Argument, shape, alignment and workspace errors are detected on the host,
+ *    before anything is launched, and returned as a status.  Device-side waits
+ *    are bounded by desc->timeout_ns; a wait that runs out records
+ *    DOMINO_ERR_TIMEOUT in the workspace's status word, which
+ *    domino_query_device_status() reads.  No C++ exception crosses this ABI.
+ */
+#ifndef DOMINO_H
+#define DOMINO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DOMINO_API __attribute__((visibility("default")))
+#else
+#define DOMINO_API
+#endif
+
+#define DOMINO_MAX_SHARDS 16
+#define DOMINO_MAX_PIECES 64 /* mu * out_slices */
+
+typedef enum domino_status {
+  DOMINO_OK = 0,
+  DOMINO_ERR_INVALID_ARG = 1, /* null pointer, negative size, unknown enum          */
+  DOMINO_ERR_UNSUPPORTED = 2, /* shape outside what the kernels handle (see below)   */
+  DOMINO_ERR_ALIGNMENT = 3,   /* pointer or leading dimension not 16-byte aligned    */
+  DOMINO_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required          */
+  DOMINO_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed                   */
+  DOMINO_ERR_TIMEOUT = 6,     /* a device-side wait exceeded timeout_ns              */
+  DOMINO_ERR_DEVICE = 7       /* current device is not sm_103 (GB300)                */
+} domino_status_t;
+
+typedef enum domino_act {
+  DOMINO_ACT_GELU = 0,      /* exact GeLU  x * Phi(x)                         */
+  DOMINO_ACT_GELU_TANH = 1, /* tanh approximation of GeLU                     */
+  DOMINO_ACT_SWIGLU = 2,    /* silu(x Wg) * (x Wu)                            */
+  DOMINO_ACT_IDENTITY = 3   /* no activation (used by tests)                  */
+} domino_act_t;
+
+typedef enum domino_partial_dtype {
+  DOMINO_PARTIAL_F32 = 0, /* each shard's partial output kept in fp32         */
+  DOMINO_PARTIAL_BF16 = 1 /* ... rounded to bf16 before the shard-sum         */
+} domino_partial_dtype_t;
+
+typedef enum domino_schedule {
+  DOMINO_SCHEDULE_SERIAL = 0, /* GEMMs and shard-sums in order on one stream: no overlap  */
+  DOMINO_SCHEDULE_STREAMS = 1 /* shard-sum of piece (k,s) on a second stream, released by
+                                 an event after its GEMM, overlapping the next piece      */
+} domino_schedule_t;
+
+/* desc->flags */
+#define DOMINO_FLAG_KERNEL_TIMES 1u /* record CUDA events around every launch; read them
+                                       back with domino_last_kernel_times()             */
+
+typedef struct domino_mlp_desc {
+  int64_t M;              /* tokens (rows of X and Y), >= 0                      */
+  int64_t d;              /* model width, > 0, multiple of 8                     */
+  int64_t F;              /* hidden width (per gate/up for SwiGLU), > 0          */
+  int32_t P;              /* shards, 1..DOMINO_MAX_SHARDS, P | F, (F/P) % 8 == 0  */
+  int32_t mu;             /* row chunks, >= 1, mu | M                            */
+  int32_t out_slices;     /* output column slices, >= 1, out_slices | d,
+                             (d / out_slices) % 8 == 0                          */
+  int32_t act;            /* domino_act_t                                        */
+  int32_t partial_dtype;  /* domino_partial_dtype_t                              */
+  int32_t schedule;       /* domino_schedule_t                                   */
+  uint32_t flags;         /* DOMINO_FLAG_*                                       */
+  uint32_t reserved;      /* must be 0                                           */
+  uint64_t timeout_ns;    /* bound on each device-side wait; 0 = 2 seconds       */
+} domino_mlp_desc_t;
+
+/* Bytes of device workspace domino_mlp_fwd/bwd need for this problem
+ * (0 for an invalid descriptor).  Layout, all owned by the library while a call
+ * runs: a 256-byte header (device status words), the hidden activations
+ * [P][M][F_p] bf16 (unless `saved` is given to fwd), and the P partial outputs
+ * [P][M][d] in the partial dtype.  with_bwd != 0 adds what the backward pass
+ * needs (the gradient of the hidden layer and the dX partials). */
+DOMINO_API size_t domino_mlp_workspace_size(const domino_mlp_desc_t* desc, int32_t with_bwd);
+
+/* Bytes of the `saved` buffer that fwd fills for bwd (0 if invalid):
+ * per shard p, [M][F_p] pre-activation g (and u for SwiGLU, as [M][2 F_p] = g|u)
+ * followed by the activation H [M][F_p], all bf16. */
+DOMINO_API size_t domino_mlp_saved_size(const domino_mlp_desc_t* desc);
+
+/* Forward pass.  X [M,d]; A_shards/B_shards as above; Y [M,d] written (bf16).
+ * saved: NULL, or domino_mlp_saved_size() bytes that receive the
+ * pre-activations and H for domino_mlp_bwd.
+ * Steps per chunk k (and slice s): GEMM1 H_{k,p} = act(X_k A_p) for all p in one
+ * launch, fused activation epilogue; GEMM2 Z_{k,p,s} = H_{k,p} B_p[:, s] into
+ * shard p's partial buffer; shard-sum Y_k[:, s] = sum_{p=0}^{P-1} Z_{k,p,s}
+ * accumulated in fp32 in shard order and rounded once to bf16. */
+DOMINO_API domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                               const void* const* B_shards, void* Y, void* saved, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Backward pass of the same block (chain rule), sliced the same way:
+ * dY [M,d] in; dX [M,d] out (sum over shards of each shard's partial input
+ * gradient, via the shard-sum); dA_shards[p] / dB_shards[p] out, in the same
+ * layouts as A_shards[p] / B_shards[p].  `saved` must hold what fwd wrote.
+ * Returns DOMINO_ERR_UNSUPPORTED while the backward kernels are not built. */
+DOMINO_API domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                               const void* const* B_shards, const void* dY, const void* saved, void* dX,
+                               void* const* dA_shards, void* const* dB_shards, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* The shard-sum alone: Y[r, c] = bf16( sum_{p=0}^{P-1} partials[p][r, c] ),
+ * fp32 accumulation in shard order, one round-to-nearest-even at the end.
+ * partials: HOST array of P device pointers to [rows, cols] matrices with leading
+ * dimension ld_partial (elements) in `partial_dtype`; Y [rows, cols] bf16 with
+ * leading dimension ld_y.  cols, ld_partial and ld_y must be multiples of 8. */
+DOMINO_API domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t partial_dtype, int64_t rows,
+                                 int64_t cols, int64_t ld_partial, void* Y, int64_t ld_y, void* stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded in the
+ * workspace's status word since the last query (DOMINO_OK if none) and clears it. */
+DOMINO_API domino_status_t domino_query_device_status(void* workspace, void* stream);
+
+/* Static, NUL-terminated name of a status code. */
+DOMINO_API const char* domino_status_string(domino_status_t status);
+
+/* Human-readable detail of the last error returned on the calling host thread. */
+DOMINO_API const char* domino_last_error(void);
+
+/* Kernel launch timing.  Every call made with DOMINO_FLAG_KERNEL_TIMES records a
+ * CUDA event before and after each of its kernel launches, on the stream the
+ * kernel is launched on, and appends one record per launch to a process-wide
+ * log (events are pooled; the log holds at most DOMINO_MAX_TIMED_LAUNCHES
+ * records, further launches are not recorded). */
+#define DOMINO_MAX_TIMED_LAUNCHES 262144
+
+typedef enum domino_kernel_kind {
+  DOMINO_KERNEL_GEMM1 = 0,     /* column-parallel GEMM + activation, all shards        */
+  DOMINO_KERNEL_GEMM2 = 1,     /* row-parallel GEMM into the partial buffers           */
+  DOMINO_KERNEL_SHARD_SUM = 2, /* sum of the P partials                                */
+  DOMINO_KERNEL_BWD_DH = 3,    /* backward: dH and the activation derivative           */
+  DOMINO_KERNEL_BWD_DX = 4,    /* backward: partial input gradients                    */
+  DOMINO_KERNEL_BWD_DW = 5     /* backward: weight gradients                           */
+} domino_kernel_kind_t;
+
+typedef struct domino_kernel_time {
+  int32_t call;     /* index of the timed call since the last reset (0-based)          */
+  int32_t kind;     /* domino_kernel_kind_t                                            */
+  int32_t chunk;    /* k                                                               */
+  int32_t slice;    /* s (0 for kernels that cover all slices)                         */
+  int32_t stream;   /* 0: the caller's stream, 1: the library's reduction stream       */
+  float start_ms;   /* event before the launch, relative to the call's first event     */
+  float end_ms;     /* event after the launch, same origin                             */
+} domino_kernel_time_t;
+
+/* Waits for the recorded events and copies up to max_records records (oldest
+ * first) into `out` (host memory; may be NULL to only count).  Returns the
+ * number of records logged since the last reset. */
+DOMINO_API int32_t domino_kernel_times(domino_kernel_time_t* out, int32_t max_records);
+
+/* Empties the log (the pooled events are kept for reuse). */
+DOMINO_API void domino_kernel_times_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DOMINO_H */

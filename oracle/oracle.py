@@ -276,3 +276,16 @@ def max_rel_err(got, ref) -> float:
     if den == 0.0:
         return num
     return num / den
+
+
+def shard_sum(partials) -> Array:
+    """The exchange step alone: Y = sum over shards of the partial outputs, in fp64.
+
+    Stands in for the tensor-parallel all-reduce of the row-parallel products
+    (Megatron-LM MLP; hidden by Domino behind the next piece's computation,
+    Domino page, Abstract).
+    """
+    acc = np.zeros(np.asarray(partials[0]).shape)
+    for z in partials:
+        acc = acc + np.asarray(z, np.float64)
+    return acc

@@ -259,6 +259,24 @@ def pin_closed_forms(orc):
                    "swiglu linear in up")
 
 
+def pin_shard_sum(orc):
+    """The exchange step: one-hot partials, and the shard split of B (rows) summed
+    over shards equals the unsharded row-parallel product."""
+    rng = _rng(17)
+    parts = [np.zeros((3, 4)) for _ in range(3)]
+    for p in range(3):
+        parts[p][p, p] = p + 1.0
+    ref = np.zeros((3, 4))
+    ref[0, 0], ref[1, 1], ref[2, 2] = 1.0, 2.0, 3.0
+    _close(orc.shard_sum(parts), ref, 0.0, "shard_sum one-hot")
+    H = rng.normal(0, 1, (5, 12))
+    B = rng.normal(0, 1, (12, 6))
+    for P in (1, 2, 3, 4):
+        Fp = 12 // P
+        parts = [H[:, p * Fp:(p + 1) * Fp] @ B[p * Fp:(p + 1) * Fp] for p in range(P)]
+        _close(orc.shard_sum(parts), H @ B, 1e-13, f"shard_sum of row-parallel partials P={P}")
+
+
 def pin_error_measure(orc):
     ref = np.array([[1.0, -4.0], [2.0, 0.5]])
     got = ref + np.array([[0.0, 0.02], [-0.04, 0.0]])
@@ -275,5 +293,6 @@ ALL_PINS = (
     pin_row_separability,
     pin_hidden_permutation,
     pin_closed_forms,
+    pin_shard_sum,
     pin_error_measure,
 )

@@ -1,0 +1,192 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GB300).
+
+Bar: max|Y - Y_ref| / max|Y_ref| <= 1e-2 per output tensor (bf16 inputs, fp32
+accumulation).  Small cases are compared element by element over the whole
+output; the full-size workloads on rows sampled across every chunk (rows are
+independent, so the oracle computes exactly those rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from communication_overlap_domino_gb300 import binding as b
+from communication_overlap_domino_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _device_inputs(w, t):
+    dev = torch.device("cuda:0")
+    A = (t["Wg"].to(dev), t["Wu"].to(dev)) if w.act == "swiglu" else t["A"].to(dev)
+    A_sh, B_sh = b.shard_weights(A, t["B"].to(dev), w.P)
+    return t["X"].to(dev), A_sh, B_sh
+
+
+def _oracle_A(w, f64):
+    return (f64["Wg"], f64["Wu"]) if w.act == "swiglu" else f64["A"]
+
+
+def _run(w, t, schedule="streams", saved=None, Y=None):
+    X, A_sh, B_sh = _device_inputs(w, t)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, schedule)
+    ws = torch.zeros(b.workspace_size(desc), dtype=torch.uint8, device="cuda:0")
+    Y = b.mlp_fwd(X, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices,
+                  schedule=schedule, workspace=ws, saved=saved, Y=Y)
+    status = b.query_device_status(ws)
+    assert status == 0, f"device status {b.STATUS.get(status)}"
+    return Y
+
+
+def _check_full(w, seed=0, schedule="streams"):
+    t = wl.generate(w, seed)
+    Y = _run(w, t, schedule)
+    f64 = wl.to_float64(t)
+    ref = oracle.mlp_fwd(f64["X"], _oracle_A(w, f64), f64["B"], w.act)
+    got = Y.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    err = oracle.max_rel_err(got, ref)
+    assert err <= TOL, f"{w.name}: max rel err {err:.3e}"
+    return err
+
+
+# --------------------------------------------------------------- shard-sum
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_shard_sum_parity(P, dtype):
+    g = torch.Generator().manual_seed(100 + P)
+    rows, cols, ld = 300, 136, 152
+    parts_cpu = [torch.randn(rows, ld, generator=g).to(dtype) for _ in range(P)]
+    parts = [z.cuda() for z in parts_cpu]
+    Y = torch.full((rows, cols + 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    b.shard_sum([z[:, :cols] for z in parts], Y[:, :cols])
+    torch.cuda.synchronize()
+    ref = oracle.shard_sum([z[:, :cols].double().numpy() for z in parts_cpu])
+    got = Y[:, :cols].double().cpu().numpy()
+    bound = 2.0 ** -8 * np.abs(ref) + P * 2.0 ** -22 * sum(np.abs(z[:, :cols].double().numpy()) for z in parts_cpu)
+    assert np.all(np.abs(got - ref) <= bound + 1e-30)
+    assert oracle.max_rel_err(got, ref) <= TOL
+    assert torch.all(Y[:, cols:] == 7.0), "wrote outside the output columns"
+
+
+# ---------------------------------------------------------- small workloads
+
+@pytest.mark.parametrize("schedule", ["serial", "streams"])
+def test_tiny_gelu_workload(schedule):
+    _check_full(wl.WORKLOADS["tiny_gelu_fwd"], schedule=schedule)
+
+
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "identity"])
+@pytest.mark.parametrize("partial", ["f32", "bf16"])
+def test_ragged_shapes(act, partial):
+    # chunk rows 200 (not a multiple of 128), F/P = 328 (N and K tails), d = 336
+    # (K tail for GEMM1), two output slices of 168 columns (N tail), P = 3, mu = 3
+    w = wl.Workload("ragged", M=600, d=336, F=984, P=3, mu=3, act=act, partial=partial, slices=2)
+    _check_full(w, seed=3)
+
+
+def test_llama_shard_width_tail():
+    # F/P = 1376 as in the Llama-style workload (10.75 tiles of 128), small M and d
+    w = wl.Workload("llama_tail", M=512, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16")
+    _check_full(w, seed=4)
+
+
+@pytest.mark.parametrize("P,mu,S", [(1, 1, 1), (4, 4, 1), (2, 1, 4), (16, 2, 1)])
+def test_degenerate_slicings(P, mu, S):
+    w = wl.Workload("degenerate", M=512, d=512, F=16 * 128, P=P, mu=mu, act="gelu", partial="f32", slices=S)
+    _check_full(w, seed=5)
+
+
+def test_empty_batch_leaves_output_untouched():
+    w = wl.Workload("empty", M=0, d=512, F=1024, P=2, mu=1, act="gelu", partial="f32")
+    t = wl.generate(w.with_(M=1))
+    X, A_sh, B_sh = _device_inputs(w, t)
+    Y = torch.full((1, 512), 3.0, dtype=torch.bfloat16, device="cuda")
+    b.mlp_fwd(X[:0], A_sh, B_sh, F=w.F, mu=1, act="gelu", partial="f32", Y=Y[:0])
+    torch.cuda.synchronize()
+    assert torch.all(Y == 3.0)
+
+
+def test_deterministic_and_schedule_independent():
+    w = wl.WORKLOADS["tiny_gelu_fwd"].with_(M=1024, mu=4)
+    t = wl.generate(w, seed=6)
+    y1 = _run(w, t, "streams").clone()
+    y2 = _run(w, t, "streams").clone()
+    y3 = _run(w, t, "serial").clone()
+    assert torch.equal(y1, y2), "two runs differ"
+    assert torch.equal(y1, y3), "serial and overlapped schedules differ"
+    w8 = w.with_(mu=8)
+    y4 = _run(w8, t, "streams")
+    assert torch.equal(y1, y4), "result depends on mu"
+
+
+def test_saved_preactivations():
+    w = wl.Workload("saved", M=256, d=512, F=2048, P=2, mu=2, act="swiglu", partial="bf16")
+    t = wl.generate(w, seed=7)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial)
+    saved = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device="cuda")
+    Y = _run(w, t, saved=saved)
+    f64 = wl.to_float64(t)
+    inter = oracle.mlp_fwd_intermediates(f64["X"], _oracle_A(w, f64), f64["B"], w.act)
+    Fp = w.Fp
+    blk = saved.view(torch.bfloat16).view(w.P, w.M, 3 * Fp)
+    for p in range(w.P):
+        cols = slice(p * Fp, (p + 1) * Fp)
+        g = blk[p, :, :Fp].double().cpu().numpy()
+        u = blk[p, :, Fp:2 * Fp].double().cpu().numpy()
+        # H lives after the [M, 2 Fp] pre-activation block of the shard
+        Hp = saved.view(torch.bfloat16)[p * w.M * 3 * Fp + w.M * 2 * Fp:(p + 1) * w.M * 3 * Fp]
+        Hp = Hp.view(w.M, Fp).double().cpu().numpy()
+        assert oracle.max_rel_err(g, inter["g"][:, cols]) <= TOL
+        assert oracle.max_rel_err(u, inter["u"][:, cols]) <= TOL
+        assert oracle.max_rel_err(Hp, inter["H"][:, cols]) <= TOL
+    ref = inter["Y"]
+    assert oracle.max_rel_err(Y.double().cpu().numpy(), ref) <= TOL
+
+
+# ------------------------------------------------------- full-size workloads
+
+def _sample_rows(w, per_chunk=6, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for k in range(w.mu):
+        lo = k * w.Mc
+        rows += [lo, lo + w.Mc - 1]
+        rows += list(lo + rng.integers(0, w.Mc, per_chunk - 2))
+    return sorted(set(int(r) for r in rows))
+
+
+def _check_sampled(w, schedule="streams"):
+    t = wl.generate(w, seed=0)
+    Y = _run(w, t, schedule)
+    rows = _sample_rows(w)
+    f64 = {k: v[rows].to(torch.float64).numpy() if k == "X" else v.to(torch.float64).numpy() for k, v in t.items()}
+    ref = oracle.mlp_fwd(f64["X"], _oracle_A(w, f64), f64["B"], w.act)
+    got = Y[rows].double().cpu().numpy()
+    err = oracle.max_rel_err(got, ref)
+    assert err <= TOL, f"{w.name} mu={w.mu}: max rel err {err:.3e} on {len(rows)} sampled rows"
+    # properties that hold at any size: finite everywhere, not all zero per chunk
+    assert torch.isfinite(Y).all()
+    for k in range(w.mu):
+        assert Y[k * w.Mc:(k + 1) * w.Mc].abs().amax() > 0
+    return err
+
+
+@pytest.mark.parametrize("name", ["gpt_gelu_fwd", "llama_swiglu_fwd"])
+def test_full_size_workload(name):
+    _check_sampled(wl.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("mu", [1, 2, 4, 8])
+def test_large_swiglu_mu_sweep(mu):
+    _check_sampled(wl.WORKLOADS["large_swiglu_fwd"].with_(mu=mu))
