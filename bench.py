@@ -42,10 +42,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("common.h", "gemm.cu", "gemm.h", "ptx.cuh", "shard_sum.cu")
+
+
 def kernel_source_hash():
+    """Hash of the device-code sources, to tell whether a stored ncu capture still applies."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "communication_overlap_domino_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

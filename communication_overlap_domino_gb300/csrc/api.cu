@@ -261,6 +261,7 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
   Shape s;
   domino_status_t st = check_desc(desc, &s);
   if (st != DOMINO_OK) return st;
+  if (s.M == 0) return DOMINO_OK;  // an empty batch reads and writes nothing; X and Y may be NULL
   if (!X || !A_shards || !B_shards || !Y || !workspace)
     return fail(DOMINO_ERR_INVALID_ARG, "X, A_shards, B_shards, Y and workspace must be non-NULL");
   for (int p = 0; p < s.P; ++p) {
@@ -273,7 +274,6 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
     return fail(DOMINO_ERR_ALIGNMENT, "X, Y, saved must be 16-byte and workspace 256-byte aligned");
   const WsLayout W = ws_layout(s, false);
   if (workspace_bytes < W.total) return fail(DOMINO_ERR_WORKSPACE, "workspace smaller than domino_mlp_workspace_size()");
-  if (s.M == 0) return DOMINO_OK;
 
   DeviceState* ds = nullptr;
   st = device_state(&ds);

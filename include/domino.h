@@ -130,6 +130,8 @@ DOMINO_API size_t domino_mlp_workspace_size(const domino_mlp_desc_t* desc, int32
 DOMINO_API size_t domino_mlp_saved_size(const domino_mlp_desc_t* desc);
 
 /* Forward pass.  X [M,d]; A_shards/B_shards as above; Y [M,d] written (bf16).
+ * M == 0 returns DOMINO_OK after checking the descriptor, touching nothing
+ * (every pointer may then be NULL).
  * saved: NULL, or domino_mlp_saved_size() bytes that receive the
  * pre-activations and H for domino_mlp_bwd.
  * Steps per chunk k (and slice s): GEMM1 H_{k,p} = act(X_k A_p) for all p in one

@@ -139,16 +139,14 @@ def test_saved_preactivations():
     f64 = wl.to_float64(t)
     inter = oracle.mlp_fwd_intermediates(f64["X"], _oracle_A(w, f64), f64["B"], w.act)
     Fp = w.Fp
-    blk = saved.view(torch.bfloat16).view(w.P, w.M, 3 * Fp)
+    # per shard: pre-activations [M, 2 Fp] (g | u), then H [M, Fp]
+    blk = saved.view(torch.bfloat16).view(w.P, 3 * w.M * Fp)
     for p in range(w.P):
         cols = slice(p * Fp, (p + 1) * Fp)
-        g = blk[p, :, :Fp].double().cpu().numpy()
-        u = blk[p, :, Fp:2 * Fp].double().cpu().numpy()
-        # H lives after the [M, 2 Fp] pre-activation block of the shard
-        Hp = saved.view(torch.bfloat16)[p * w.M * 3 * Fp + w.M * 2 * Fp:(p + 1) * w.M * 3 * Fp]
-        Hp = Hp.view(w.M, Fp).double().cpu().numpy()
-        assert oracle.max_rel_err(g, inter["g"][:, cols]) <= TOL
-        assert oracle.max_rel_err(u, inter["u"][:, cols]) <= TOL
+        pre = blk[p, :2 * w.M * Fp].view(w.M, 2 * Fp).double().cpu().numpy()
+        Hp = blk[p, 2 * w.M * Fp:].view(w.M, Fp).double().cpu().numpy()
+        assert oracle.max_rel_err(pre[:, :Fp], inter["g"][:, cols]) <= TOL
+        assert oracle.max_rel_err(pre[:, Fp:], inter["u"][:, cols]) <= TOL
         assert oracle.max_rel_err(Hp, inter["H"][:, cols]) <= TOL
     ref = inter["Y"]
     assert oracle.max_rel_err(Y.double().cpu().numpy(), ref) <= TOL
