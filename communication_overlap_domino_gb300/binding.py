@@ -76,6 +76,7 @@ SIGNATURES = [
     ("domino_query_device_status", ctypes.c_int, [_VP, _VP]),
     ("domino_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("domino_last_error", ctypes.c_char_p, []),
+    ("domino_mlp_fwd_noalloc", ctypes.c_int, [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP]),
     ("domino_kernel_times", ctypes.c_int32, [ctypes.POINTER(KernelTime), ctypes.c_int32]),
     ("domino_kernel_times_reset", None, []),
 ]
@@ -203,6 +204,24 @@ def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, par
         _ptr_array([b.data_ptr() for b in B_shards]), Y.data_ptr(), saved.data_ptr() if saved is not None else None,
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "domino_mlp_fwd")
+    return Y
+
+
+def mlp_fwd_noalloc(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str,
+                    out_slices: int = 1, Y=None, stream=None, timeout_ns: int = 0):
+    """domino_mlp_fwd_noalloc: the forward pass with the library's own fixed scratch
+    array instead of a workspace, for callers that cannot allocate device memory
+    while the layer runs.  Serial schedule; returns Y [M, d] bf16."""
+    torch = _torch()
+    M, d = X.shape
+    P = len(A_shards)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, "serial", False, timeout_ns)
+    if Y is None:
+        Y = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
+    st = lib().domino_mlp_fwd_noalloc(
+        ctypes.byref(desc), X.data_ptr(), _ptr_array([a.data_ptr() for a in A_shards]),
+        _ptr_array([b.data_ptr() for b in B_shards]), Y.data_ptr(), _stream_handle(stream))
+    _check(st, "domino_mlp_fwd_noalloc")
     return Y
 
 

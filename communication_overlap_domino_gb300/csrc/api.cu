@@ -223,6 +223,12 @@ domino_status_t timed(Timer& T, cudaStream_t st, int32_t stream_id, int32_t kind
 
 }  // namespace
 
+namespace domino {
+// Lets other translation units of the library report a detailed error through
+// domino_last_error().
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace domino
+
 // ====================================================================== ABI
 
 extern "C" {

@@ -39,6 +39,9 @@ struct GemmLaunch {
 cudaError_t prepare_gemm_kernels();
 domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
 
+// Records a detailed message for domino_last_error() (api.cu).
+void set_last_error(const std::string& msg);
+
 // Shard-sum launch (shard_sum.cu).
 domino_status_t launch_shard_sum(const ShardSumParams& p, int num_sms, cudaStream_t stream, std::string* err);
 

@@ -170,6 +170,34 @@ DOMINO_API const char* domino_status_string(domino_status_t status);
 /* Human-readable detail of the last error returned on the calling host thread. */
 DOMINO_API const char* domino_last_error(void);
 
+/* Forward pass without a caller-provided workspace, for callers that cannot
+ * allocate device memory when they run the layer (allocation-free real-time
+ * loops, hosts that hand out all device memory themselves, runtimes that forbid
+ * allocation after start-up).  No counterpart on the pages: this is a packaging
+ * of domino_mlp_fwd, not a step of the method.
+ *
+ * Same arguments and result as domino_mlp_fwd with saved = NULL, but the scratch
+ * (hidden activations and shard partials) lives in a fixed array of
+ * DOMINO_NOALLOC_SCRATCH_BYTES of device memory inside the library, which every
+ * GPU that loads the library holds until the process exits.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no stream or event creation.
+ *  - Runs the SERIAL schedule on `stream` whatever desc->schedule says; desc->flags
+ *    must be 0.
+ *  - A problem whose workspace (domino_mlp_workspace_size(desc, 0)) exceeds
+ *    DOMINO_NOALLOC_SCRATCH_BYTES is rejected with DOMINO_ERR_WORKSPACE.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array and leaves its contents behind:
+ *    calls that overlap on the GPU (other streams, other host threads) race, so
+ *    serialise them.
+ *  - Device-side waits are bounded as in domino_mlp_fwd, but a timeout of this
+ *    variant is not reported through domino_query_device_status. */
+#define DOMINO_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_desc_t* desc, const void* X,
+                                                  const void* const* A_shards, const void* const* B_shards, void* Y,
+                                                  void* stream);
+
 /* Kernel launch timing.  Every call made with DOMINO_FLAG_KERNEL_TIMES records a
  * CUDA event before and after each of its kernel launches, on the stream the
  * kernel is launched on, and appends one record per launch to a process-wide
