@@ -143,21 +143,31 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_row_sample(w, t, target_s):
-    """Times the fp64 oracle's forward on a row sample sized for about target_s.
-
-    Rows are independent in the block, so the sample's flops scale exactly with
-    its row count.  Returns (rows, seconds, flops)."""
+def oracle_step(w, f64, X, dY):
+    """One oracle step on a row sample: forward, plus backward for training workloads."""
     import oracle
-    f64 = {k: v.to("cpu").double().numpy() for k, v in t.items() if k != "X"}
     A = (f64["Wg"], f64["Wu"]) if w.act == "swiglu" else f64["A"]
+    if w.bwd:
+        return oracle.mlp_bwd(X, A, f64["B"], dY, w.act)
+    return oracle.mlp_fwd(X, A, f64["B"], w.act)
+
+
+def oracle_row_sample(w, t, target_s):
+    """Times the fp64 oracle on a row sample sized for about target_s.
+
+    Rows are independent in the block (and the weight gradients are sums over
+    rows), so the sample's flops scale exactly with its row count.
+    Returns (rows, seconds, flops)."""
+    f64 = {k: v.to("cpu").double().numpy() for k, v in t.items() if k not in ("X", "dY")}
     rows = min(w.M, 32)
+    step_flops = w.fwd_flops() + (w.bwd_flops() if w.bwd else 0)
     while True:
         X = t["X"][:rows].double().numpy()
+        dY = t["dY"][:rows].double().numpy() if w.bwd else None
         t0 = time.perf_counter()
-        oracle.mlp_fwd(X, A, f64["B"], w.act)
+        oracle_step(w, f64, X, dY)
         dt = time.perf_counter() - t0
-        flops = w.fwd_flops() * rows / w.M
+        flops = step_flops * rows / w.M
         if dt >= 0.5 * target_s or rows >= w.M:
             return rows, dt, flops
         rows = int(min(w.M, max(rows * 2, rows * target_s / max(dt, 1e-3))))
@@ -174,7 +184,7 @@ def timeline_stats(records):
     for recs in calls.values():
         lo = min(r["start_ms"] for r in recs)
         hi = max(r["end_ms"] for r in recs)
-        ivs = sorted((r["start_ms"], r["end_ms"]) for r in recs if r["kind"] in ("gemm1", "gemm2"))
+        ivs = sorted((r["start_ms"], r["end_ms"]) for r in recs if r["kind"] != "shard_sum")
         busy, cur_s, cur_e = 0.0, None, None
         for s, e in ivs:
             if cur_e is None or s > cur_e:
@@ -206,13 +216,23 @@ def run_ours(args, w, rank, world, local_rank):
     X = t["X"].to(dev)
     Y = torch.empty((w.M, w.d), dtype=torch.bfloat16, device=dev)
     desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, args.schedule)
-    ws = torch.zeros(b.workspace_size(desc), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(b.workspace_size(desc, with_bwd=w.bwd), dtype=torch.uint8, device=dev)
+    if w.bwd:  # training step: forward keeping the pre-activations, then backward
+        dY = t["dY"].to(dev)
+        saved = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device=dev)
+        dX = torch.empty_like(X)
+        dA_sh = [torch.empty_like(a) for a in A_sh]
+        dB_sh = [torch.empty_like(x) for x in B_sh]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(timed=False, x=X):
+    def step(timed=False, x=X, dy=None):
         b.mlp_fwd(x, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices,
-                  schedule=args.schedule, Y=Y, workspace=ws, kernel_times=timed)
+                  schedule=args.schedule, Y=Y, workspace=ws, kernel_times=timed, saved=saved if w.bwd else None)
+        if w.bwd:
+            b.mlp_bwd(x, A_sh, B_sh, dY if dy is None else dy, saved, F=w.F, mu=w.mu, act=w.act,
+                      partial=w.partial, out_slices=w.slices, schedule=args.schedule, dX=dX, dA_shards=dA_sh,
+                      dB_shards=dB_sh, workspace=ws, kernel_times=timed)
 
     def barrier():
         torch.cuda.synchronize()
@@ -260,12 +280,21 @@ def run_ours(args, w, rank, world, local_rank):
     Xh = t["X"].pin_memory()
     Yh = torch.empty((w.M, w.d), dtype=torch.bfloat16).pin_memory()
     Xd = torch.empty_like(X)
+    if w.bwd:
+        dYh = t["dY"].pin_memory()
+        dXh = torch.empty((w.M, w.d), dtype=torch.bfloat16).pin_memory()
+        dYd = torch.empty_like(X)
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     for i in range(e2e_steps):
         flush.zero_()
         ev2[i][0].record(stream)
         Xd.copy_(Xh, non_blocking=True)
-        step(x=Xd)
+        if w.bwd:
+            dYd.copy_(dYh, non_blocking=True)
+            step(x=Xd, dy=dYd)
+            dXh.copy_(dX, non_blocking=True)
+        else:
+            step(x=Xd)
         Yh.copy_(Y, non_blocking=True)
         ev2[i][1].record(stream)
     barrier()
@@ -282,25 +311,35 @@ def run_ours(args, w, rank, world, local_rank):
 
     # ---- per-kernel durations from the live events of the timed region
     peaks, peak_src = load_peaks()
-    by_kind = {}
-    for r in records:
-        by_kind.setdefault(r["kind"], []).append(r["end_ms"] - r["start_ms"])
     nact = 2 if w.act == "swiglu" else 1
-    flops_per_launch = {
-        "gemm1": 2.0 * w.Mc * w.d * w.F * nact,
-        "gemm2": 2.0 * w.Mc * w.F * (w.d // w.slices),
-    }
+    ds_ = w.d // w.slices
+
+    def launch_flops(r):  # algorithmic GEMM flops of one launch (all shards)
+        return {"gemm1": 2.0 * w.Mc * w.d * w.F * nact, "gemm2": 2.0 * w.Mc * w.F * ds_,
+                "bwd_dh": 2.0 * w.Mc * w.d * w.F, "bwd_dx": 2.0 * w.Mc * nact * w.F * ds_,
+                "bwd_dw": 2.0 * w.M * w.d * w.F * (nact if r["slice"] == 0 else 1)}.get(r["kind"], 0.0)
+
     psize = 4 if w.partial == "f32" else 2
-    ss_bytes = (w.P * psize + 2) * w.Mc * (w.d // w.slices)
-    kinds = {k: {"launches": len(v), "avg_us": 1e3 * statistics.mean(v), "total_ms": sum(v)}
-             for k, v in by_kind.items()}
-    dominant = max((k for k in kinds if k.startswith("gemm")), key=lambda k: kinds[k]["total_ms"])
-    dom_tflops = flops_per_launch[dominant] / (kinds[dominant]["avg_us"] * 1e-6) / 1e12
+    ss_bytes = (w.P * psize + 2) * w.Mc * ds_
+    kinds = {}
+    for r in records:
+        k = kinds.setdefault(r["kind"], {"launches": 0, "total_ms": 0.0, "flops": 0.0})
+        k["launches"] += 1
+        k["total_ms"] += r["end_ms"] - r["start_ms"]
+        k["flops"] += launch_flops(r)
+    for k in kinds.values():
+        k["avg_us"] = 1e3 * k["total_ms"] / k["launches"]
+    dominant = max((k for k in kinds if k != "shard_sum"), key=lambda k: kinds[k]["total_ms"])
+    dom_tflops = kinds[dominant]["flops"] / (kinds[dominant]["total_ms"] * 1e-3) / 1e12
+    dom_flops_per_launch = kinds[dominant]["flops"] / kinds[dominant]["launches"]
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     ss_gbs = ss_bytes / (kinds["shard_sum"]["avg_us"] * 1e-6) / 1e9
     span_ms, exposed_ms = timeline_stats(records)
+    calls_per_step = 2 if w.bwd else 1
+    span_ms *= calls_per_step
+    exposed_ms *= calls_per_step
 
-    flops = w.fwd_flops()
+    flops = w.fwd_flops() + (w.bwd_flops() if w.bwd else 0)
     value = world * flops / (mean_ms * 1e-3) / 1e12
     line = {
         "metric": "sliced TP-MLP layer TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",
@@ -323,6 +362,7 @@ def run_ours(args, w, rank, world, local_rank):
         "exposed_reduce_frac": round(exposed_ms / span_ms, 4) if span_ms > 0 else None,
         "roofline": {
             "kernel": f"gemm_bf16_tcgen05 ({dominant})",
+            "note": "achieved = algorithmic flops of the kernel's launches / their summed event durations",
             "bound": "tensor",
             "achieved": round(dom_tflops, 2),
             "peak": peak_tf,
@@ -331,7 +371,7 @@ def run_ours(args, w, rank, world, local_rank):
             "peak_source": f"{peak_src} bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
             else f"{peak_src} bf16_tflops",
             "frac_of_burst": round(dom_tflops / float(peaks.get("bf16_tflops", peak_tf)), 4),
-            "flops_per_launch": flops_per_launch[dominant],
+            "flops_per_launch": dom_flops_per_launch,
             "traffic": ncu_traffic(dominant, w.name),
         },
         "shard_sum": {
@@ -344,11 +384,13 @@ def run_ours(args, w, rank, world, local_rank):
             "traffic": ncu_traffic("shard_sum", w.name),
         },
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
+                        "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["flops"] else None,
                         "share": round(v["total_ms"] / sum(x["total_ms"] for x in kinds.values()), 4)}
                     for k, v in kinds.items()},
         "gpu_launches": len(records),
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": w.M * w.d * 2, "d2h_bytes_per_step": w.M * w.d * 2,
+                "h2d_bytes_per_step": w.M * w.d * 2 * calls_per_step,
+                "d2h_bytes_per_step": w.M * w.d * 2 * calls_per_step,
                 "ms_per_step": round(e2e_ms, 4)},
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
@@ -357,7 +399,8 @@ def run_ours(args, w, rank, world, local_rank):
         rows, dt, fl = oracle_row_sample(w, t, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 5), "unit": "TFLOP/s", "cores": blas_threads(),
                                 "kind": "oracle",
-                                "sample": f"fp64 oracle forward on {rows} of {w.M} rows ({dt:.1f} s; rows are "
+                                "sample": f"fp64 oracle {'forward+backward' if w.bwd else 'forward'} on {rows} "
+                                          f"of {w.M} rows ({dt:.1f} s; rows are "
                                           f"independent, flops scale with rows)"}
     return line
 
@@ -371,21 +414,21 @@ def run_reference(args, w):
     t = wl.generate(w, seed=0)
     budget_s = 150.0
     rows, dt, _ = oracle_row_sample(w, t, target_s=min(5.0, budget_s / max(1, args.steps + args.warmup)))
-    import oracle
-    f64 = {k: v.double().numpy() for k, v in t.items() if k != "X"}
-    A = (f64["Wg"], f64["Wu"]) if w.act == "swiglu" else f64["A"]
+    f64 = {k: v.double().numpy() for k, v in t.items() if k not in ("X", "dY")}
     X = t["X"][:rows].double().numpy()
+    dY = t["dY"][:rows].double().numpy() if w.bwd else None
     for _ in range(args.warmup):
-        oracle.mlp_fwd(X, A, f64["B"], w.act)
+        oracle_step(w, f64, X, dY)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.mlp_fwd(X, A, f64["B"], w.act)
+        oracle_step(w, f64, X, dY)
         times.append(time.perf_counter() - t0)
     mean_s = statistics.mean(times)
-    flops = w.fwd_flops() * rows / w.M
+    flops = (w.fwd_flops() + (w.bwd_flops() if w.bwd else 0)) * rows / w.M
     value = flops / mean_s / 1e12
-    sample = f"fp64 oracle forward on {rows} of {w.M} rows per step"
+    what = "forward+backward" if w.bwd else "forward"
+    sample = f"fp64 oracle {what} on {rows} of {w.M} rows per step"
     return {
         "impl": "reference",
         "metric": "sliced TP-MLP layer TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",

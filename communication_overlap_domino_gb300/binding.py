@@ -207,6 +207,48 @@ def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, par
     return Y
 
 
+def mlp_bwd(X, A_shards: List, B_shards: List, dY, saved, *, F: int, mu: int, act: str, partial: str,
+            out_slices: int = 1, schedule: str = "streams", dX=None, dA_shards=None, dB_shards=None, workspace=None,
+            stream=None, kernel_times: bool = False, timeout_ns: int = 0):
+    """domino_mlp_bwd on torch tensors; returns (dX, dA_shards, dB_shards).
+
+    `saved` must be the buffer a domino_mlp_fwd call with the same inputs filled."""
+    torch = _torch()
+    M, d = X.shape
+    P = len(A_shards)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns)
+    if dX is None:
+        dX = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
+    if dA_shards is None:
+        dA_shards = [torch.empty_like(a) for a in A_shards]
+    if dB_shards is None:
+        dB_shards = [torch.empty_like(b) for b in B_shards]
+    if workspace is None:
+        workspace = _workspace(max(workspace_size(desc, with_bwd=True), 256), X.device)
+    st = lib().domino_mlp_bwd(
+        ctypes.byref(desc), X.data_ptr(), _ptr_array([a.data_ptr() for a in A_shards]),
+        _ptr_array([b.data_ptr() for b in B_shards]), dY.data_ptr(), saved.data_ptr(), dX.data_ptr(),
+        _ptr_array([a.data_ptr() for a in dA_shards]), _ptr_array([b.data_ptr() for b in dB_shards]),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "domino_mlp_bwd")
+    return dX, dA_shards, dB_shards
+
+
+def unshard_grads(dA_shards: List, dB_shards: List, act: str):
+    """Inverse of shard_weights for gradients: returns (dA or (dWg, dWu), dB) in
+    the mathematical layout ([d, F] and [F, d])."""
+    torch = _torch()
+    if act == "swiglu":
+        Fp = dA_shards[0].shape[0] // 2
+        dWg = torch.cat([a[:Fp].t() for a in dA_shards], dim=1)
+        dWu = torch.cat([a[Fp:].t() for a in dA_shards], dim=1)
+        dA = (dWg, dWu)
+    else:
+        dA = torch.cat([a.t() for a in dA_shards], dim=1)
+    dB = torch.cat([b.t() for b in dB_shards], dim=0)
+    return dA, dB
+
+
 def mlp_fwd_noalloc(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str,
                     out_slices: int = 1, Y=None, stream=None, timeout_ns: int = 0):
     """domino_mlp_fwd_noalloc: the forward pass with the library's own fixed scratch

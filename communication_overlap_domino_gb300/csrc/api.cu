@@ -149,8 +149,9 @@ domino_status_t check_desc(const domino_mlp_desc_t* desc, Shape* s) {
 }
 
 struct WsLayout {
-  size_t h_off, h_shard;  // hidden activations [P][M][Fp] bf16
-  size_t z_off, z_shard;  // partials [P][M][d]
+  size_t h_off, h_shard;    // hidden activations [P][M][Fp] bf16
+  size_t z_off, z_shard;    // partials [P][M][d]
+  size_t dg_off, dg_shard;  // backward: gradient of the pre-activations [P][M][nact*Fp] bf16
   size_t total;
 };
 
@@ -163,10 +164,9 @@ WsLayout ws_layout(const Shape& s, bool with_bwd) {
   L.z_shard = static_cast<size_t>(s.M) * s.d * s.psize;
   L.z_off = off;
   off = align_up(off + L.z_shard * s.P, 256);
-  if (with_bwd) {
-    // gradient of the hidden layer [P][M][nact*Fp] bf16
-    off = align_up(off + static_cast<size_t>(s.M) * s.Fp * s.nact * 2 * s.P, 256);
-  }
+  L.dg_shard = static_cast<size_t>(s.M) * s.Fp * s.nact * 2;
+  L.dg_off = off;
+  if (with_bwd) off = align_up(off + L.dg_shard * s.P, 256);
   L.total = off;
   return L;
 }
@@ -420,11 +420,189 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   Shape s;
   domino_status_t st = check_desc(desc, &s);
   if (st != DOMINO_OK) return st;
-  if (!X || !A_shards || !B_shards || !dY || !saved || !dX || !dA_shards || !dB_shards || !workspace)
-    return fail(DOMINO_ERR_INVALID_ARG, "NULL argument");
-  (void)workspace_bytes;
-  (void)stream;
-  return fail(DOMINO_ERR_UNSUPPORTED, "backward kernels are not built yet");
+  if (!A_shards || !B_shards || !dA_shards || !dB_shards)
+    return fail(DOMINO_ERR_INVALID_ARG, "A_shards, B_shards, dA_shards and dB_shards must be non-NULL");
+  for (int p = 0; p < s.P; ++p) {
+    if (!A_shards[p] || !B_shards[p] || !dA_shards[p] || !dB_shards[p])
+      return fail(DOMINO_ERR_INVALID_ARG, "NULL shard pointer");
+    if (!aligned16(A_shards[p]) || !aligned16(B_shards[p]) || !aligned16(dA_shards[p]) || !aligned16(dB_shards[p]))
+      return fail(DOMINO_ERR_ALIGNMENT, "shard pointers must be 16-byte aligned");
+  }
+  cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  if (s.M == 0) {
+    // gradients of a sum over no tokens: zero weight gradients, nothing else touched
+    for (int p = 0; p < s.P; ++p) {
+      cudaError_t e = cudaMemsetAsync(dA_shards[p], 0, static_cast<size_t>(s.nact) * s.Fp * s.d * 2, s0);
+      if (e == cudaSuccess) e = cudaMemsetAsync(dB_shards[p], 0, static_cast<size_t>(s.d) * s.Fp * 2, s0);
+      if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("memset: ") + cudaGetErrorString(e));
+    }
+    return DOMINO_OK;
+  }
+  if (!X || !dY || !saved || !dX || !workspace)
+    return fail(DOMINO_ERR_INVALID_ARG, "X, dY, saved, dX and workspace must be non-NULL");
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(saved) || !aligned16(dX) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(DOMINO_ERR_ALIGNMENT, "X, dY, saved, dX must be 16-byte and workspace 256-byte aligned");
+  const WsLayout W = ws_layout(s, true);
+  if (workspace_bytes < W.total)
+    return fail(DOMINO_ERR_WORKSPACE, "workspace smaller than domino_mlp_workspace_size(desc, 1)");
+
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != DOMINO_OK) return st;
+  cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
+  const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DeviceStatus* dstat = reinterpret_cast<DeviceStatus*>(ws);
+  Timer T;
+  T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
+  T.ds = ds;
+  if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
+
+  const int64_t nF = s.nact * s.Fp;  // columns of the pre-activation block / rows of A_shards[p]
+  const void* pre[kMaxShards];
+  const void* H[kMaxShards];
+  void* dG[kMaxShards];
+  void* Z[kMaxShards];
+  for (int p = 0; p < s.P; ++p) {
+    const uint8_t* blk = static_cast<const uint8_t*>(saved) + saved_shard_bytes(s) * p;
+    pre[p] = blk;
+    H[p] = blk + static_cast<size_t>(s.M) * nF * 2;
+    dG[p] = ws + W.dg_off + W.dg_shard * p;
+    Z[p] = ws + W.z_off + W.z_shard * p;
+  }
+  static const int kDgEpi[4] = {EPI_DG_GELU, EPI_DG_GELU_TANH, EPI_DG_SWIGLU, EPI_DG_IDENTITY};
+  std::string err;
+  if (sr != s0) {
+    cudaEventRecord(ds->ev_fork, s0);
+    cudaStreamWaitEvent(sr, ds->ev_fork, 0);
+  }
+  for (int k = 0; k < s.mu; ++k) {
+    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
+    // ---- dH_{k,p} = dY_k B_p^T with the activation derivative fused -> dG_{k,p}
+    {
+      GemmLaunch L;
+      L.epi = kDgEpi[s.act];
+      L.b_mn = true;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {dY, s.M, s.d, s.d};
+        L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};  // stored [d][Fp]: K = d rows, N = Fp contiguous
+        L.b1[p] = L.b0[p];
+        L.out[p] = dG[p];
+        L.aux[p] = const_cast<void*>(pre[p]);
+      }
+      L.ldo = nF;
+      L.ld_aux = nF;
+      L.aux_u_off = s.Fp;
+      L.out_u_off = s.Fp;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = 0;
+      L.n_end = static_cast<int32_t>(s.Fp);
+      L.K = s.d;
+      L.status = dstat;
+      L.timeout_ns = tmo;
+      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DH, k, 0, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      if (st != DOMINO_OK) return fail(st, err);
+    }
+    for (int sl = 0; sl < s.S; ++sl) {
+      const int32_t col0 = static_cast<int32_t>(sl * s.ds);
+      // ---- partial input gradient of shard p: dG_{k,p} A_p^T -> Z_p
+      GemmLaunch L;
+      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
+      L.b_mn = true;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {dG[p], s.M, nF, nF};
+        L.b0[p] = {A_shards[p], nF, s.d, s.d};  // stored [nF][d]: K = nF rows, N = d contiguous
+        L.b1[p] = L.b0[p];
+        L.out[p] = Z[p];
+      }
+      L.ldo = s.d;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = col0;
+      L.n_end = static_cast<int32_t>(col0 + s.ds);
+      L.K = nF;
+      L.status = dstat;
+      L.timeout_ns = tmo;
+      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      if (st != DOMINO_OK) return fail(st, err);
+      // ---- dX_k[:, s] = sum_p of the partials (the all-reduce of the input gradient)
+      if (sr != s0) {
+        cudaEvent_t ev = ds->ev_piece[k * s.S + sl];
+        cudaEventRecord(ev, s0);
+        cudaStreamWaitEvent(sr, ev, 0);
+      }
+      ShardSumParams q;
+      memset(&q, 0, sizeof q);
+      const size_t zoff = (static_cast<size_t>(row0) * s.d + col0) * s.psize;
+      for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
+      q.rows = s.Mc;
+      q.cols = s.ds;
+      q.ld_part = s.d;
+      q.ld_y = s.d;
+      q.y = static_cast<uint8_t*>(dX) + (static_cast<size_t>(row0) * s.d + col0) * 2;
+      q.P = s.P;
+      q.f32 = s.partial == DOMINO_PARTIAL_F32;
+      st = timed(T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
+                 [&] { return launch_shard_sum(q, ds->num_sms, sr, &err); });
+      if (st != DOMINO_OK) return fail(st, err);
+    }
+  }
+  // ---- weight gradients over all M (they run while the last shard-sum drains)
+  {
+    GemmLaunch L;  // dA_p = dG_p^T X : [nF, d], contraction over tokens
+    L.epi = EPI_Z_BF16;
+    L.a_mn = true;
+    L.b_mn = true;
+    L.num_shards = s.P;
+    for (int p = 0; p < s.P; ++p) {
+      L.a[p] = {dG[p], s.M, nF, nF};
+      L.b0[p] = {X, s.M, s.d, s.d};
+      L.b1[p] = L.b0[p];
+      L.out[p] = dA_shards[p];
+    }
+    L.ldo = s.d;
+    L.rows = static_cast<int32_t>(nF);
+    L.n_base = 0;
+    L.n_end = static_cast<int32_t>(s.d);
+    L.K = s.M;
+    L.status = dstat;
+    L.timeout_ns = tmo;
+    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+    if (st != DOMINO_OK) return fail(st, err);
+  }
+  {
+    GemmLaunch L;  // dB_p = dY^T H_p : [d, Fp]
+    L.epi = EPI_Z_BF16;
+    L.a_mn = true;
+    L.b_mn = true;
+    L.num_shards = s.P;
+    for (int p = 0; p < s.P; ++p) {
+      L.a[p] = {dY, s.M, s.d, s.d};
+      L.b0[p] = {H[p], s.M, s.Fp, s.Fp};
+      L.b1[p] = L.b0[p];
+      L.out[p] = dB_shards[p];
+    }
+    L.ldo = s.Fp;
+    L.rows = static_cast<int32_t>(s.d);
+    L.n_base = 0;
+    L.n_end = static_cast<int32_t>(s.Fp);
+    L.K = s.M;
+    L.status = dstat;
+    L.timeout_ns = tmo;
+    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+    if (st != DOMINO_OK) return fail(st, err);
+  }
+  if (sr != s0) {
+    cudaEventRecord(ds->ev_join, sr);
+    cudaStreamWaitEvent(s0, ds->ev_join, 0);
+  }
+  return DOMINO_OK;
 }
 
 domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t partial_dtype, int64_t rows,

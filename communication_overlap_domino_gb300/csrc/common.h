@@ -31,13 +31,17 @@ enum : uint32_t {
 
 // Epilogue of the tcgen05 GEMM: what is done with each fp32 accumulator tile.
 enum Epi : int {
-  EPI_H_GELU = 0,       // H = gelu(acc) -> bf16            (GEMM1, GeLU)
-  EPI_H_GELU_TANH = 1,  // H = gelu_tanh(acc) -> bf16
-  EPI_H_IDENTITY = 2,   // H = acc -> bf16
-  EPI_H_SWIGLU = 3,     // H = silu(acc[:, :128]) * acc[:, 128:] -> bf16 (gate | up in one N=256 tile)
-  EPI_Z_F32 = 4,        // partial Z = acc, fp32             (GEMM2)
-  EPI_Z_BF16 = 5,       // partial Z = acc -> bf16
-  EPI_COUNT = 6
+  EPI_H_GELU = 0,        // H = gelu(acc) -> bf16            (forward GEMM1, GeLU)
+  EPI_H_GELU_TANH = 1,   // H = gelu_tanh(acc) -> bf16
+  EPI_H_IDENTITY = 2,    // H = acc -> bf16
+  EPI_H_SWIGLU = 3,      // H = silu(acc[:, :128]) * acc[:, 128:] -> bf16 (gate | up in one N=256 tile)
+  EPI_Z_F32 = 4,         // C = acc, fp32                    (forward GEMM2 partials, backward dX partials)
+  EPI_Z_BF16 = 5,        // C = acc -> bf16                  (bf16 partials, weight gradients)
+  EPI_DG_GELU = 6,       // dG = acc * gelu'(g), g read from the saved pre-activations (backward dH GEMM)
+  EPI_DG_GELU_TANH = 7,  // dG = acc * gelu_tanh'(g)
+  EPI_DG_IDENTITY = 8,   // dG = acc
+  EPI_DG_SWIGLU = 9,     // dg = acc * u * silu'(g), du = acc * silu(g), written side by side
+  EPI_COUNT = 10
 };
 
 // GEMM tile shape: one CTA computes a 128 x 256 fp32 accumulator (tcgen05
@@ -53,16 +57,19 @@ constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*
 constexpr uint32_t kTmemCols = 2 * kBN;  // double-buffered accumulator
 
 // One grouped, persistent GEMM launch: C_s = A_s * B_s^T for every shard s,
-// A_s [rows, K] and B_s [N, K] bf16 K-major, through TMA tensor maps.
+// through TMA tensor maps.  A_s is [rows, K] and B_s [N, K]; each is read
+// K-major (K contiguous in memory, box 64 K x 128 rows) or MN-major (the
+// matrix is stored [K, rows] with rows contiguous, box 64 rows x 64 K).
 struct GemmParams {  // CUtensorMap members carry 64-byte alignment
-  CUtensorMap map_a[kMaxShards];   // A operand, box 64 x 128
-  CUtensorMap map_b0[kMaxShards];  // B operand rows [n0, n0+128), box 64 x 128
+  CUtensorMap map_a[kMaxShards];   // A operand
+  CUtensorMap map_b0[kMaxShards];  // B operand rows [n0, n0+128)
   CUtensorMap map_b1[kMaxShards];  // B operand rows for accumulator columns 128..255
   void* out[kMaxShards];           // output matrix per shard
   void* aux[kMaxShards];           // optional copy of the pre-activation(s) (bf16), or null
   int64_t ldo;                     // leading dimension of out (elements)
   int64_t ld_aux;                  // leading dimension of aux (elements)
   int64_t aux_u_off;               // SwiGLU: column offset of u inside aux
+  int64_t out_u_off;               // SwiGLU backward: column offset of du inside out
   int32_t a_row0;                  // first row of A read by tile row 0
   int32_t out_row0;                // first output row written by tile row 0
   int32_t rows;                    // valid rows (tile rows >= rows are not stored)

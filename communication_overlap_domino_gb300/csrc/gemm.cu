@@ -12,7 +12,11 @@
 //         fp32 or bf16, into that shard's own partial buffer -- the operand of
 //         the shard-sum that stands in for the tensor-parallel all-reduce
 //         (Domino page, Abstract: each piece's communication is issued as soon
-//         as the piece is computed).
+//         as the piece is computed);
+//   backward: dH = dY B^T with the activation derivative fused (reads the
+//         saved pre-activations), the partial input gradients dG A^T, and the
+//         weight gradients X^T dG, dY^T H.  These read operands MN-major
+//         (stored [K, rows]); the tensor core takes either major-ness.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over tiles):
 //   warp 0 lane 0: TMA producer     warp 1: TMEM allocator; lane 0 issues MMAs
@@ -40,6 +44,26 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
 }
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+// Derivatives for the backward epilogue (product and chain rules).
+__device__ __forceinline__ float gelu_erf_grad(float x) {
+  // d/dx [x Phi(x)] = Phi(x) + x phi(x)
+  return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * __expf(-0.5f * x * x);
+}
+__device__ __forceinline__ float gelu_tanh_grad(float x) {
+  const float k = 0.79788456080286536f;
+  const float t = tanhf(k * (x + 0.044715f * x * x * x));
+  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
+}
+
+template <int EPI>
+__device__ __forceinline__ float activate_grad(float x) {
+  if constexpr (EPI == EPI_DG_GELU) return gelu_erf_grad(x);
+  else if constexpr (EPI == EPI_DG_GELU_TANH) return gelu_tanh_grad(x);
+  else return 1.0f;
+}
+
+__host__ __device__ constexpr bool is_dg(int epi) { return epi >= EPI_DG_GELU && epi <= EPI_DG_SWIGLU; }
 
 template <int EPI>
 __device__ __forceinline__ float activate(float x) {
@@ -70,6 +94,26 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (j < n) dst[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+// Loads n <= 32 bf16 values from src (16-byte aligned when n == 32) as floats.
+__device__ __forceinline__ void load_row_bf16(const __nv_bfloat16* src, float (&v)[32], int n) {
+  if (n >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = s4[q];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
+        v[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < n ? __bfloat162float(src[j]) : 0.0f;
   }
 }
 
@@ -126,6 +170,32 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc
           store_row_bf16(a + p.aux_u_off, u, n);
         }
       }
+    } else if constexpr (is_dg(EPI)) {
+      tmem_ld_wait();
+      if (row_ok) {
+        const __nv_bfloat16* pre = static_cast<const __nv_bfloat16*>(p.aux[shard]) + orow * p.ld_aux + col;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col;
+        float g[32];
+        load_row_bf16(pre, g, n);
+        if constexpr (EPI == EPI_DG_SWIGLU) {
+          float u[32], dg[32], du[32];
+          load_row_bf16(pre + p.aux_u_off, u, n);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float dh = __uint_as_float(r0[j]);
+            const float sg = 1.0f / (1.0f + __expf(-g[j]));
+            du[j] = dh * g[j] * sg;                               // dH * silu(g)
+            dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
+          }
+          store_row_bf16(dst, dg, n);
+          store_row_bf16(dst + p.out_u_off, du, n);
+        } else {
+          float dgv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dgv[j] = __uint_as_float(r0[j]) * activate_grad<EPI>(g[j]);
+          store_row_bf16(dst, dgv, n);
+        }
+      }
     } else {
       tmem_ld_wait();
       if (row_ok) {
@@ -159,7 +229,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& sha
 
 // ------------------------------------------------------------------- kernel
 
-template <int EPI>
+template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -227,10 +297,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
         uint8_t* sa = smem_a + stage * kAStageBytes;
         uint8_t* sb = smem_b + stage * kBStageBytes;
         mbar_arrive_expect_tx(&full_bar[stage], kAStageBytes + kBStageBytes);
-        const int x = kb * kBK;
-        tma_load_2d(sa, &p.map_a[shard], &full_bar[stage], x, ya);
-        tma_load_2d(sb, &p.map_b0[shard], &full_bar[stage], x, yb0);
-        tma_load_2d(sb + kBStageBytes / 2, &p.map_b1[shard], &full_bar[stage], x, yb1);
+        const int k0 = kb * kBK;
+        if constexpr (A_MN) {
+          // two boxes of 64 rows x 64 K (MN innermost), 8 KB apart
+          tma_load_2d(sa, &p.map_a[shard], &full_bar[stage], ya, k0);
+          tma_load_2d(sa + 8192, &p.map_a[shard], &full_bar[stage], ya + 64, k0);
+        } else {
+          tma_load_2d(sa, &p.map_a[shard], &full_bar[stage], k0, ya);
+        }
+        if constexpr (B_MN) {
+          tma_load_2d(sb, &p.map_b0[shard], &full_bar[stage], yb0, k0);
+          tma_load_2d(sb + 8192, &p.map_b0[shard], &full_bar[stage], yb0 + 64, k0);
+          tma_load_2d(sb + 16384, &p.map_b1[shard], &full_bar[stage], yb1, k0);
+          tma_load_2d(sb + 24576, &p.map_b1[shard], &full_bar[stage], yb1 + 64, k0);
+        } else {
+          tma_load_2d(sb, &p.map_b0[shard], &full_bar[stage], k0, yb0);
+          tma_load_2d(sb + kBStageBytes / 2, &p.map_b1[shard], &full_bar[stage], k0, yb1);
+        }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -249,7 +332,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
+    // K advance per MMA (16 bf16), in the descriptor's (address >> 4) units:
+    // K-major: 32 bytes along a 128-byte row; MN-major: 16 K-rows of 128 bytes.
+    constexpr uint64_t kAdvA = A_MN ? (2048 >> 4) : (32 >> 4);
+    constexpr uint64_t kAdvB = B_MN ? (2048 >> 4) : (32 >> 4);
     uint32_t stage = 0, phase = 0;
     int i = 0;
     for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++i) {
@@ -265,13 +352,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
           break;
         }
         tc_fence_after_sync();
-        const uint64_t adesc = smem_desc_k128(smem_u32(smem_a + stage * kAStageBytes));
-        const uint64_t bdesc = smem_desc_k128(smem_u32(smem_b + stage * kBStageBytes));
+        const uint32_t sa = smem_u32(smem_a + stage * kAStageBytes);
+        const uint32_t sb = smem_u32(smem_b + stage * kBStageBytes);
+        const uint64_t adesc = A_MN ? smem_desc_mn128(sa) : smem_desc_k128(sa);
+        const uint64_t bdesc = B_MN ? smem_desc_mn128(sb) : smem_desc_k128(sb);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          // advancing K by 16 bf16 = 32 bytes = 2 in the (address >> 4) field
-          mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < kBK / 16; ++k)
+          mma_bf16_ss(d_tmem, adesc + kAdvA * k, bdesc + kAdvB * k, idesc, (kb | k) != 0 ? 1u : 0u);
         mma_commit(&empty_bar[stage]);
         if (++stage == kStages) {
           stage = 0;
@@ -336,31 +423,57 @@ EncodeTiledFn get_encode_fn(std::string* err) {
   return fn;
 }
 
-template <int EPI>
+template <int EPI, bool A_MN, bool B_MN>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&gemm_bf16_tcgen05_kernel<EPI>);
+  return reinterpret_cast<void*>(&gemm_bf16_tcgen05_kernel<EPI, A_MN, B_MN>);
 }
 
-void* kernel_for(int epi) {
-  switch (epi) {
-    case EPI_H_GELU: return kernel_ptr<EPI_H_GELU>();
-    case EPI_H_GELU_TANH: return kernel_ptr<EPI_H_GELU_TANH>();
-    case EPI_H_IDENTITY: return kernel_ptr<EPI_H_IDENTITY>();
-    case EPI_H_SWIGLU: return kernel_ptr<EPI_H_SWIGLU>();
-    case EPI_Z_F32: return kernel_ptr<EPI_Z_F32>();
-    case EPI_Z_BF16: return kernel_ptr<EPI_Z_BF16>();
-    default: return nullptr;
-  }
+// The instantiations the library uses: forward (K-major x K-major), backward
+// dH and dX (K-major A, MN-major B), weight gradients (MN-major x MN-major).
+struct KernelEntry {
+  int epi;
+  bool a_mn, b_mn;
+  void* fn;
+};
+
+const KernelEntry* kernel_table(int* n) {
+  static const KernelEntry table[] = {
+      {EPI_H_GELU, false, false, kernel_ptr<EPI_H_GELU, false, false>()},
+      {EPI_H_GELU_TANH, false, false, kernel_ptr<EPI_H_GELU_TANH, false, false>()},
+      {EPI_H_IDENTITY, false, false, kernel_ptr<EPI_H_IDENTITY, false, false>()},
+      {EPI_H_SWIGLU, false, false, kernel_ptr<EPI_H_SWIGLU, false, false>()},
+      {EPI_Z_F32, false, false, kernel_ptr<EPI_Z_F32, false, false>()},
+      {EPI_Z_BF16, false, false, kernel_ptr<EPI_Z_BF16, false, false>()},
+      {EPI_DG_GELU, false, true, kernel_ptr<EPI_DG_GELU, false, true>()},
+      {EPI_DG_GELU_TANH, false, true, kernel_ptr<EPI_DG_GELU_TANH, false, true>()},
+      {EPI_DG_IDENTITY, false, true, kernel_ptr<EPI_DG_IDENTITY, false, true>()},
+      {EPI_DG_SWIGLU, false, true, kernel_ptr<EPI_DG_SWIGLU, false, true>()},
+      {EPI_Z_F32, false, true, kernel_ptr<EPI_Z_F32, false, true>()},
+      {EPI_Z_BF16, false, true, kernel_ptr<EPI_Z_BF16, false, true>()},
+      {EPI_Z_BF16, true, true, kernel_ptr<EPI_Z_BF16, true, true>()},
+  };
+  *n = static_cast<int>(sizeof(table) / sizeof(table[0]));
+  return table;
+}
+
+void* kernel_for(int epi, bool a_mn, bool b_mn) {
+  int n = 0;
+  const KernelEntry* t = kernel_table(&n);
+  for (int i = 0; i < n; ++i)
+    if (t[i].epi == epi && t[i].a_mn == a_mn && t[i].b_mn == b_mn) return t[i].fn;
+  return nullptr;
 }
 
 }  // namespace
 
-bool encode_bf16_kmajor(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err) {
+// TMA map of a bf16 row-major matrix with the 128-byte swizzle: box of 64
+// innermost elements (one 128-byte row) x box_rows rows; zero fill outside.
+bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err) {
   EncodeTiledFn enc = get_encode_fn(err);
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.ld) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(64), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -378,8 +491,10 @@ bool encode_bf16_kmajor(CUtensorMap* map, const Operand2D& op, int box_rows, std
 }
 
 cudaError_t prepare_gemm_kernels() {
-  for (int e = 0; e < EPI_COUNT; ++e) {
-    cudaError_t st = cudaFuncSetAttribute(kernel_for(e), cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  int n = 0;
+  const KernelEntry* t = kernel_table(&n);
+  for (int i = 0; i < n; ++i) {
+    cudaError_t st = cudaFuncSetAttribute(t[i].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (st != cudaSuccess) return st;
   }
   return cudaSuccess;
@@ -392,16 +507,19 @@ domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stre
     if (err) *err = "launch_gemm: bad shard count";
     return DOMINO_ERR_INVALID_ARG;
   }
+  const int a_box = L.a_mn ? kBK : kBM;     // MN-major: 64 x 64 boxes; K-major: 64 x 128
+  const int b_box = L.b_mn ? kBK : kBN / 2;
   for (int s = 0; s < L.num_shards; ++s) {
-    if (!encode_bf16_kmajor(&p.map_a[s], L.a[s], kBM, err)) return DOMINO_ERR_CUDA;
-    if (!encode_bf16_kmajor(&p.map_b0[s], L.b0[s], kBN / 2, err)) return DOMINO_ERR_CUDA;
-    if (!encode_bf16_kmajor(&p.map_b1[s], L.b1[s], kBN / 2, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&p.map_a[s], L.a[s], a_box, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&p.map_b0[s], L.b0[s], b_box, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&p.map_b1[s], L.b1[s], b_box, err)) return DOMINO_ERR_CUDA;
     p.out[s] = L.out[s];
     p.aux[s] = L.aux[s];
   }
   p.ldo = L.ldo;
   p.ld_aux = L.ld_aux;
   p.aux_u_off = L.aux_u_off;
+  p.out_u_off = L.out_u_off;
   p.a_row0 = L.a_row0;
   p.out_row0 = L.out_row0;
   p.rows = L.rows;
@@ -418,9 +536,9 @@ domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stre
   p.timeout_ns = L.timeout_ns;
   if (p.num_tiles == 0) return DOMINO_OK;
   const int grid = p.num_tiles < max_ctas ? p.num_tiles : max_ctas;
-  void* fn = kernel_for(L.epi);
+  void* fn = kernel_for(L.epi, L.a_mn, L.b_mn);
   if (!fn) {
-    if (err) *err = "launch_gemm: bad epilogue";
+    if (err) *err = "launch_gemm: no kernel for this epilogue and operand layout";
     return DOMINO_ERR_INVALID_ARG;
   }
   void* args[] = {&p};

@@ -8,7 +8,9 @@
 
 namespace domino {
 
-// A bf16 row-major matrix [rows, cols] with leading dimension ld (elements).
+// A bf16 row-major matrix [rows, cols] with leading dimension ld (elements), as
+// stored in memory.  For a K-major operand rows = the operand's M (or N) extent
+// and cols = K; for an MN-major operand rows = K and cols = the M (or N) extent.
 struct Operand2D {
   const void* base = nullptr;
   int64_t rows = 0;
@@ -17,18 +19,21 @@ struct Operand2D {
 };
 
 // One grouped GEMM launch: for every shard s, out_s = epi(A_s B_s^T), where
-// A_s = a[s] rows [a_row0, a_row0 + rows), B_s = rows [n_base + nb*n_tile, ...)
-// of b0[s] (accumulator columns 0..127) and b1[s] (columns 128..255, at row
-// offset b1_off from the b0 box), contraction length K.
+// A_s = operand rows [a_row0, a_row0 + rows) of a[s], B_s = operand rows
+// [n_base + nb*n_tile, ...) of b0[s] (accumulator columns 0..127) and b1[s]
+// (columns 128..255, at operand-row offset b1_off from the b0 box), contraction
+// length K.  a_mn / b_mn select MN-major storage of A / B.
 struct GemmLaunch {
   int epi = 0;
+  bool a_mn = false;
+  bool b_mn = false;
   int num_shards = 0;
   Operand2D a[kMaxShards];
   Operand2D b0[kMaxShards];
   Operand2D b1[kMaxShards];
   void* out[kMaxShards] = {};
   void* aux[kMaxShards] = {};
-  int64_t ldo = 0, ld_aux = 0, aux_u_off = 0;
+  int64_t ldo = 0, ld_aux = 0, aux_u_off = 0, out_u_off = 0;
   int32_t a_row0 = 0, out_row0 = 0, rows = 0;
   int32_t n_base = 0, n_end = 0, n_tile = kBN, b1_off = kBN / 2;
   int64_t K = 0;

@@ -200,12 +200,28 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
   return desc;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// shape M x N (M in {64,128}, N a multiple of 16 up to 256).
+// Shared-memory matrix descriptor for an MN-major operand tile written by TMA
+// boxes of 64 MN-elements (128 bytes, 128-byte swizzle) x 64 K-rows: within a
+// box, K-row r sits at r * 128 bytes, so groups of 8 K-rows (one swizzle atom)
+// are 1024 bytes apart (stride-dimension offset); boxes for consecutive
+// 64-element MN blocks are 8192 bytes apart (leading-dimension offset).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  desc |= static_cast<uint64_t>(8192u >> 4) << 16;
+  desc |= static_cast<uint64_t>(1024u >> 4) << 32;
+  desc |= static_cast<uint64_t>(1u) << 46;
+  desc |= static_cast<uint64_t>(2u) << 61;
+  return desc;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, shape M x N
+// (M in {64,128}, N a multiple of 16 up to 256).
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16)
-//   bit 15/16 A/B major (0 = K-major); bits 17-22 N >> 3; bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+//   bit 15/16 A/B major (0 = K-major, 1 = MN-major); bits 17-22 N >> 3; bits 24-28 M >> 4
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace domino

@@ -142,11 +142,20 @@ DOMINO_API domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const v
                                const void* const* B_shards, void* Y, void* saved, void* workspace,
                                size_t workspace_bytes, void* stream);
 
-/* Backward pass of the same block (chain rule), sliced the same way:
- * dY [M,d] in; dX [M,d] out (sum over shards of each shard's partial input
- * gradient, via the shard-sum); dA_shards[p] / dB_shards[p] out, in the same
- * layouts as A_shards[p] / B_shards[p].  `saved` must hold what fwd wrote.
- * Returns DOMINO_ERR_UNSUPPORTED while the backward kernels are not built. */
+/* Backward pass of the same block (chain rule), sliced the same way.
+ * dY [M,d] in; dX [M,d] out; dA_shards[p] / dB_shards[p] out (bf16, the same
+ * layouts as A_shards[p] / B_shards[p]).  `saved` must hold what domino_mlp_fwd
+ * wrote for the same X and weights.  workspace: domino_mlp_workspace_size(desc, 1)
+ * bytes.  Steps per chunk k (and slice s):
+ *   dH_{k,p} = dY_k B_p^T, with the activation derivative fused into the
+ *     epilogue: dG = dH * act'(g) (SwiGLU: dg = dH * u * silu'(g),
+ *     du = dH * silu(g)), from the saved pre-activations;
+ *   the partial input gradient of shard p, dG_{k,p} A_p^T, into shard p's partial
+ *     buffer, then dX_k[:, s] = sum over p of the partials (the shard-sum, in fp32,
+ *     shard order; it overlaps the next chunk's GEMMs);
+ * then, over all M: dA_p = dG_p^T X and dB_p = dY^T H_p (they overlap the last
+ * chunk's shard-sum).  M == 0 writes zero weight gradients and touches nothing
+ * else (X, dY, saved, dX and workspace may then be NULL). */
 DOMINO_API domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
                                const void* const* B_shards, const void* dY, const void* saved, void* dX,
                                void* const* dA_shards, void* const* dB_shards, void* workspace,

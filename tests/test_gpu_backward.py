@@ -1,0 +1,120 @@
+"""Backward pass of the sliced MLP vs the fp64 oracle, through the C ABI (GB300).
+
+Bar per output tensor (dX, dA or dWg/dWu, dB): max|g - g_ref| / max|g_ref| <= 1e-2.
+Small problems are compared in full.  At full size (the Llama-style fwd+bwd
+workload) dX is checked on rows sampled from every chunk (rows of dX depend only
+on the same rows of X and dY), and the weight gradients on sampled hidden units:
+the columns of dWg, dWu and the rows of dWd that belong to a set of hidden units
+depend only on those units' weights, so the oracle computes them exactly from the
+column-restricted problem.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from communication_overlap_domino_gb300 import binding as b
+from communication_overlap_domino_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _run_fwd_bwd(w, t, schedule="streams"):
+    dev = torch.device("cuda:0")
+    A = (t["Wg"].to(dev), t["Wu"].to(dev)) if w.act == "swiglu" else t["A"].to(dev)
+    A_sh, B_sh = b.shard_weights(A, t["B"].to(dev), w.P)
+    X, dY = t["X"].to(dev), t["dY"].to(dev)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, schedule)
+    saved = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(b.workspace_size(desc, with_bwd=True), dtype=torch.uint8, device=dev)
+    Y = b.mlp_fwd(X, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices,
+                  schedule=schedule, saved=saved, workspace=ws)
+    dX, dA_sh, dB_sh = b.mlp_bwd(X, A_sh, B_sh, dY, saved, F=w.F, mu=w.mu, act=w.act, partial=w.partial,
+                                 out_slices=w.slices, schedule=schedule, workspace=ws)
+    assert b.query_device_status(ws) == 0
+    dA, dB = b.unshard_grads(dA_sh, dB_sh, w.act)
+    return Y, dX, dA, dB
+
+
+def _f64(t):
+    return t.double().cpu().numpy()
+
+
+def _check_full(w, seed, schedule="streams"):
+    t = wl.generate(w, seed, with_dy=True)
+    Y, dX, dA, dB = _run_fwd_bwd(w, t, schedule)
+    f = wl.to_float64(t)
+    A = (f["Wg"], f["Wu"]) if w.act == "swiglu" else f["A"]
+    ref = oracle.mlp_bwd(f["X"], A, f["B"], f["dY"], w.act)
+    errs = {"Y": oracle.max_rel_err(_f64(Y), oracle.mlp_fwd(f["X"], A, f["B"], w.act)),
+            "dX": oracle.max_rel_err(_f64(dX), ref["dX"]),
+            "dB": oracle.max_rel_err(_f64(dB), ref["dB"])}
+    if w.act == "swiglu":
+        errs["dWg"] = oracle.max_rel_err(_f64(dA[0]), ref["dWg"])
+        errs["dWu"] = oracle.max_rel_err(_f64(dA[1]), ref["dWu"])
+    else:
+        errs["dA"] = oracle.max_rel_err(_f64(dA), ref["dA"])
+    bad = {k: v for k, v in errs.items() if not v <= TOL}
+    assert not bad, f"{w.name}: {errs}"
+    return errs
+
+
+def test_tiny_backward():
+    _check_full(wl.WORKLOADS["tiny_gelu_fwd"].with_(bwd=True), seed=0)
+
+
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "identity"])
+def test_backward_ragged(act):
+    w = wl.Workload("ragged_bwd", M=600, d=336, F=984, P=3, mu=3, act=act, partial="f32", slices=2, bwd=True)
+    _check_full(w, seed=8)
+
+
+def test_backward_llama_tail_bf16_partials():
+    w = wl.Workload("llama_tail_bwd", M=512, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
+    _check_full(w, seed=9, schedule="serial")
+
+
+def test_backward_empty_batch_zeroes_weight_grads():
+    w = wl.Workload("empty_bwd", M=1, d=512, F=1024, P=2, mu=1, act="swiglu", partial="bf16", bwd=True)
+    t = wl.generate(w, 0, with_dy=True)
+    A_sh, B_sh = b.shard_weights((t["Wg"].cuda(), t["Wu"].cuda()), t["B"].cuda(), w.P)
+    dA = [torch.full_like(a, 5.0) for a in A_sh]
+    dB = [torch.full_like(x, 5.0) for x in B_sh]
+    X = t["X"].cuda()[:0]
+    b.mlp_bwd(X, A_sh, B_sh, X, X, F=w.F, mu=1, act="swiglu", partial="bf16", dX=X, dA_shards=dA, dB_shards=dB)
+    torch.cuda.synchronize()
+    assert all(torch.all(a == 0) for a in dA) and all(torch.all(x == 0) for x in dB)
+
+
+def test_llama_fwdbwd_full_size_sampled():
+    w = wl.WORKLOADS["llama_swiglu_fwdbwd"]
+    t = wl.generate(w, 0, with_dy=True)
+    Y, dX, dA, dB = _run_fwd_bwd(w, t)
+    rng = np.random.default_rng(0)
+    rows = sorted(set(int(r) for k in range(w.mu) for r in
+                      [k * w.Mc, k * w.Mc + w.Mc - 1, *(k * w.Mc + rng.integers(0, w.Mc, 4))]))
+    Xr = t["X"][rows].double().numpy()
+    dYr = t["dY"][rows].double().numpy()
+    Wg, Wu, Wd = (t[k].double().numpy() for k in ("Wg", "Wu", "B"))
+    ref_rows = oracle.mlp_bwd(Xr, (Wg, Wu), Wd, dYr, "swiglu")
+    assert oracle.max_rel_err(_f64(dX[rows]), ref_rows["dX"]) <= TOL
+    assert oracle.max_rel_err(_f64(Y[rows]), oracle.mlp_fwd(Xr, (Wg, Wu), Wd, "swiglu")) <= TOL
+    # hidden units from every shard, including each shard's last unit (the N and K tails)
+    units = sorted(set([p * w.Fp + j for p in range(w.P) for j in (0, w.Fp - 1)] +
+                       [int(u) for u in rng.integers(0, w.F, 8)]))
+    ref_cols = oracle.mlp_bwd(t["X"].double().numpy(), (Wg[:, units], Wu[:, units]), Wd[units],
+                              t["dY"].double().numpy(), "swiglu")
+    assert oracle.max_rel_err(_f64(dA[0][:, units]), ref_cols["dWg"]) <= TOL
+    assert oracle.max_rel_err(_f64(dA[1][:, units]), ref_cols["dWu"]) <= TOL
+    assert oracle.max_rel_err(_f64(dB[units]), ref_cols["dB"]) <= TOL
+    for g in (dX, dA[0], dA[1], dB):
+        assert torch.isfinite(g).all()
