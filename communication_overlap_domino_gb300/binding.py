@@ -19,8 +19,8 @@ STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTE
           4: "DOMINO_ERR_WORKSPACE", 5: "DOMINO_ERR_CUDA", 6: "DOMINO_ERR_TIMEOUT", 7: "DOMINO_ERR_DEVICE"}
 ACT = {"gelu": 0, "gelu_tanh": 1, "swiglu": 2, "identity": 3}
 PARTIAL = {"f32": 0, "bf16": 1}
-SCHEDULE = {"serial": 0, "streams": 1}
-KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw"}
+SCHEDULE = {"serial": 0, "streams": 1, "fused": 2}
+KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused"}
 FLAG_KERNEL_TIMES = 1
 MAX_SHARDS = 16
 
@@ -46,6 +46,10 @@ class MlpDesc(ctypes.Structure):
         ("reserved", ctypes.c_uint32),
         ("timeout_ns", ctypes.c_uint64),
     ]
+
+
+class Timeline(ctypes.Structure):
+    _fields_ = [("start_ns", ctypes.c_uint64), ("gemm_end_ns", ctypes.c_uint64), ("reduce_end_ns", ctypes.c_uint64)]
 
 
 class KernelTime(ctypes.Structure):
@@ -74,6 +78,8 @@ SIGNATURES = [
     ("domino_shard_sum", ctypes.c_int,
      [_VPP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int64, _VP]),
     ("domino_query_device_status", ctypes.c_int, [_VP, _VP]),
+    ("domino_read_timeline", ctypes.c_int, [_VP, _VP, ctypes.POINTER(Timeline)]),
+    ("domino_selftest_wait_timeout", ctypes.c_int, [_VP, ctypes.c_uint64, _VP]),
     ("domino_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("domino_last_error", ctypes.c_char_p, []),
     ("domino_mlp_fwd_noalloc", ctypes.c_int, [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP]),
@@ -277,6 +283,20 @@ def shard_sum(partials: List, Y, *, stream=None):
                                 partials[0].stride(0), Y.data_ptr(), Y.stride(0), _stream_handle(stream))
     _check(st, "domino_shard_sum")
     return Y
+
+
+def read_timeline(workspace, stream=None) -> dict:
+    """domino_read_timeline: device timeline (ns) of the last fused forward call on this workspace."""
+    tl = Timeline()
+    _check(lib().domino_read_timeline(workspace.data_ptr(), _stream_handle(stream), ctypes.byref(tl)),
+           "domino_read_timeline")
+    return {"start_ns": tl.start_ns, "gemm_end_ns": tl.gemm_end_ns, "reduce_end_ns": tl.reduce_end_ns}
+
+
+def selftest_wait_timeout(workspace, timeout_ns: int, stream=None) -> None:
+    """Launches a kernel whose bounded wait runs out (a flag nothing sets)."""
+    _check(lib().domino_selftest_wait_timeout(workspace.data_ptr(), timeout_ns, _stream_handle(stream)),
+           "domino_selftest_wait_timeout")
 
 
 def query_device_status(workspace, stream=None) -> int:

@@ -50,6 +50,7 @@ struct TimedLaunch {
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  int fused_max_ctas = 0;  // co-resident CTAs of the fused kernel (cooperative launch limit)
   cudaStream_t reduce_stream = nullptr;
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join = nullptr;
@@ -86,6 +87,9 @@ domino_status_t device_state(DeviceState** out) {
     }
     e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = prepare_gemm_kernels();
+    int per_sm = 0;
+    if (e == cudaSuccess) e = prepare_fused_kernels(&per_sm);
+    ds.fused_max_ctas = per_sm * ds.num_sms;
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ds.reduce_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_join, cudaEventDisableTiming);
@@ -117,7 +121,8 @@ domino_status_t check_desc(const domino_mlp_desc_t* desc, Shape* s) {
   if (d.act < DOMINO_ACT_GELU || d.act > DOMINO_ACT_IDENTITY) return fail(DOMINO_ERR_INVALID_ARG, "unknown act");
   if (d.partial_dtype != DOMINO_PARTIAL_F32 && d.partial_dtype != DOMINO_PARTIAL_BF16)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown partial_dtype");
-  if (d.schedule != DOMINO_SCHEDULE_SERIAL && d.schedule != DOMINO_SCHEDULE_STREAMS)
+  if (d.schedule != DOMINO_SCHEDULE_SERIAL && d.schedule != DOMINO_SCHEDULE_STREAMS &&
+      d.schedule != DOMINO_SCHEDULE_FUSED)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
   if (d.reserved != 0) return fail(DOMINO_ERR_INVALID_ARG, "reserved must be 0");
   if ((d.flags & ~DOMINO_FLAG_KERNEL_TIMES) != 0) return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
@@ -152,8 +157,11 @@ struct WsLayout {
   size_t h_off, h_shard;    // hidden activations [P][M][Fp] bf16
   size_t z_off, z_shard;    // partials [P][M][d]
   size_t dg_off, dg_shard;  // backward: gradient of the pre-activations [P][M][nact*Fp] bf16
+  size_t sync_off, sync_bytes;  // fused schedule: tile counters
   size_t total;
 };
+
+constexpr size_t kTimelineOff = 64;  // header offset of the fused kernel's 3 timeline words
 
 WsLayout ws_layout(const Shape& s, bool with_bwd) {
   WsLayout L;
@@ -164,6 +172,9 @@ WsLayout ws_layout(const Shape& s, bool with_bwd) {
   L.z_shard = static_cast<size_t>(s.M) * s.d * s.psize;
   L.z_off = off;
   off = align_up(off + L.z_shard * s.P, 256);
+  L.sync_bytes = fused_sync_bytes(s.Mc, s.d, s.P, s.mu);
+  L.sync_off = off;
+  off = align_up(off + L.sync_bytes, 256);
   L.dg_shard = static_cast<size_t>(s.M) * s.Fp * s.nact * 2;
   L.dg_off = off;
   if (with_bwd) off = align_up(off + L.dg_shard * s.P, 256);
@@ -316,6 +327,39 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
   const bool swiglu = s.act == DOMINO_ACT_SWIGLU;
   std::string err;
 
+  if (s.schedule == DOMINO_SCHEDULE_FUSED) {
+    if (ds->fused_max_ctas < 1) return fail(DOMINO_ERR_DEVICE, "fused kernel cannot be resident on this device");
+    FusedLaunch F;
+    F.X = X;
+    for (int p = 0; p < s.P; ++p) {
+      F.A_shards[p] = A_shards[p];
+      F.B_shards[p] = B_shards[p];
+      F.H[p] = H[p];
+      F.aux[p] = pre[p];
+      F.Z[p] = Z[p];
+    }
+    F.Y = Y;
+    F.sync = reinterpret_cast<uint32_t*>(ws + W.sync_off);
+    F.timeline = reinterpret_cast<uint64_t*>(ws + kTimelineOff);
+    F.M = s.M;
+    F.d = s.d;
+    F.Fp = s.Fp;
+    F.mu = s.mu;
+    F.P = s.P;
+    F.epi_a = kEpiOfAct[s.act];
+    F.partial_f32 = s.partial == DOMINO_PARTIAL_F32;
+    F.status = dstat;
+    F.timeout_ns = tmo;
+    cudaError_t e = cudaMemsetAsync(F.sync, 0, W.sync_bytes, s0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(F.timeline, 0xFF, 8, s0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(F.timeline + 1, 0, 16, s0);
+    if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("counter reset: ") + cudaGetErrorString(e));
+    st = timed(T, s0, 0, DOMINO_KERNEL_FUSED, 0, 0,
+               [&] { return launch_fused_fwd(F, ds->fused_max_ctas, s0, &err); });
+    if (st != DOMINO_OK) return fail(st, err);
+    return DOMINO_OK;
+  }
+
   if (sr != s0) {
     cudaEventRecord(ds->ev_fork, s0);
     cudaStreamWaitEvent(sr, ds->ev_fork, 0);
@@ -450,7 +494,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != DOMINO_OK) return st;
-  cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
+  cudaStream_t sr = s.schedule != DOMINO_SCHEDULE_SERIAL ? ds->reduce_stream : s0;  // FUSED: streams for the backward
   const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DeviceStatus* dstat = reinterpret_cast<DeviceStatus*>(ws);
@@ -637,6 +681,28 @@ domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t
   std::string err;
   st = launch_shard_sum(q, ds->num_sms, static_cast<cudaStream_t>(stream), &err);
   if (st != DOMINO_OK) return fail(st, err);
+  return DOMINO_OK;
+}
+
+domino_status_t domino_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream) {
+  if (!workspace) return fail(DOMINO_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(DOMINO_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DeviceState* ds = nullptr;
+  domino_status_t st = device_state(&ds);
+  if (st != DOMINO_OK) return st;
+  std::string err;
+  st = launch_selftest_wait(workspace, timeout_ns, static_cast<cudaStream_t>(stream), &err);
+  if (st != DOMINO_OK) return fail(st, err);
+  return DOMINO_OK;
+}
+
+domino_status_t domino_read_timeline(const void* workspace, void* stream, domino_timeline_t* out) {
+  if (!workspace || !out) return fail(DOMINO_ERR_INVALID_ARG, "workspace and out must be non-NULL");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(out, static_cast<const uint8_t*>(workspace) + kTimelineOff, sizeof(domino_timeline_t),
+                   cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("timeline read: ") + cudaGetErrorString(e));
   return DOMINO_OK;
 }
 

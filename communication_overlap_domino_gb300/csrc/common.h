@@ -27,6 +27,9 @@ enum : uint32_t {
   kSiteMmaTmemEmpty = 3,
   kSiteEpilogueTmemFull = 4,
   kSiteDrain = 5,
+  kSiteFusedH = 6,  // fused kernel: GEMM2 producer waiting for H row block
+  kSiteFusedZ = 7,  // fused kernel: reducer waiting for the P partials of a tile
+  kSiteSelfTest = 8,  // domino_selftest_wait_timeout
 };
 
 // Epilogue of the tcgen05 GEMM: what is done with each fp32 accumulator tile.
@@ -79,6 +82,34 @@ struct GemmParams {  // CUtensorMap members carry 64-byte alignment
   int32_t b1_off;                  // B row of the second 128-row box relative to the first
   int32_t num_kb;                  // K blocks of 64
   int32_t tiles_m, tiles_n, num_shards, num_tiles;
+  DeviceStatus* status;
+  uint64_t timeout_ns;
+};
+
+// The fused forward kernel (fused.cu): both projections and the shard-sum of
+// every chunk in one persistent launch, ordered by counters in the workspace.
+struct FusedParams {
+  CUtensorMap map_x;                 // X [M, d], box 64 x 128
+  CUtensorMap map_w1a[kMaxShards];   // GEMM1 B operand, accumulator columns 0..127 (SwiGLU: gate)
+  CUtensorMap map_w1b[kMaxShards];   // GEMM1 B operand, accumulator columns 128..255 (SwiGLU: up)
+  CUtensorMap map_h[kMaxShards];     // H_p [M, Fp], box 64 x 128
+  CUtensorMap map_w2[kMaxShards];    // B_p^T [d, Fp], box 64 x 128
+  void* h[kMaxShards];
+  void* aux[kMaxShards];             // saved pre-activations or null
+  void* z[kMaxShards];               // partial outputs [M, d]
+  void* y;                           // output [M, d] bf16
+  uint32_t* hcnt;                    // [mu][P][tiles_m]: finished GEMM1 tile quarters
+  uint32_t* zcnt;                    // [mu][tiles_m][tiles_n2][4]: finished GEMM2 tile quarters
+  uint32_t* red_next;                // ticket of the next reduction piece
+  uint64_t* timeline;                // [0] first CTA start, [1] last GEMM tile end, [2] last reduction end (ns)
+  int64_t d, Fp;
+  int64_t ld_aux, aux_u_off;
+  int32_t Mc, mu, P;
+  int32_t n_tile1, b1_off1;          // GEMM1 output columns per tile and second-box row offset
+  int32_t tiles_m, tiles_n1, tiles_n2;
+  int32_t tiles_a, tiles_b;          // GEMM1 / GEMM2 tiles per chunk (all shards)
+  int32_t num_gemm_tiles, num_red_items;
+  int32_t kb1, kb2;                  // K blocks of GEMM1 (d) and GEMM2 (Fp)
   DeviceStatus* status;
   uint64_t timeout_ns;
 };

@@ -1,0 +1,266 @@
+// Epilogue device code shared by the grouped GEMM (gemm.cu) and the fused
+// forward kernel (fused.cu): activations and their derivatives, bf16/fp32 row
+// stores and loads, and the drain of one 128 x 256 fp32 accumulator tile from
+// tensor memory (each epilogue thread owns one accumulator row).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace domino {
+
+// Where one tile's epilogue writes (and, for the backward, reads).
+struct EpiArgs {
+  void* out;          // output matrix of this shard
+  void* aux;          // saved pre-activations (written by GEMM1, read by the backward dH epilogue) or null
+  int64_t ldo;        // leading dimension of out (elements)
+  int64_t ld_aux;     // leading dimension of aux (elements)
+  int64_t aux_u_off;  // SwiGLU: column offset of u inside aux
+  int64_t out_u_off;  // SwiGLU backward: column offset of du inside out
+  int32_t rows;       // valid accumulator rows (tile rows >= rows are not stored)
+  int32_t out_row0;   // output row of accumulator row 0 of tile row-block 0
+  int32_t n_end;      // output columns >= n_end are not stored
+};
+
+// ------------------------------------------------------------------ epilogue
+
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_tanh(float x) {
+  return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
+}
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+// Derivatives for the backward epilogue (product and chain rules).
+__device__ __forceinline__ float gelu_erf_grad(float x) {
+  // d/dx [x Phi(x)] = Phi(x) + x phi(x)
+  return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * __expf(-0.5f * x * x);
+}
+__device__ __forceinline__ float gelu_tanh_grad(float x) {
+  const float k = 0.79788456080286536f;
+  const float t = tanhf(k * (x + 0.044715f * x * x * x));
+  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
+}
+
+template <int EPI>
+__device__ __forceinline__ float activate_grad(float x) {
+  if constexpr (EPI == EPI_DG_GELU) return gelu_erf_grad(x);
+  else if constexpr (EPI == EPI_DG_GELU_TANH) return gelu_tanh_grad(x);
+  else return 1.0f;
+}
+
+__host__ __device__ constexpr bool is_dg(int epi) { return epi >= EPI_DG_GELU && epi <= EPI_DG_SWIGLU; }
+
+template <int EPI>
+__device__ __forceinline__ float activate(float x) {
+  if constexpr (EPI == EPI_H_GELU) return gelu_erf(x);
+  else if constexpr (EPI == EPI_H_GELU_TANH) return gelu_tanh(x);
+  else return x;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Stores v[0..n) (n <= 32) as bf16 at dst (16-byte aligned when n == 32).
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (&v)[32], int n) {
+  if (n >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      d4[q] = w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) dst[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+// Loads n <= 32 bf16 values from src (16-byte aligned when n == 32) as floats.
+__device__ __forceinline__ void load_row_bf16(const __nv_bfloat16* src, float (&v)[32], int n) {
+  if (n >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = s4[q];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
+        v[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < n ? __bfloat162float(src[j]) : 0.0f;
+  }
+}
+
+__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], int n) {
+  if (n >= 32) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) dst[j] = v[j];
+  }
+}
+
+// Drains one accumulator tile (this thread: one row) through the epilogue.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const EpiArgs& e, uint32_t tacc, int mb, int col0, int row_in_tile) {
+  const int64_t grow = static_cast<int64_t>(mb) * kBM + row_in_tile;
+  const bool row_ok = grow < e.rows;
+  const int64_t orow = e.out_row0 + grow;
+  constexpr int kChunks = (EPI == EPI_H_SWIGLU) ? (kBN / 2) / 32 : kBN / 32;
+#pragma unroll 1
+  for (int c = 0; c < kChunks; ++c) {
+    const int col = col0 + c * 32;
+    if (col >= e.n_end) break;  // uniform across the warp
+    const int n = e.n_end - col;
+    uint32_t r0[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, r0);
+    if constexpr (EPI == EPI_H_SWIGLU) {
+      uint32_t r1[32];
+      tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
+      tmem_ld_wait();
+      if (row_ok) {
+        float h[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float g = __uint_as_float(r0[j]);
+          const float u = __uint_as_float(r1[j]);
+          h[j] = silu(g) * u;
+        }
+        store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, h, n);
+        if (e.aux != nullptr) {
+          float g[32], u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            g[j] = __uint_as_float(r0[j]);
+            u[j] = __uint_as_float(r1[j]);
+          }
+          __nv_bfloat16* a = static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col;
+          store_row_bf16(a, g, n);
+          store_row_bf16(a + e.aux_u_off, u, n);
+        }
+      }
+    } else {
+      tmem_ld_wait();
+      if (row_ok) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+        if constexpr (EPI == EPI_Z_F32) {
+          store_row_f32(static_cast<float*>(e.out) + orow * e.ldo + col, v, n);
+        } else if constexpr (EPI == EPI_Z_BF16) {
+          store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, v, n);
+        } else {
+          if (e.aux != nullptr)
+            store_row_bf16(static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col, v, n);
+          float h[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(v[j]);
+          store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, h, n);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&q)[4], float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+      v[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+}
+
+// Backward dH epilogue: dG = dH * act'(g) (SwiGLU: dg and du), with the saved
+// pre-activations of the next 32-column chunk loaded while the current chunk
+// is computed, so their load latency overlaps the tensor-memory reads and math.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc, int mb, int col0,
+                                                 int row_in_tile) {
+  constexpr bool kSwiglu = EPI == EPI_DG_SWIGLU;
+  constexpr int kChunks = kBN / 32;
+  const int64_t grow = static_cast<int64_t>(mb) * kBM + row_in_tile;
+  const bool row_ok = grow < e.rows;
+  const int64_t orow = e.out_row0 + grow;
+  const __nv_bfloat16* pre_row = static_cast<const __nv_bfloat16*>(e.aux) + orow * e.ld_aux;
+  __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo;
+  uint4 gq[4], uq[4];
+  auto prefetch = [&](int c) {
+    const int col = col0 + c * 32;
+    if (row_ok && col + 32 <= e.n_end) {
+      const uint4* g4 = reinterpret_cast<const uint4*>(pre_row + col);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gq[i] = g4[i];
+      if constexpr (kSwiglu) {
+        const uint4* u4 = reinterpret_cast<const uint4*>(pre_row + e.aux_u_off + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) uq[i] = u4[i];
+      }
+    }
+  };
+  prefetch(0);
+#pragma unroll 1
+  for (int c = 0; c < kChunks; ++c) {
+    const int col = col0 + c * 32;
+    if (col >= e.n_end) break;  // uniform across the warp
+    const int n = e.n_end - col;
+    uint4 gc[4], uc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      gc[i] = gq[i];
+      uc[i] = uq[i];
+    }
+    if (c + 1 < kChunks) prefetch(c + 1);
+    uint32_t r0[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, r0);
+    tmem_ld_wait();
+    if (row_ok) {
+      float g[32], u[32];
+      if (n >= 32) {
+        unpack_bf16x32(gc, g);
+        if constexpr (kSwiglu) unpack_bf16x32(uc, u);
+      } else {
+        load_row_bf16(pre_row + col, g, n);
+        if constexpr (kSwiglu) load_row_bf16(pre_row + e.aux_u_off + col, u, n);
+      }
+      if constexpr (kSwiglu) {
+        float dg[32], du[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float dh = __uint_as_float(r0[j]);
+          const float sg = 1.0f / (1.0f + __expf(-g[j]));
+          du[j] = dh * g[j] * sg;                               // dH * silu(g)
+          dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
+        }
+        store_row_bf16(dst_row + col, dg, n);
+        store_row_bf16(dst_row + e.out_u_off + col, du, n);
+      } else {
+        float dgv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dgv[j] = __uint_as_float(r0[j]) * activate_grad<EPI>(g[j]);
+        store_row_bf16(dst_row + col, dgv, n);
+      }
+    }
+  }
+}
+
+}  // namespace domino

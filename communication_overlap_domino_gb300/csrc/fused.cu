@@ -1,0 +1,578 @@
+// Fused forward pass: both projections and the shard-sum of every chunk in ONE
+// persistent, cooperative launch.
+//
+// The Domino page ("Domino: Eliminating Communication in LLM Training via
+// Generic Tensor Slicing and Overlapping", Abstract) hides each piece's
+// communication behind the computation of the next piece.  Here the pieces are
+// made as small as one output tile: the shard-sum of output tile (k, m, n) of
+// chunk k starts as soon as the P row-parallel partials of that tile exist, on
+// reducer warps of the same SMs that keep running GEMM tiles, so the
+// memory-bound exchange overlaps tensor-core work at tile granularity and only
+// the reduction of the last tiles is left exposed.
+//
+// Work, in one global order shared by all CTAs (static round-robin, tile t is
+// processed by CTA t mod gridDim.x, in increasing t):
+//   for each chunk k:  GEMM1 tiles, then GEMM2 tiles (shard, column block, row
+//                      block; the last chunk's GEMM2 in groups of 8 row blocks)
+// Dependencies, through counters in the workspace (release/acquire at GPU scope):
+//   GEMM2 tile (k, m, n, p) needs H_{k,p}[row block m] complete: hcnt[k][p][m]
+//     counts finished 32-row quarters of GEMM1 tiles (target tiles_n1 * 4); the
+//     TMA producer polls it before loading H (then a proxy fence orders the
+//     generic-proxy stores before its async-proxy reads).
+//   shard-sum of (k, m, n), quarter q: zcnt[k][m][n][q] counts the GEMM2 tiles
+//     whose quarter q is stored (target P).  These 32-row pieces are taken from
+//     a kernel-wide queue (an atomic ticket) by the reducer warps, and by the
+//     epilogue warps once their GEMM tiles are done.
+// GEMM tiles never wait on the reducers and a GEMM2 tile only waits on GEMM1
+// tiles earlier in the global order, so with all CTAs resident (the cooperative
+// launch guarantees it) every wait ends; each is still bounded by timeout_ns.
+//
+// Warp roles (256 threads, one CTA per SM):
+//   warp 0 lane 0: TMA producer      warp 1: TMEM allocator, lane 0 issues MMAs
+//   warps 2..5   : epilogue          warps 6..7: reducers (shard-sum)
+#include <cuda_bf16.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "epilogue.cuh"
+#include "gemm.h"
+#include "ptx.cuh"
+
+namespace domino {
+
+namespace {
+
+constexpr int kFusedThreads = 256;  // 8 warps: 2 per SM sub-partition, so up to 255 registers
+constexpr int kFirstReducerWarp = 6;
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* ptr, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_u4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr)
+               : "memory");
+  return v;
+}
+
+struct FusedTile {
+  int phase;  // 0: GEMM1 (column-parallel + activation), 1: GEMM2 (row-parallel partial)
+  int k, p, m, n;
+};
+
+// Tiles of one phase of one chunk, in groups of G row blocks: for each group:
+// for each shard p: for each column block n: for each row block of the group.
+// With G = all row blocks this is the order of the separate launches (a column
+// block of the weights is loaded once and reused by every row block while it is
+// in L2).  The last chunk's GEMM2 uses smaller groups, so the P partials of its
+// first output tiles are complete -- and their shard-sum runs -- while the rest
+// of the chunk is still being multiplied.
+constexpr int kLastChunkGroupM = 8;
+
+__device__ __forceinline__ void grouped_coords(int r, int G, int P, int tiles_m, int tiles_n, int& p, int& m,
+                                               int& n) {
+  const int full = P * tiles_n * G;
+  const int g = r / full;
+  const int r2 = r - g * full;
+  const int rows_left = tiles_m - g * G;
+  const int gm = rows_left < G ? rows_left : G;
+  const int per_p = tiles_n * gm;
+  p = r2 / per_p;
+  const int r3 = r2 - p * per_p;
+  n = r3 / gm;
+  m = g * G + (r3 - n * gm);
+}
+
+__device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
+  FusedTile T;
+  const int per_chunk = f.tiles_a + f.tiles_b;
+  T.k = t / per_chunk;
+  int r = t - T.k * per_chunk;
+  if (r < f.tiles_a) {
+    T.phase = 0;
+    grouped_coords(r, f.tiles_m, f.P, f.tiles_m, f.tiles_n1, T.p, T.m, T.n);
+  } else {
+    T.phase = 1;
+    const int G = T.k == f.mu - 1 ? (f.tiles_m < kLastChunkGroupM ? f.tiles_m : kLastChunkGroupM) : f.tiles_m;
+    grouped_coords(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+  }
+  return T;
+}
+
+// Waits until *ctr >= target (acquire).  Bounded: gives up on *abort or after
+// timeout_ns, recording the error.  Executed by every lane of a warp, or by a
+// single thread.
+__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t target, volatile int* abort,
+                                             uint64_t timeout_ns, DeviceStatus* st, uint32_t where, uint32_t aux) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      record_error(st, kStatusTimeout, where, aux);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] += __uint_as_float(w[q] << 16);
+    acc[2 * q + 1] += __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Shard-sum of up to 32 rows x 8 columns per lane (the lane's 16-byte slice of
+// the 256-column tile): y = bf16(sum_{p=0}^{P-1} z_p), fp32 accumulation in
+// shard order.  Several rows' loads are in flight per step.
+template <int NP, bool F32>
+__device__ __forceinline__ void reduce_rows(const FusedParams& f, int64_t row0, int nrows, int64_t col, int P) {
+  if constexpr (NP == 0) {
+    // any shard count: one row at a time, loads consumed as they arrive
+    for (int rr = 0; rr < nrows; ++rr) {
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      for (int s = 0; s < P; ++s) {
+        if constexpr (F32) {
+          const float* src = static_cast<const float*>(f.z[s]) + (row0 + rr) * f.d + col;
+          const uint4 lo = ld_u4(src), hi = ld_u4(src + 4);
+          acc[0] += __uint_as_float(lo.x);
+          acc[1] += __uint_as_float(lo.y);
+          acc[2] += __uint_as_float(lo.z);
+          acc[3] += __uint_as_float(lo.w);
+          acc[4] += __uint_as_float(hi.x);
+          acc[5] += __uint_as_float(hi.y);
+          acc[6] += __uint_as_float(hi.z);
+          acc[7] += __uint_as_float(hi.w);
+        } else {
+          add_bf16x8(acc, ld_u4(static_cast<const __nv_bfloat16*>(f.z[s]) + (row0 + rr) * f.d + col));
+        }
+      }
+      uint4 o;
+      o.x = pack2(acc[0], acc[1]);
+      o.y = pack2(acc[2], acc[3]);
+      o.z = pack2(acc[4], acc[5]);
+      o.w = pack2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.y) + (row0 + rr) * f.d + col) = o;
+    }
+    return;
+  }
+  // rows in flight per step: about 16 sixteen-byte loads per lane
+  constexpr int kNP = NP > 0 ? NP : 1;
+  constexpr int kVec = F32 ? 2 : 1;
+  constexpr int kRowsRaw = 16 / (kNP * kVec);
+  constexpr int kRows = kRowsRaw < 1 ? 1 : (kRowsRaw > 4 ? 4 : kRowsRaw);
+  for (int rr = 0; rr < nrows; rr += kRows) {
+    const int nr = nrows - rr >= kRows ? kRows : nrows - rr;
+    uint4 x[kRows][kNP][kVec];
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+#pragma unroll
+      for (int s = 0; s < kNP; ++s)
+#pragma unroll
+        for (int v = 0; v < kVec; ++v)
+          if (i < nr) {
+            const uint8_t* base = static_cast<const uint8_t*>(f.z[s]);
+            x[i][s][v] = ld_u4(base + ((row0 + rr + i) * f.d + col) * (F32 ? 4 : 2) + 16 * v);
+          }
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      if (i < nr) {
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kNP; ++s) {
+          if constexpr (F32) {
+            acc[0] += __uint_as_float(x[i][s][0].x);
+            acc[1] += __uint_as_float(x[i][s][0].y);
+            acc[2] += __uint_as_float(x[i][s][0].z);
+            acc[3] += __uint_as_float(x[i][s][0].w);
+            acc[4] += __uint_as_float(x[i][s][kVec - 1].x);
+            acc[5] += __uint_as_float(x[i][s][kVec - 1].y);
+            acc[6] += __uint_as_float(x[i][s][kVec - 1].z);
+            acc[7] += __uint_as_float(x[i][s][kVec - 1].w);
+          } else {
+            add_bf16x8(acc, x[i][s][0]);
+          }
+        }
+        uint4 o;
+        o.x = pack2(acc[0], acc[1]);
+        o.y = pack2(acc[2], acc[3]);
+        o.z = pack2(acc[4], acc[5]);
+        o.w = pack2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.y) + (row0 + rr + i) * f.d + col) = o;
+      }
+    }
+  }
+}
+
+template <bool F32>
+__device__ __forceinline__ void reduce_dispatch(const FusedParams& f, int64_t row0, int nrows, int64_t col) {
+  switch (f.P) {
+    case 1: reduce_rows<1, F32>(f, row0, nrows, col, 1); break;
+    case 2: reduce_rows<2, F32>(f, row0, nrows, col, 2); break;
+    case 4: reduce_rows<4, F32>(f, row0, nrows, col, 4); break;
+    case 8: reduce_rows<8, F32>(f, row0, nrows, col, 8); break;
+    default: reduce_rows<0, F32>(f, row0, nrows, col, f.P); break;
+  }
+}
+
+// Takes reduction pieces (32 rows x 256 columns of one output tile: the zcnt
+// entry j) from the kernel-wide queue in order and sums each one once its P
+// partials are stored.  Run by the reducer warps from the start and by the
+// epilogue warps once their own GEMM tiles are done (so a piece never waits on
+// work of the warp that holds it).  Returns false if a wait gave up.
+template <bool F32>
+__device__ __forceinline__ bool run_reduction_pieces(const FusedParams& f, volatile int* abort, int lane) {
+  const int num_pieces = f.num_red_items * 4;
+  const int per_k = f.tiles_m * f.tiles_n2;
+  while (!*abort) {
+    int j = 0;
+    if (lane == 0) j = static_cast<int>(atomicAdd(f.red_next, 1u));
+    j = __shfl_sync(0xffffffffu, j, 0);
+    if (j >= num_pieces) break;
+    const int item = j >> 2, q = j & 3;
+    const int k = item / per_k;
+    const int r = item - k * per_k;
+    const int m = r / f.tiles_n2;
+    const int n = r - m * f.tiles_n2;
+    if (!wait_counter(f.zcnt + j, static_cast<uint32_t>(f.P), abort, f.timeout_ns, f.status, kSiteFusedZ, j))
+      return false;
+    const int row_lo = m * kBM + q * 32;
+    int nrows = f.Mc - row_lo;
+    nrows = nrows > 32 ? 32 : nrows;
+    const int64_t col = static_cast<int64_t>(n) * kBN + lane * 8;
+    if (nrows > 0 && col < f.d) reduce_dispatch<F32>(f, static_cast<int64_t>(k) * f.Mc + row_lo, nrows, col);
+    __syncwarp();
+    if (lane == 0)
+      atomicMax(reinterpret_cast<unsigned long long*>(&f.timeline[2]),
+                static_cast<unsigned long long>(globaltimer_ns()));
+  }
+  return true;
+}
+
+template <int EPI_A, int EPI_B>
+__global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __grid_constant__ FusedParams f) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem_a = smem;
+  uint8_t* smem_b = smem + kStages * kAStageBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + kStages * kBStageBytes);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* final_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4 * 32);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    atomicMin(reinterpret_cast<unsigned long long*>(&f.timeline[0]),
+              static_cast<unsigned long long>(globaltimer_ns()));
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = f.num_gemm_tiles;
+  const uint64_t tmo = f.timeout_ns;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    prefetch_tmap(&f.map_x);
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+      const FusedTile T = fused_tile(f, t);
+      const CUtensorMap *ma, *mb0, *mb1;
+      int ya, yb0, yb1, nkb;
+      if (T.phase == 0) {
+        ma = &f.map_x;
+        mb0 = &f.map_w1a[T.p];
+        mb1 = &f.map_w1b[T.p];
+        ya = T.k * f.Mc + T.m * kBM;
+        yb0 = T.n * f.n_tile1;
+        yb1 = yb0 + f.b1_off1;
+        nkb = f.kb1;
+      } else {
+        const uint32_t* ctr = f.hcnt + (T.k * f.P + T.p) * f.tiles_m + T.m;
+        if (!wait_counter(ctr, static_cast<uint32_t>(f.tiles_n1) * 4, abort_flag, tmo, f.status, kSiteFusedH, t))
+          break;
+        fence_proxy_async_global();  // H was written through the generic proxy; TMA reads it
+        ma = &f.map_h[T.p];
+        mb0 = &f.map_w2[T.p];
+        mb1 = mb0;
+        ya = T.k * f.Mc + T.m * kBM;
+        yb0 = T.n * kBN;
+        yb1 = yb0 + kBN / 2;
+        nkb = f.kb2;
+      }
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, tmo, f.status, kSiteProducerEmpty, t)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem_a + stage * kAStageBytes;
+        uint8_t* sb = smem_b + stage * kBStageBytes;
+        mbar_arrive_expect_tx(&full_bar[stage], kAStageBytes + kBStageBytes);
+        const int k0 = kb * kBK;
+        tma_load_2d(sa, ma, &full_bar[stage], k0, ya);
+        tma_load_2d(sb, mb0, &full_bar[stage], k0, yb0);
+        tma_load_2d(sb + kBStageBytes / 2, mb1, &full_bar[stage], k0, yb1);
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+    for (int s = 0; s < kStages; ++s) {
+      if (issued_mask & (1u << s)) {
+        volatile int no_abort = 0;
+        mbar_wait(&full_bar[s], (issued_parity >> s) & 1u, &no_abort, tmo, f.status, kSiteDrain, s);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+    uint32_t stage = 0, phase = 0;
+    int i = 0;
+    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++i) {
+      const FusedTile T = fused_tile(f, t);
+      const int nkb = T.phase == 0 ? f.kb1 : f.kb2;
+      const uint32_t acc = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag, tmo, f.status, kSiteMmaTmemEmpty, t)) break;
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + acc * kBN;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, abort_flag, tmo, f.status, kSiteMmaFull, t)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t adesc = smem_desc_k128(smem_u32(smem_a + stage * kAStageBytes));
+        const uint64_t bdesc = smem_desc_k128(smem_u32(smem_b + stage * kBStageBytes));
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+        mma_commit(&empty_bar[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      mma_commit(&tfull_bar[acc]);
+    }
+    mma_commit(final_bar);
+    volatile int no_abort = 0;
+    mbar_wait(final_bar, 0, &no_abort, tmo, f.status, kSiteDrain, 99);
+  } else if (warp >= 2 && warp < kFirstReducerWarp) {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int i = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
+      const uint32_t acc = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, tmo, f.status, kSiteEpilogueTmemFull, t)) break;
+      tc_fence_after_sync();
+      const FusedTile T = fused_tile(f, t);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+      if (T.phase == 0) {
+        const EpiArgs e{f.h[T.p], f.aux[T.p], f.Fp, f.ld_aux, f.aux_u_off, 0,
+                        f.Mc, static_cast<int32_t>(T.k * f.Mc), static_cast<int32_t>(f.Fp)};
+        epilogue_tile<EPI_A>(e, tacc, T.m, T.n * f.n_tile1, row_in_tile);
+        tc_fence_before_sync();
+        mbar_arrive(&tempty_bar[acc]);
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(f.hcnt + (T.k * f.P + T.p) * f.tiles_m + T.m, 1);
+      } else {
+        const EpiArgs e{f.z[T.p], nullptr, f.d, 0, 0, 0, f.Mc, static_cast<int32_t>(T.k * f.Mc),
+                        static_cast<int32_t>(f.d)};
+        epilogue_tile<EPI_B>(e, tacc, T.m, T.n * kBN, row_in_tile);
+        tc_fence_before_sync();
+        mbar_arrive(&tempty_bar[acc]);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          red_release_gpu_add(f.zcnt + ((static_cast<int64_t>(T.k) * f.tiles_m + T.m) * f.tiles_n2 + T.n) * 4 +
+                                  quarter, 1);
+      }
+    }
+    if (lane == 0)
+      atomicMax(reinterpret_cast<unsigned long long*>(&f.timeline[1]),
+                static_cast<unsigned long long>(globaltimer_ns()));
+    __syncwarp();
+    run_reduction_pieces<EPI_B == EPI_Z_F32>(f, abort_flag, lane);
+  } else if (warp >= kFirstReducerWarp) {
+    // -------------------------------------------------------------- reducers
+    run_reduction_pieces<EPI_B == EPI_Z_F32>(f, abort_flag, lane);
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int A, int B>
+void* fused_ptr() {
+  return reinterpret_cast<void*>(&fused_fwd_kernel<A, B>);
+}
+
+void* fused_kernel_for(int epi_a, bool f32) {
+  switch (epi_a) {
+    case EPI_H_GELU: return f32 ? fused_ptr<EPI_H_GELU, EPI_Z_F32>() : fused_ptr<EPI_H_GELU, EPI_Z_BF16>();
+    case EPI_H_GELU_TANH:
+      return f32 ? fused_ptr<EPI_H_GELU_TANH, EPI_Z_F32>() : fused_ptr<EPI_H_GELU_TANH, EPI_Z_BF16>();
+    case EPI_H_IDENTITY:
+      return f32 ? fused_ptr<EPI_H_IDENTITY, EPI_Z_F32>() : fused_ptr<EPI_H_IDENTITY, EPI_Z_BF16>();
+    case EPI_H_SWIGLU: return f32 ? fused_ptr<EPI_H_SWIGLU, EPI_Z_F32>() : fused_ptr<EPI_H_SWIGLU, EPI_Z_BF16>();
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+size_t fused_sync_bytes(int64_t Mc, int64_t d, int P, int mu) {
+  const int64_t tiles_m = (Mc + kBM - 1) / kBM;
+  const int64_t tiles_n2 = (d + kBN - 1) / kBN;
+  return static_cast<size_t>(4 * (mu * P * tiles_m + mu * tiles_m * tiles_n2 * 4 + 1));
+}
+
+cudaError_t prepare_fused_kernels(int* max_ctas_per_sm) {
+  const int epis[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_IDENTITY, EPI_H_SWIGLU};
+  int occ = 1 << 30;
+  for (int a = 0; a < 4; ++a) {
+    for (int f32 = 0; f32 < 2; ++f32) {
+      void* fn = fused_kernel_for(epis[a], f32 != 0);
+      cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+      if (st != cudaSuccess) return st;
+      int n = 0;
+      st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kFusedThreads, kGemmSmemBytes);
+      if (st != cudaSuccess) return st;
+      occ = n < occ ? n : occ;
+    }
+  }
+  *max_ctas_per_sm = occ;
+  return cudaSuccess;
+}
+
+domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, cudaStream_t stream, std::string* err) {
+  FusedParams f;
+  memset(&f, 0, sizeof f);
+  const int64_t Fp = L.Fp;
+  const bool swiglu = L.epi_a == EPI_H_SWIGLU;
+  if (!encode_bf16_sw128(&f.map_x, Operand2D{L.X, L.M, L.d, L.d}, kBM, err)) return DOMINO_ERR_CUDA;
+  for (int p = 0; p < L.P; ++p) {
+    const uint8_t* W1 = static_cast<const uint8_t*>(L.A_shards[p]);
+    const Operand2D w1a{W1, Fp, L.d, L.d};
+    const Operand2D w1b = swiglu ? Operand2D{W1 + static_cast<size_t>(Fp) * L.d * 2, Fp, L.d, L.d} : w1a;
+    if (!encode_bf16_sw128(&f.map_w1a[p], w1a, kBN / 2, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&f.map_w1b[p], w1b, kBN / 2, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&f.map_h[p], Operand2D{L.H[p], L.M, Fp, Fp}, kBM, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&f.map_w2[p], Operand2D{L.B_shards[p], L.d, Fp, Fp}, kBN / 2, err))
+      return DOMINO_ERR_CUDA;
+    f.h[p] = L.H[p];
+    f.aux[p] = L.aux[p];
+    f.z[p] = L.Z[p];
+  }
+  f.y = L.Y;
+  f.hcnt = L.sync;
+  f.Mc = static_cast<int32_t>(L.M / L.mu);
+  f.tiles_m = (f.Mc + kBM - 1) / kBM;
+  f.tiles_n1 = static_cast<int32_t>((Fp + (swiglu ? kBN / 2 : kBN) - 1) / (swiglu ? kBN / 2 : kBN));
+  f.tiles_n2 = static_cast<int32_t>((L.d + kBN - 1) / kBN);
+  f.zcnt = L.sync + static_cast<int64_t>(L.mu) * L.P * f.tiles_m;
+  f.red_next = f.zcnt + static_cast<int64_t>(L.mu) * f.tiles_m * f.tiles_n2 * 4;
+  f.timeline = L.timeline;
+  f.d = L.d;
+  f.Fp = Fp;
+  f.mu = L.mu;
+  f.P = L.P;
+  f.n_tile1 = swiglu ? kBN / 2 : kBN;
+  f.b1_off1 = swiglu ? 0 : kBN / 2;
+  f.ld_aux = Fp * (swiglu ? 2 : 1);
+  f.aux_u_off = Fp;
+  f.tiles_a = L.P * f.tiles_m * f.tiles_n1;
+  f.tiles_b = L.P * f.tiles_m * f.tiles_n2;
+  f.num_gemm_tiles = L.mu * (f.tiles_a + f.tiles_b);
+  f.num_red_items = L.mu * f.tiles_m * f.tiles_n2;
+  f.kb1 = static_cast<int32_t>((L.d + kBK - 1) / kBK);
+  f.kb2 = static_cast<int32_t>((Fp + kBK - 1) / kBK);
+  f.status = L.status;
+  f.timeout_ns = L.timeout_ns;
+  if (f.num_gemm_tiles == 0) return DOMINO_OK;
+  void* fn = fused_kernel_for(L.epi_a, L.partial_f32);
+  if (!fn) {
+    if (err) *err = "launch_fused_fwd: bad activation";
+    return DOMINO_ERR_INVALID_ARG;
+  }
+  const int grid = f.num_gemm_tiles < max_ctas ? f.num_gemm_tiles : max_ctas;
+  void* args[] = {&f};
+  cudaError_t st = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kFusedThreads), args, kGemmSmemBytes, stream);
+  if (st != cudaSuccess) {
+    if (err) *err = std::string("fused launch: ") + cudaGetErrorString(st);
+    return DOMINO_ERR_CUDA;
+  }
+  return DOMINO_OK;
+}
+
+}  // namespace domino

@@ -32,192 +32,11 @@
 #include <mutex>
 #include <string>
 
+#include "epilogue.cuh"
 #include "gemm.h"
 #include "ptx.cuh"
 
 namespace domino {
-
-// ------------------------------------------------------------------ epilogue
-
-__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
-__device__ __forceinline__ float gelu_tanh(float x) {
-  return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
-}
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
-
-// Derivatives for the backward epilogue (product and chain rules).
-__device__ __forceinline__ float gelu_erf_grad(float x) {
-  // d/dx [x Phi(x)] = Phi(x) + x phi(x)
-  return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * __expf(-0.5f * x * x);
-}
-__device__ __forceinline__ float gelu_tanh_grad(float x) {
-  const float k = 0.79788456080286536f;
-  const float t = tanhf(k * (x + 0.044715f * x * x * x));
-  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
-}
-
-template <int EPI>
-__device__ __forceinline__ float activate_grad(float x) {
-  if constexpr (EPI == EPI_DG_GELU) return gelu_erf_grad(x);
-  else if constexpr (EPI == EPI_DG_GELU_TANH) return gelu_tanh_grad(x);
-  else return 1.0f;
-}
-
-__host__ __device__ constexpr bool is_dg(int epi) { return epi >= EPI_DG_GELU && epi <= EPI_DG_SWIGLU; }
-
-template <int EPI>
-__device__ __forceinline__ float activate(float x) {
-  if constexpr (EPI == EPI_H_GELU) return gelu_erf(x);
-  else if constexpr (EPI == EPI_H_GELU_TANH) return gelu_tanh(x);
-  else return x;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Stores v[0..n) (n <= 32) as bf16 at dst (16-byte aligned when n == 32).
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (&v)[32], int n) {
-  if (n >= 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-      d4[q] = w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < n) dst[j] = __float2bfloat16_rn(v[j]);
-  }
-}
-
-// Loads n <= 32 bf16 values from src (16-byte aligned when n == 32) as floats.
-__device__ __forceinline__ void load_row_bf16(const __nv_bfloat16* src, float (&v)[32], int n) {
-  if (n >= 32) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = s4[q];
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
-        v[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < n ? __bfloat162float(src[j]) : 0.0f;
-  }
-}
-
-__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], int n) {
-  if (n >= 32) {
-    float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < n) dst[j] = v[j];
-  }
-}
-
-// Drains one accumulator tile (this thread: one row) through the epilogue.
-template <int EPI>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tacc, int shard, int mb, int nb,
-                                              int row_in_tile) {
-  const int64_t grow = static_cast<int64_t>(mb) * kBM + row_in_tile;
-  const bool row_ok = grow < p.rows;
-  const int64_t orow = p.out_row0 + grow;
-  const int col0 = p.n_base + nb * p.n_tile;
-  constexpr int kChunks = (EPI == EPI_H_SWIGLU) ? (kBN / 2) / 32 : kBN / 32;
-#pragma unroll 1
-  for (int c = 0; c < kChunks; ++c) {
-    const int col = col0 + c * 32;
-    if (col >= p.n_end) break;  // uniform across the warp
-    const int n = p.n_end - col;
-    uint32_t r0[32];
-    tmem_ld_32x32b_x32(tacc + c * 32, r0);
-    if constexpr (EPI == EPI_H_SWIGLU) {
-      uint32_t r1[32];
-      tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
-      tmem_ld_wait();
-      if (row_ok) {
-        float h[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float g = __uint_as_float(r0[j]);
-          const float u = __uint_as_float(r1[j]);
-          h[j] = silu(g) * u;
-        }
-        store_row_bf16(static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col, h, n);
-        if (p.aux[shard] != nullptr) {
-          float g[32], u[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            g[j] = __uint_as_float(r0[j]);
-            u[j] = __uint_as_float(r1[j]);
-          }
-          __nv_bfloat16* a = static_cast<__nv_bfloat16*>(p.aux[shard]) + orow * p.ld_aux + col;
-          store_row_bf16(a, g, n);
-          store_row_bf16(a + p.aux_u_off, u, n);
-        }
-      }
-    } else if constexpr (is_dg(EPI)) {
-      tmem_ld_wait();
-      if (row_ok) {
-        const __nv_bfloat16* pre = static_cast<const __nv_bfloat16*>(p.aux[shard]) + orow * p.ld_aux + col;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col;
-        float g[32];
-        load_row_bf16(pre, g, n);
-        if constexpr (EPI == EPI_DG_SWIGLU) {
-          float u[32], dg[32], du[32];
-          load_row_bf16(pre + p.aux_u_off, u, n);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float dh = __uint_as_float(r0[j]);
-            const float sg = 1.0f / (1.0f + __expf(-g[j]));
-            du[j] = dh * g[j] * sg;                               // dH * silu(g)
-            dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
-          }
-          store_row_bf16(dst, dg, n);
-          store_row_bf16(dst + p.out_u_off, du, n);
-        } else {
-          float dgv[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) dgv[j] = __uint_as_float(r0[j]) * activate_grad<EPI>(g[j]);
-          store_row_bf16(dst, dgv, n);
-        }
-      }
-    } else {
-      tmem_ld_wait();
-      if (row_ok) {
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
-        if constexpr (EPI == EPI_Z_F32) {
-          store_row_f32(static_cast<float*>(p.out[shard]) + orow * p.ldo + col, v, n);
-        } else if constexpr (EPI == EPI_Z_BF16) {
-          store_row_bf16(static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col, v, n);
-        } else {
-          if (p.aux[shard] != nullptr)
-            store_row_bf16(static_cast<__nv_bfloat16*>(p.aux[shard]) + orow * p.ld_aux + col, v, n);
-          float h[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(v[j]);
-          store_row_bf16(static_cast<__nv_bfloat16*>(p.out[shard]) + orow * p.ldo + col, h, n);
-        }
-      }
-    }
-  }
-}
 
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& shard, int& mb, int& nb) {
   const int per = p.tiles_m * p.tiles_n;
@@ -385,7 +204,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
       int shard, mb, nb;
       tile_coords(p, t, shard, mb, nb);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
-      epilogue_tile<EPI>(p, tacc, shard, mb, nb, row_in_tile);
+      const EpiArgs e{p.out[shard], p.aux[shard], p.ldo, p.ld_aux, p.aux_u_off, p.out_u_off,
+                      p.rows, p.out_row0, p.n_end};
+      const int col0 = p.n_base + nb * p.n_tile;
+      if constexpr (is_dg(EPI))
+        epilogue_tile_dg<EPI>(e, tacc, mb, col0, row_in_tile);
+      else
+        epilogue_tile<EPI>(e, tacc, mb, col0, row_in_tile);
       tc_fence_before_sync();
       mbar_arrive(&tempty_bar[acc]);
     }

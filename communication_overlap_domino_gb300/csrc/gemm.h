@@ -42,10 +42,36 @@ struct GemmLaunch {
 };
 
 cudaError_t prepare_gemm_kernels();
+bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err);
 domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
+
+// The fused forward pass (fused.cu).
+struct FusedLaunch {
+  const void* X = nullptr;
+  const void* A_shards[kMaxShards] = {};
+  const void* B_shards[kMaxShards] = {};
+  void* H[kMaxShards] = {};
+  void* aux[kMaxShards] = {};
+  void* Z[kMaxShards] = {};
+  void* Y = nullptr;
+  uint32_t* sync = nullptr;      // fused_sync_bytes() of zeroed counters
+  uint64_t* timeline = nullptr;  // 3 words: {UINT64_MAX, 0, 0} before the launch
+  int64_t M = 0, d = 0, Fp = 0;
+  int mu = 1, P = 1;
+  int epi_a = EPI_H_GELU;
+  bool partial_f32 = true;
+  DeviceStatus* status = nullptr;
+  uint64_t timeout_ns = 0;
+};
+size_t fused_sync_bytes(int64_t Mc, int64_t d, int P, int mu);
+cudaError_t prepare_fused_kernels(int* max_ctas_per_sm);
+domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
 
 // Records a detailed message for domino_last_error() (api.cu).
 void set_last_error(const std::string& msg);
+
+// Bounded-wait self-test (shard_sum.cu).
+domino_status_t launch_selftest_wait(void* workspace, uint64_t timeout_ns, cudaStream_t stream, std::string* err);
 
 // Shard-sum launch (shard_sum.cu).
 domino_status_t launch_shard_sum(const ShardSumParams& p, int num_sms, cudaStream_t stream, std::string* err);

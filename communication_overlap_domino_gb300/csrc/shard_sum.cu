@@ -16,6 +16,7 @@
 #include <string>
 
 #include "gemm.h"
+#include "ptx.cuh"
 
 namespace domino {
 
@@ -113,7 +114,38 @@ void* pick(int P) {
   }
 }
 
+// One warp waits for a flag word (header offset 128) that nothing sets, through
+// the same bounded-wait pattern as the kernels' inter-CTA waits.
+__global__ void selftest_wait_kernel(DeviceStatus* st, const uint32_t* flag, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0) return;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      if (threadIdx.x == 0) record_error(st, kStatusTimeout, kSiteSelfTest, 0);
+      return;
+    }
+    __nanosleep(1000);
+  }
+}
+
 }  // namespace
+
+domino_status_t launch_selftest_wait(void* workspace, uint64_t timeout_ns, cudaStream_t stream, std::string* err) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t st = cudaMemsetAsync(ws + 128, 0, 4, stream);
+  if (st == cudaSuccess) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<DeviceStatus*>(ws),
+                                               reinterpret_cast<const uint32_t*>(ws + 128), timeout_ns);
+    st = cudaGetLastError();
+  }
+  if (st != cudaSuccess) {
+    if (err) *err = std::string("self-test launch: ") + cudaGetErrorString(st);
+    return DOMINO_ERR_CUDA;
+  }
+  return DOMINO_OK;
+}
 
 domino_status_t launch_shard_sum(const ShardSumParams& p, int num_sms, cudaStream_t stream, std::string* err) {
   const int64_t nvec = p.rows * (p.cols / 8);

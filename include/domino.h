@@ -92,8 +92,15 @@ typedef enum domino_partial_dtype {
 
 typedef enum domino_schedule {
   DOMINO_SCHEDULE_SERIAL = 0, /* GEMMs and shard-sums in order on one stream: no overlap  */
-  DOMINO_SCHEDULE_STREAMS = 1 /* shard-sum of piece (k,s) on a second stream, released by
-                                 an event after its GEMM, overlapping the next piece      */
+  DOMINO_SCHEDULE_STREAMS = 1, /* shard-sum of piece (k,s) on a second stream, released by
+                                  an event after its GEMM, overlapping the next piece      */
+  DOMINO_SCHEDULE_FUSED = 2    /* forward only: GEMM1, GEMM2 and the shard-sum of every chunk
+                                  in one persistent cooperative launch; the shard-sum of each
+                                  128x256 output tile starts as soon as its P partials are
+                                  stored, on the same SMs that keep running GEMM tiles.  The
+                                  result is bit-identical to the other schedules; out_slices
+                                  does not change the work (the pieces are already tiles).
+                                  domino_mlp_bwd runs the STREAMS schedule for it.          */
 } domino_schedule_t;
 
 /* desc->flags */
@@ -118,9 +125,10 @@ typedef struct domino_mlp_desc {
 
 /* Bytes of device workspace domino_mlp_fwd/bwd need for this problem
  * (0 for an invalid descriptor).  Layout, all owned by the library while a call
- * runs: a 256-byte header (device status words), the hidden activations
- * [P][M][F_p] bf16 (unless `saved` is given to fwd), and the P partial outputs
- * [P][M][d] in the partial dtype.  with_bwd != 0 adds what the backward pass
+ * runs: a 256-byte header (device status words, fused-kernel timeline), the
+ * hidden activations [P][M][F_p] bf16 (unless `saved` is given to fwd), the P
+ * partial outputs [P][M][d] in the partial dtype, and the fused schedule's tile
+ * counters.  with_bwd != 0 adds what the backward pass
  * needs (the gradient of the hidden layer and the dX partials). */
 DOMINO_API size_t domino_mlp_workspace_size(const domino_mlp_desc_t* desc, int32_t with_bwd);
 
@@ -169,9 +177,29 @@ DOMINO_API domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const v
 DOMINO_API domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t partial_dtype, int64_t rows,
                                  int64_t cols, int64_t ld_partial, void* Y, int64_t ld_y, void* stream);
 
+/* Device-side timeline of the last DOMINO_SCHEDULE_FUSED forward call made with
+ * this workspace (%globaltimer nanoseconds): when its first CTA started, when the
+ * last GEMM tile's epilogue finished, and when the last shard-sum finished.
+ * reduce_end_ns - gemm_end_ns (if positive) is the reduction time left exposed.
+ * Synchronises `stream`; `out` is host memory. */
+typedef struct domino_timeline {
+  uint64_t start_ns;
+  uint64_t gemm_end_ns;
+  uint64_t reduce_end_ns;
+} domino_timeline_t;
+DOMINO_API domino_status_t domino_read_timeline(const void* workspace, void* stream, domino_timeline_t* out);
+
 /* Synchronises `stream`, returns the first device-side error recorded in the
  * workspace's status word since the last query (DOMINO_OK if none) and clears it. */
 DOMINO_API domino_status_t domino_query_device_status(void* workspace, void* stream);
+
+/* Self-test of the bounded device-side waits: launches one block that waits, with
+ * the same bounded wait the kernels use, for a flag in the workspace header that
+ * nothing sets.  After timeout_ns the wait gives up and records
+ * DOMINO_ERR_TIMEOUT in the workspace's status words (read them with
+ * domino_query_device_status); the context stays usable.  workspace: at least
+ * 256 bytes (the header).  Returns the launch status. */
+DOMINO_API domino_status_t domino_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream);
 
 /* Static, NUL-terminated name of a status code. */
 DOMINO_API const char* domino_status_string(domino_status_t status);
@@ -220,7 +248,8 @@ typedef enum domino_kernel_kind {
   DOMINO_KERNEL_SHARD_SUM = 2, /* sum of the P partials                                */
   DOMINO_KERNEL_BWD_DH = 3,    /* backward: dH and the activation derivative           */
   DOMINO_KERNEL_BWD_DX = 4,    /* backward: partial input gradients                    */
-  DOMINO_KERNEL_BWD_DW = 5     /* backward: weight gradients                           */
+  DOMINO_KERNEL_BWD_DW = 5,    /* backward: weight gradients                           */
+  DOMINO_KERNEL_FUSED = 6      /* the fused forward kernel (whole call)                */
 } domino_kernel_kind_t;
 
 typedef struct domino_kernel_time {

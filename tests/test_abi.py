@@ -55,12 +55,15 @@ def desc(**kw):
 
 def test_workspace_layout(lib):
     d = desc()
-    M, dd, F, P = 256, 512, 2048, 2
+    M, dd, F, P, mu = 256, 512, 2048, 2, 2
     Fp = F // P
-    expect = 256 + P * M * Fp * 2 + P * M * dd * 4
+    tiles_m, tiles_n2 = (M // mu + 127) // 128, (dd + 255) // 256
+    sync = 4 * (mu * P * tiles_m + mu * tiles_m * tiles_n2 * 4 + 1)
+    sync = (sync + 255) // 256 * 256
+    expect = 256 + P * M * Fp * 2 + P * M * dd * 4 + sync
     assert b.workspace_size(d) == expect
     d16 = desc(partial="bf16")
-    assert b.workspace_size(d16) == 256 + P * M * Fp * 2 + P * M * dd * 2
+    assert b.workspace_size(d16) == 256 + P * M * Fp * 2 + P * M * dd * 2 + sync
     assert b.saved_size(d) == P * M * Fp * 2 * 2
     assert b.saved_size(desc(act="swiglu")) == P * M * Fp * 3 * 2
     assert b.workspace_size(d, with_bwd=True) > b.workspace_size(d)
@@ -82,7 +85,7 @@ def test_descriptor_validation(lib, kw, status):
 
 
 def test_enum_validation(lib):
-    for field, bad in (("act", 9), ("partial_dtype", 5), ("schedule", 7), ("reserved", 1), ("flags", 0x80)):
+    for field, bad in (("act", 9), ("partial_dtype", 5), ("schedule", 3), ("reserved", 1), ("flags", 0x80)):
         d = desc()
         setattr(d, field, bad)
         arr = b._ptr_array([0x20000] * 2)

@@ -81,30 +81,34 @@ def test_shard_sum_parity(P, dtype):
 
 # ---------------------------------------------------------- small workloads
 
-@pytest.mark.parametrize("schedule", ["serial", "streams"])
+@pytest.mark.parametrize("schedule", ["serial", "streams", "fused"])
 def test_tiny_gelu_workload(schedule):
     _check_full(wl.WORKLOADS["tiny_gelu_fwd"], schedule=schedule)
 
 
 @pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "identity"])
 @pytest.mark.parametrize("partial", ["f32", "bf16"])
-def test_ragged_shapes(act, partial):
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_ragged_shapes(act, partial, schedule):
     # chunk rows 200 (not a multiple of 128), F/P = 328 (N and K tails), d = 336
     # (K tail for GEMM1), two output slices of 168 columns (N tail), P = 3, mu = 3
     w = wl.Workload("ragged", M=600, d=336, F=984, P=3, mu=3, act=act, partial=partial, slices=2)
-    _check_full(w, seed=3)
+    _check_full(w, seed=3, schedule=schedule)
 
 
-def test_llama_shard_width_tail():
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_llama_shard_width_tail(schedule):
     # F/P = 1376 as in the Llama-style workload (10.75 tiles of 128), small M and d
     w = wl.Workload("llama_tail", M=512, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16")
-    _check_full(w, seed=4)
+    _check_full(w, seed=4, schedule=schedule)
 
 
-@pytest.mark.parametrize("P,mu,S", [(1, 1, 1), (4, 4, 1), (2, 1, 4), (16, 2, 1)])
-def test_degenerate_slicings(P, mu, S):
-    w = wl.Workload("degenerate", M=512, d=512, F=16 * 128, P=P, mu=mu, act="gelu", partial="f32", slices=S)
-    _check_full(w, seed=5)
+@pytest.mark.parametrize("P,mu,S", [(1, 1, 1), (4, 4, 1), (2, 1, 4), (16, 2, 1), (3, 5, 1)])
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_degenerate_slicings(P, mu, S, schedule):
+    w = wl.Workload("degenerate", M=640, d=512, F=P * 128 * (3 if P == 3 else 1), P=P, mu=mu, act="gelu",
+                    partial="f32", slices=S)
+    _check_full(w, seed=5, schedule=schedule)
 
 
 def test_empty_batch_leaves_output_untouched():
@@ -128,6 +132,30 @@ def test_deterministic_and_schedule_independent():
     w8 = w.with_(mu=8)
     y4 = _run(w8, t, "streams")
     assert torch.equal(y1, y4), "result depends on mu"
+    y5 = _run(w, t, "fused")
+    assert torch.equal(y1, y5), "fused and stream schedules differ"
+    y6 = _run(w8, t, "fused")
+    assert torch.equal(y1, y6), "fused result depends on mu"
+
+
+def test_fused_timeline_and_saved():
+    w = wl.Workload("fused_saved", M=512, d=512, F=2048, P=4, mu=2, act="swiglu", partial="bf16")
+    t = wl.generate(w, seed=10)
+    X, A_sh, B_sh = _device_inputs(w, t)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, "fused")
+    ws = torch.zeros(b.workspace_size(desc), dtype=torch.uint8, device="cuda")
+    saved_f = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device="cuda")
+    saved_s = torch.zeros_like(saved_f)
+    yf = b.mlp_fwd(X, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, schedule="fused", workspace=ws,
+                   saved=saved_f)
+    tl = b.read_timeline(ws)
+    assert tl["start_ns"] <= tl["gemm_end_ns"] and tl["start_ns"] <= tl["reduce_end_ns"]
+    assert tl["reduce_end_ns"] - tl["start_ns"] < 10_000_000_000
+    ys = b.mlp_fwd(X, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, schedule="streams", saved=saved_s)
+    torch.cuda.synchronize()
+    assert torch.equal(yf, ys)
+    assert torch.equal(saved_f, saved_s), "fused schedule saved different pre-activations"
+    assert b.query_device_status(ws) == 0
 
 
 def test_saved_preactivations():
@@ -164,7 +192,7 @@ def _sample_rows(w, per_chunk=6, seed=0):
     return sorted(set(int(r) for r in rows))
 
 
-def _check_sampled(w, schedule="streams"):
+def _check_sampled(w, schedule="streams"):  # noqa: C901
     t = wl.generate(w, seed=0)
     Y = _run(w, t, schedule)
     rows = _sample_rows(w)
@@ -181,10 +209,26 @@ def _check_sampled(w, schedule="streams"):
 
 
 @pytest.mark.parametrize("name", ["gpt_gelu_fwd", "llama_swiglu_fwd"])
-def test_full_size_workload(name):
-    _check_sampled(wl.WORKLOADS[name])
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_full_size_workload(name, schedule):
+    _check_sampled(wl.WORKLOADS[name], schedule)
 
 
 @pytest.mark.parametrize("mu", [1, 2, 4, 8])
-def test_large_swiglu_mu_sweep(mu):
-    _check_sampled(wl.WORKLOADS["large_swiglu_fwd"].with_(mu=mu))
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_large_swiglu_mu_sweep(mu, schedule):
+    _check_sampled(wl.WORKLOADS["large_swiglu_fwd"].with_(mu=mu), schedule)
+
+
+# ------------------------------------------------------- failure detection
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A device wait on a flag that nothing sets gives up after its limit, records
+    DOMINO_ERR_TIMEOUT for the host, and the next call on the GPU still works."""
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    assert b.query_device_status(ws) == 0
+    b.selftest_wait_timeout(ws, timeout_ns=50_000_000)  # 50 ms
+    assert b.query_device_status(ws) == 6  # DOMINO_ERR_TIMEOUT
+    assert "gave up" in b.lib().domino_last_error().decode()
+    assert b.query_device_status(ws) == 0  # cleared by the read
+    _check_full(wl.WORKLOADS["tiny_gelu_fwd"], schedule="fused")
