@@ -173,6 +173,25 @@ def oracle_row_sample(w, t, target_s):
         rows = int(min(w.M, max(rows * 2, rows * target_s / max(dt, 1e-3))))
 
 
+# -------------------------------------------------------------- multi-rank
+
+def max_over_ranks(value_ms, world, device=None):
+    """The slowest rank's time: every rank runs its own replica of the workload
+    (weak scaling), so the job's step time is the maximum over ranks."""
+    if world <= 1:
+        return float(value_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank, world, max_ms):
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return world * flops_per_rank / (max_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- our arm
 
 def timeline_stats(records):
@@ -270,10 +289,7 @@ def run_ours(args, w, rank, world, local_rank):
     step_ms = [s.elapsed_time(e) for s, e in ev]
     mean_ms = statistics.mean(step_ms)
     records = b.kernel_times()
-    if world > 1:
-        tt = torch.tensor([mean_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_ms = float(tt.item())
+    mean_ms = max_over_ranks(mean_ms, world, dev)
 
     # ---- fused schedule: reduction time left after the last GEMM tile, from the
     # kernel's own %globaltimer stamps (read back after each of a few extra calls)
@@ -311,10 +327,7 @@ def run_ours(args, w, rank, world, local_rank):
         ev2[i][1].record(stream)
     barrier()
     e2e_ms = statistics.mean(s.elapsed_time(e) for s, e in ev2)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     if not torch.equal(Yh, Y.cpu()):
         raise RuntimeError("end-to-end output differs from the device result")
 
@@ -355,7 +368,7 @@ def run_ours(args, w, rank, world, local_rank):
         exposed_ms = fused_exposed + (exposed_ms * (calls_per_step - 1) / calls_per_step if w.bwd else 0.0)
 
     flops = w.fwd_flops() + (w.bwd_flops() if w.bwd else 0)
-    value = world * flops / (mean_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, mean_ms)
     line = {
         "metric": "sliced TP-MLP layer TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",
         "value": round(value, 2),
@@ -403,7 +416,7 @@ def run_ours(args, w, rank, world, local_rank):
                         "share": round(v["total_ms"] / sum(x["total_ms"] for x in kinds.values()), 4)}
                     for k, v in kinds.items()},
         "gpu_launches": len(records),
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": w.M * w.d * 2 * calls_per_step,
                 "d2h_bytes_per_step": w.M * w.d * 2 * calls_per_step,
                 "ms_per_step": round(e2e_ms, 4)},

@@ -388,6 +388,8 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
       L.n_tile = swiglu ? kBN / 2 : kBN;
       L.b1_off = swiglu ? 0 : kBN / 2;
       L.ldo = s.Fp;
+      L.out_rows = s.M;
+      L.out_cols = s.Fp;
       L.ld_aux = s.Fp * s.nact;
       L.aux_u_off = s.Fp;
       L.a_row0 = row0;
@@ -416,6 +418,8 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
       L.n_tile = kBN;
       L.b1_off = kBN / 2;
       L.ldo = s.d;
+      L.out_rows = s.M;
+      L.out_cols = s.d;
       L.a_row0 = row0;
       L.out_row0 = row0;
       L.rows = static_cast<int32_t>(s.Mc);
@@ -565,6 +569,8 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
         L.out[p] = Z[p];
       }
       L.ldo = s.d;
+      L.out_rows = s.M;
+      L.out_cols = s.d;
       L.a_row0 = row0;
       L.out_row0 = row0;
       L.rows = static_cast<int32_t>(s.Mc);
@@ -611,6 +617,8 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
       L.out[p] = dA_shards[p];
     }
     L.ldo = s.d;
+    L.out_rows = nF;
+    L.out_cols = s.d;
     L.rows = static_cast<int32_t>(nF);
     L.n_base = 0;
     L.n_end = static_cast<int32_t>(s.d);
@@ -633,6 +641,8 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
       L.out[p] = dB_shards[p];
     }
     L.ldo = s.Fp;
+    L.out_rows = s.d;
+    L.out_cols = s.Fp;
     L.rows = static_cast<int32_t>(s.d);
     L.n_base = 0;
     L.n_end = static_cast<int32_t>(s.Fp);

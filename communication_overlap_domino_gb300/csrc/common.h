@@ -56,7 +56,12 @@ constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kBStageBytes = kBN * kBK * 2;
-constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256 /*barriers*/;
+// Epilogue staging for TMA stores: per epilogue warp two 4 KB buffers (a 32 x 32
+// chunk of fp32 or bf16 output), swizzled to match the store's tensor map.
+constexpr int kStageOutBytesPerWarp = 2 * 4096;
+constexpr int kStageOutBytes = 4 * kStageOutBytesPerWarp;
+constexpr int kGemmSmemBytes =
+    kStages * (kAStageBytes + kBStageBytes) + kStageOutBytes + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint32_t kTmemCols = 2 * kBN;  // double-buffered accumulator
 
 // One grouped, persistent GEMM launch: C_s = A_s * B_s^T for every shard s,
@@ -67,6 +72,7 @@ struct GemmParams {  // CUtensorMap members carry 64-byte alignment
   CUtensorMap map_a[kMaxShards];   // A operand
   CUtensorMap map_b0[kMaxShards];  // B operand rows [n0, n0+128)
   CUtensorMap map_b1[kMaxShards];  // B operand rows for accumulator columns 128..255
+  CUtensorMap map_out[kMaxShards]; // output store map (box 32 x 32), when use_tma_store
   void* out[kMaxShards];           // output matrix per shard
   void* aux[kMaxShards];           // optional copy of the pre-activation(s) (bf16), or null
   int64_t ldo;                     // leading dimension of out (elements)
@@ -82,6 +88,7 @@ struct GemmParams {  // CUtensorMap members carry 64-byte alignment
   int32_t b1_off;                  // B row of the second 128-row box relative to the first
   int32_t num_kb;                  // K blocks of 64
   int32_t tiles_m, tiles_n, num_shards, num_tiles;
+  int32_t use_tma_store;           // epilogue writes full 32 x 32 chunks through map_out
   DeviceStatus* status;
   uint64_t timeout_ns;
 };
@@ -94,6 +101,8 @@ struct FusedParams {
   CUtensorMap map_w1b[kMaxShards];   // GEMM1 B operand, accumulator columns 128..255 (SwiGLU: up)
   CUtensorMap map_h[kMaxShards];     // H_p [M, Fp], box 64 x 128
   CUtensorMap map_w2[kMaxShards];    // B_p^T [d, Fp], box 64 x 128
+  CUtensorMap map_hout[kMaxShards];  // H_p store map, box 32 x 32
+  CUtensorMap map_zout[kMaxShards];  // Z_p store map, box 32 x 32
   void* h[kMaxShards];
   void* aux[kMaxShards];             // saved pre-activations or null
   void* z[kMaxShards];               // partial outputs [M, d]

@@ -22,6 +22,8 @@ struct EpiArgs {
   int32_t rows;       // valid accumulator rows (tile rows >= rows are not stored)
   int32_t out_row0;   // output row of accumulator row 0 of tile row-block 0
   int32_t n_end;      // output columns >= n_end are not stored
+  const CUtensorMap* out_map;  // TMA store map of `out` (box 32 x 32), or null: direct stores
+  uint8_t* stage;              // this warp's two 4 KB staging buffers (1024-byte aligned)
 };
 
 // ------------------------------------------------------------------ epilogue
@@ -116,64 +118,106 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], 
   }
 }
 
+// Writes one 32-row x 32-column chunk (this lane: row `lane`, values v) through
+// shared memory and a TMA store at output coordinates (x, y).  The staging
+// layout is the store map's swizzle: 128-byte rows (fp32) with the 128-byte
+// swizzle, or 64-byte rows (bf16) with the 64-byte swizzle, so the 16-byte
+// writes of a warp spread over all banks.  Two buffers alternate; before one is
+// rewritten, lane 0 waits until the store that last read it is done reading.
+template <bool F32>
+__device__ __forceinline__ void stage_and_store(const EpiArgs& e, const float (&v)[32], int lane, int& sbuf,
+                                                int32_t x, int32_t y) {
+  uint8_t* buf = e.stage + (sbuf & 1) * 4096;
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  if constexpr (F32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 w = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                 __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+      *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+      w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+      w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+      w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+      *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = w;
+    }
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(e.out_map, buf, x, y);
+    bulk_commit_group();
+  }
+  ++sbuf;
+}
+
 // Drains one accumulator tile (this thread: one row) through the epilogue.
+// Drains one 128 x 256 accumulator tile (this thread: one row) through the
+// epilogue.  Full 32 x 32 chunks inside the valid rows and columns go out
+// through shared memory and TMA stores when e.out_map is set; edge chunks (and
+// the saved pre-activations) use direct stores.  sbuf: the warp's staging
+// buffer counter.
 template <int EPI>
-__device__ __forceinline__ void epilogue_tile(const EpiArgs& e, uint32_t tacc, int mb, int col0, int row_in_tile) {
+__device__ __forceinline__ void epilogue_tile(const EpiArgs& e, uint32_t tacc, int mb, int col0, int row_in_tile,
+                                              int& sbuf) {
+  const int lane = row_in_tile & 31;
   const int64_t grow = static_cast<int64_t>(mb) * kBM + row_in_tile;
   const bool row_ok = grow < e.rows;
   const int64_t orow = e.out_row0 + grow;
+  const int64_t warp_row0 = static_cast<int64_t>(mb) * kBM + (row_in_tile & ~31);
+  const bool warp_rows_full = warp_row0 + 32 <= e.rows;  // uniform across the warp
+  constexpr bool kF32Out = EPI == EPI_Z_F32;
   constexpr int kChunks = (EPI == EPI_H_SWIGLU) ? (kBN / 2) / 32 : kBN / 32;
 #pragma unroll 1
   for (int c = 0; c < kChunks; ++c) {
     const int col = col0 + c * 32;
     if (col >= e.n_end) break;  // uniform across the warp
     const int n = e.n_end - col;
+    const bool tma = e.out_map != nullptr && warp_rows_full && n >= 32;  // uniform
     uint32_t r0[32];
     tmem_ld_32x32b_x32(tacc + c * 32, r0);
+    float h[32];
     if constexpr (EPI == EPI_H_SWIGLU) {
       uint32_t r1[32];
       tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
       tmem_ld_wait();
-      if (row_ok) {
-        float h[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) h[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+      if (row_ok && e.aux != nullptr) {
+        float g[32], u[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float g = __uint_as_float(r0[j]);
-          const float u = __uint_as_float(r1[j]);
-          h[j] = silu(g) * u;
+          g[j] = __uint_as_float(r0[j]);
+          u[j] = __uint_as_float(r1[j]);
         }
-        store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, h, n);
-        if (e.aux != nullptr) {
-          float g[32], u[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            g[j] = __uint_as_float(r0[j]);
-            u[j] = __uint_as_float(r1[j]);
-          }
-          __nv_bfloat16* a = static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col;
-          store_row_bf16(a, g, n);
-          store_row_bf16(a + e.aux_u_off, u, n);
-        }
+        __nv_bfloat16* a = static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col;
+        store_row_bf16(a, g, n);
+        store_row_bf16(a + e.aux_u_off, u, n);
       }
     } else {
       tmem_ld_wait();
-      if (row_ok) {
-        float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
-        if constexpr (EPI == EPI_Z_F32) {
-          store_row_f32(static_cast<float*>(e.out) + orow * e.ldo + col, v, n);
-        } else if constexpr (EPI == EPI_Z_BF16) {
-          store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, v, n);
-        } else {
-          if (e.aux != nullptr)
-            store_row_bf16(static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col, v, n);
-          float h[32];
+      for (int j = 0; j < 32; ++j) h[j] = __uint_as_float(r0[j]);
+      if constexpr (EPI != EPI_Z_F32 && EPI != EPI_Z_BF16) {
+        if (row_ok && e.aux != nullptr)
+          store_row_bf16(static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col, h, n);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(v[j]);
-          store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, h, n);
-        }
+        for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(h[j]);
       }
+    }
+    if (tma) {
+      stage_and_store<kF32Out>(e, h, lane, sbuf, col, static_cast<int32_t>(e.out_row0 + warp_row0));
+    } else if (row_ok) {
+      if constexpr (kF32Out)
+        store_row_f32(static_cast<float*>(e.out) + orow * e.ldo + col, h, n);
+      else
+        store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, h, n);
     }
   }
 }

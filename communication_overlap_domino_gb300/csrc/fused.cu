@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + kStages * kAStageBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + kStages * kBStageBytes);
+  uint8_t* smem_out = smem_b + kStages * kBStageBytes;  // epilogue staging, 4 warps x 8 KB
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_out + kStageOutBytes);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* tfull_bar = empty_bar + kStages;
   uint64_t* tempty_bar = tfull_bar + 2;
@@ -421,6 +422,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    uint8_t* stage = smem_out + (warp - 2) * kStageOutBytesPerWarp;
+    int sbuf = 0;
     int i = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
       const uint32_t acc = i & 1;
@@ -431,20 +434,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
       if (T.phase == 0) {
         const EpiArgs e{f.h[T.p], f.aux[T.p], f.Fp, f.ld_aux, f.aux_u_off, 0,
-                        f.Mc, static_cast<int32_t>(T.k * f.Mc), static_cast<int32_t>(f.Fp)};
-        epilogue_tile<EPI_A>(e, tacc, T.m, T.n * f.n_tile1, row_in_tile);
+                        f.Mc, static_cast<int32_t>(T.k * f.Mc), static_cast<int32_t>(f.Fp),
+                        &f.map_hout[T.p], stage};
+        epilogue_tile<EPI_A>(e, tacc, T.m, T.n * f.n_tile1, row_in_tile, sbuf);
         tc_fence_before_sync();
         mbar_arrive(&tempty_bar[acc]);
+        // publish: the TMA stores of this quarter are complete, then release the counter
+        if (lane == 0) bulk_wait_group<0>();
         fence_proxy_async_global();
         __threadfence();
         __syncwarp();
         if (lane == 0) red_release_gpu_add(f.hcnt + (T.k * f.P + T.p) * f.tiles_m + T.m, 1);
       } else {
         const EpiArgs e{f.z[T.p], nullptr, f.d, 0, 0, 0, f.Mc, static_cast<int32_t>(T.k * f.Mc),
-                        static_cast<int32_t>(f.d)};
-        epilogue_tile<EPI_B>(e, tacc, T.m, T.n * kBN, row_in_tile);
+                        static_cast<int32_t>(f.d), &f.map_zout[T.p], stage};
+        epilogue_tile<EPI_B>(e, tacc, T.m, T.n * kBN, row_in_tile, sbuf);
         tc_fence_before_sync();
         mbar_arrive(&tempty_bar[acc]);
+        if (lane == 0) bulk_wait_group<0>();
+        fence_proxy_async_global();
         __threadfence();
         __syncwarp();
         if (lane == 0)
@@ -530,6 +538,8 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, cudaStream_
     if (!encode_bf16_sw128(&f.map_h[p], Operand2D{L.H[p], L.M, Fp, Fp}, kBM, err)) return DOMINO_ERR_CUDA;
     if (!encode_bf16_sw128(&f.map_w2[p], Operand2D{L.B_shards[p], L.d, Fp, Fp}, kBN / 2, err))
       return DOMINO_ERR_CUDA;
+    if (!encode_store_map(&f.map_hout[p], L.H[p], L.M, Fp, Fp, false, err)) return DOMINO_ERR_CUDA;
+    if (!encode_store_map(&f.map_zout[p], L.Z[p], L.M, L.d, L.d, L.partial_f32, err)) return DOMINO_ERR_CUDA;
     f.h[p] = L.H[p];
     f.aux[p] = L.aux[p];
     f.z[p] = L.Z[p];

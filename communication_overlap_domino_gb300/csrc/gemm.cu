@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;
   uint8_t* smem_b = smem + kStages * kAStageBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_b + kStages * kBStageBytes);
+  uint8_t* smem_out = smem_b + kStages * kBStageBytes;  // epilogue staging, 4 warps x 8 KB
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_out + kStageOutBytes);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* tfull_bar = empty_bar + kStages;
   uint64_t* tempty_bar = tfull_bar + 2;
@@ -195,6 +196,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    uint8_t* stage = smem_out + (warp - 2) * kStageOutBytesPerWarp;
+    int sbuf = 0;
     int i = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
       const uint32_t acc = i & 1;
@@ -205,15 +208,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
       tile_coords(p, t, shard, mb, nb);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
       const EpiArgs e{p.out[shard], p.aux[shard], p.ldo, p.ld_aux, p.aux_u_off, p.out_u_off,
-                      p.rows, p.out_row0, p.n_end};
+                      p.rows, p.out_row0, p.n_end, p.use_tma_store ? &p.map_out[shard] : nullptr, stage};
       const int col0 = p.n_base + nb * p.n_tile;
       if constexpr (is_dg(EPI))
         epilogue_tile_dg<EPI>(e, tacc, mb, col0, row_in_tile);
       else
-        epilogue_tile<EPI>(e, tacc, mb, col0, row_in_tile);
+        epilogue_tile<EPI>(e, tacc, mb, col0, row_in_tile, sbuf);
       tc_fence_before_sync();
       mbar_arrive(&tempty_bar[acc]);
     }
+    if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA releases its shared memory
   }
 
   __syncwarp();
@@ -315,6 +319,34 @@ bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std:
   return true;
 }
 
+// TMA store map of a row-major output [rows, cols] (leading dimension ld
+// elements): box 32 x 32, 128-byte swizzle for fp32 (128-byte rows), 64-byte
+// swizzle for bf16 (64-byte rows), matching stage_and_store's staging layout.
+bool encode_store_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool f32,
+                      std::string* err) {
+  EncodeTiledFn enc = get_encode_fn(err);
+  if (!enc) return false;
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (err) {
+      char buf[256];
+      snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (store) failed (%d) rows=%lld cols=%lld ld=%lld", (int)r,
+               (long long)rows, (long long)cols, (long long)ld);
+      *err = buf;
+    }
+    return false;
+  }
+  return true;
+}
+
 cudaError_t prepare_gemm_kernels() {
   int n = 0;
   const KernelEntry* t = kernel_table(&n);
@@ -340,6 +372,14 @@ domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stre
     if (!encode_bf16_sw128(&p.map_b1[s], L.b1[s], b_box, err)) return DOMINO_ERR_CUDA;
     p.out[s] = L.out[s];
     p.aux[s] = L.aux[s];
+  }
+  const bool store_epi = L.epi == EPI_H_GELU || L.epi == EPI_H_GELU_TANH || L.epi == EPI_H_IDENTITY ||
+                         L.epi == EPI_H_SWIGLU || L.epi == EPI_Z_F32 || L.epi == EPI_Z_BF16;
+  if (store_epi && L.out_rows > 0 && L.out_cols > 0) {
+    for (int s = 0; s < L.num_shards; ++s)
+      if (!encode_store_map(&p.map_out[s], L.out[s], L.out_rows, L.out_cols, L.ldo, L.epi == EPI_Z_F32, err))
+        return DOMINO_ERR_CUDA;
+    p.use_tma_store = 1;
   }
   p.ldo = L.ldo;
   p.ld_aux = L.ld_aux;

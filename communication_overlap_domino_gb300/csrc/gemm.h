@@ -34,6 +34,7 @@ struct GemmLaunch {
   void* out[kMaxShards] = {};
   void* aux[kMaxShards] = {};
   int64_t ldo = 0, ld_aux = 0, aux_u_off = 0, out_u_off = 0;
+  int64_t out_rows = 0, out_cols = 0;  // extent of each out[s]; 0: no TMA stores (direct stores only)
   int32_t a_row0 = 0, out_row0 = 0, rows = 0;
   int32_t n_base = 0, n_end = 0, n_tile = kBN, b1_off = kBN / 2;
   int64_t K = 0;
@@ -43,6 +44,8 @@ struct GemmLaunch {
 
 cudaError_t prepare_gemm_kernels();
 bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err);
+bool encode_store_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool f32,
+                      std::string* err);
 domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
 
 // The fused forward pass (fused.cu).
