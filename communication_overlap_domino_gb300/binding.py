@@ -22,6 +22,7 @@ PARTIAL = {"f32": 0, "bf16": 1}
 SCHEDULE = {"serial": 0, "streams": 1, "fused": 2}
 KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused"}
 FLAG_KERNEL_TIMES = 1
+FLAG_ONE_CTA = 2
 MAX_SHARDS = 16
 
 
@@ -118,10 +119,13 @@ def _ptr_array(ptrs: Sequence[int]):
 
 
 def make_desc(M: int, d: int, F: int, P: int, mu: int, act: str, partial: str, out_slices: int = 1,
-              schedule: str = "streams", kernel_times: bool = False, timeout_ns: int = 0) -> MlpDesc:
+              schedule: str = "streams", kernel_times: bool = False, timeout_ns: int = 0,
+              pair_cta: bool = True) -> MlpDesc:
+    """pair_cta: run the separate-launch GEMMs as paired-CTA 256x256 tiles (default) or,
+    if False, as one-CTA 128x256 tiles."""
+    flags = (FLAG_KERNEL_TIMES if kernel_times else 0) | (0 if pair_cta else FLAG_ONE_CTA)
     return MlpDesc(M=M, d=d, F=F, P=P, mu=mu, out_slices=out_slices, act=ACT[act], partial_dtype=PARTIAL[partial],
-                   schedule=SCHEDULE[schedule], flags=FLAG_KERNEL_TIMES if kernel_times else 0, reserved=0,
-                   timeout_ns=timeout_ns)
+                   schedule=SCHEDULE[schedule], flags=flags, reserved=0, timeout_ns=timeout_ns)
 
 
 def workspace_size(desc: MlpDesc, with_bwd: bool = False) -> int:
@@ -192,12 +196,12 @@ def shard_weights(A, B, P: int):
 
 def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str, out_slices: int = 1,
             schedule: str = "streams", Y=None, saved=None, workspace=None, stream=None, kernel_times: bool = False,
-            timeout_ns: int = 0):
+            timeout_ns: int = 0, pair_cta: bool = True):
     """domino_mlp_fwd on torch tensors; returns Y [M, d] bf16."""
     torch = _torch()
     M, d = X.shape
     P = len(A_shards)
-    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
     if Y is None:
         Y = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
     need = workspace_size(desc)
@@ -215,14 +219,14 @@ def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, par
 
 def mlp_bwd(X, A_shards: List, B_shards: List, dY, saved, *, F: int, mu: int, act: str, partial: str,
             out_slices: int = 1, schedule: str = "streams", dX=None, dA_shards=None, dB_shards=None, workspace=None,
-            stream=None, kernel_times: bool = False, timeout_ns: int = 0):
+            stream=None, kernel_times: bool = False, timeout_ns: int = 0, pair_cta: bool = True):
     """domino_mlp_bwd on torch tensors; returns (dX, dA_shards, dB_shards).
 
     `saved` must be the buffer a domino_mlp_fwd call with the same inputs filled."""
     torch = _torch()
     M, d = X.shape
     P = len(A_shards)
-    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
     if dX is None:
         dX = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
     if dA_shards is None:

@@ -50,7 +50,9 @@ struct TimedLaunch {
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
-  int fused_max_ctas = 0;  // co-resident CTAs of the fused kernel (cooperative launch limit)
+  int fused_max_ctas = 0;     // co-resident CTAs of the fused kernel (cooperative launch limit)
+  int pair_max_clusters = 0;  // co-resident 2-CTA clusters of the paired GEMM
+  int fused_pair_clusters = 0;  // co-resident 2-CTA clusters of the paired fused kernel (0: not usable)
   cudaStream_t reduce_stream = nullptr;
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join = nullptr;
@@ -87,8 +89,9 @@ domino_status_t device_state(DeviceState** out) {
     }
     e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = prepare_gemm_kernels();
+    if (e == cudaSuccess) e = prepare_pair_kernels(&ds.pair_max_clusters);
     int per_sm = 0;
-    if (e == cudaSuccess) e = prepare_fused_kernels(&per_sm);
+    if (e == cudaSuccess) e = prepare_fused_kernels(&per_sm, &ds.fused_pair_clusters);
     ds.fused_max_ctas = per_sm * ds.num_sms;
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ds.reduce_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_fork, cudaEventDisableTiming);
@@ -125,7 +128,8 @@ domino_status_t check_desc(const domino_mlp_desc_t* desc, Shape* s) {
       d.schedule != DOMINO_SCHEDULE_FUSED)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
   if (d.reserved != 0) return fail(DOMINO_ERR_INVALID_ARG, "reserved must be 0");
-  if ((d.flags & ~DOMINO_FLAG_KERNEL_TIMES) != 0) return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
+  if ((d.flags & ~(DOMINO_FLAG_KERNEL_TIMES | DOMINO_FLAG_ONE_CTA)) != 0)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
   if (static_cast<int64_t>(d.mu) * d.out_slices > DOMINO_MAX_PIECES)
     return fail(DOMINO_ERR_UNSUPPORTED, "mu * out_slices exceeds DOMINO_MAX_PIECES");
   if (d.F % d.P) return fail(DOMINO_ERR_UNSUPPORTED, "P must divide F");
@@ -232,6 +236,11 @@ domino_status_t timed(Timer& T, cudaStream_t st, int32_t stream_id, int32_t kind
   return r;
 }
 
+// One grouped GEMM launch, as one-CTA tiles or as paired-CTA clusters.
+domino_status_t run_gemm(const GemmLaunch& L, const DeviceState* ds, bool pair, cudaStream_t st, std::string* err) {
+  return pair ? launch_gemm_pair(L, ds->pair_max_clusters, st, err) : launch_gemm(L, ds->num_sms, st, err);
+}
+
 }  // namespace
 
 namespace domino {
@@ -305,6 +314,7 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
   Timer T;
   T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
   T.ds = ds;
+  const bool pair = (desc->flags & DOMINO_FLAG_ONE_CTA) == 0 && ds->pair_max_clusters > 0;
   if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
 
   // Where H and the saved pre-activations go.
@@ -354,8 +364,17 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
     if (e == cudaSuccess) e = cudaMemsetAsync(F.timeline, 0xFF, 8, s0);
     if (e == cudaSuccess) e = cudaMemsetAsync(F.timeline + 1, 0, 16, s0);
     if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("counter reset: ") + cudaGetErrorString(e));
-    st = timed(T, s0, 0, DOMINO_KERNEL_FUSED, 0, 0,
-               [&] { return launch_fused_fwd(F, ds->fused_max_ctas, s0, &err); });
+    F.pair = pair;
+    st = timed(T, s0, 0, DOMINO_KERNEL_FUSED, 0, 0, [&] {
+      domino_status_t r = launch_fused_fwd(F, ds->fused_max_ctas, ds->fused_pair_clusters, s0, &err);
+      if (r == DOMINO_ERR_UNSUPPORTED && F.pair) {
+        // paired cooperative launches refused on this device: use one-CTA tiles from now on
+        ds->fused_pair_clusters = 0;
+        F.pair = false;
+        r = launch_fused_fwd(F, ds->fused_max_ctas, 0, s0, &err);
+      }
+      return r;
+    });
     if (st != DOMINO_OK) return fail(st, err);
     return DOMINO_OK;
   }
@@ -400,7 +419,7 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
       L.K = s.d;
       L.status = dstat;
       L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
       if (st != DOMINO_OK) return fail(st, err);
     }
     for (int sl = 0; sl < s.S; ++sl) {
@@ -428,7 +447,7 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
       L.K = s.Fp;
       L.status = dstat;
       L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return run_gemm(L, ds, pair, s0, &err); });
       if (st != DOMINO_OK) return fail(st, err);
 
       // ---- shard-sum of piece (k, s)
@@ -505,6 +524,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   Timer T;
   T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
   T.ds = ds;
+  const bool pair = (desc->flags & DOMINO_FLAG_ONE_CTA) == 0 && ds->pair_max_clusters > 0;
   if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
 
   const int64_t nF = s.nact * s.Fp;  // columns of the pre-activation block / rows of A_shards[p]
@@ -552,7 +572,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
       L.K = s.d;
       L.status = dstat;
       L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DH, k, 0, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DH, k, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
       if (st != DOMINO_OK) return fail(st, err);
     }
     for (int sl = 0; sl < s.S; ++sl) {
@@ -579,7 +599,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
       L.K = nF;
       L.status = dstat;
       L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return run_gemm(L, ds, pair, s0, &err); });
       if (st != DOMINO_OK) return fail(st, err);
       // ---- dX_k[:, s] = sum_p of the partials (the all-reduce of the input gradient)
       if (sr != s0) {
@@ -625,7 +645,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
     L.K = s.M;
     L.status = dstat;
     L.timeout_ns = tmo;
-    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
     if (st != DOMINO_OK) return fail(st, err);
   }
   {
@@ -649,7 +669,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
     L.K = s.M;
     L.status = dstat;
     L.timeout_ns = tmo;
-    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return launch_gemm(L, ds->num_sms, s0, &err); });
+    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return run_gemm(L, ds, pair, s0, &err); });
     if (st != DOMINO_OK) return fail(st, err);
   }
   if (sr != s0) {

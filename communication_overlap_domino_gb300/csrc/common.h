@@ -118,6 +118,8 @@ struct FusedParams {
   int32_t tiles_m, tiles_n1, tiles_n2;
   int32_t tiles_a, tiles_b;          // GEMM1 / GEMM2 tiles per chunk (all shards)
   int32_t num_gemm_tiles, num_red_items;
+  int32_t tiles_m2, tiles_a2, tiles_b2;  // paired kernel: 256-row blocks, tiles per chunk and phase
+  int32_t num_pair_tiles;
   int32_t kb1, kb2;                  // K blocks of GEMM1 (d) and GEMM2 (Fp)
   DeviceStatus* status;
   uint64_t timeout_ns;

@@ -20,9 +20,9 @@
 //     TMA producer polls it before loading H (then a proxy fence orders the
 //     generic-proxy stores before its async-proxy reads).
 //   shard-sum of (k, m, n), quarter q: zcnt[k][m][n][q] counts the GEMM2 tiles
-//     whose quarter q is stored (target P).  These 32-row pieces are taken from
-//     a kernel-wide queue (an atomic ticket) by the reducer warps, and by the
-//     epilogue warps once their GEMM tiles are done.
+//     whose quarter q is stored (target P).  The shard-sum runs in 8-row pieces
+//     taken from a kernel-wide queue (an atomic ticket) by the reducer warps,
+//     and by every other warp once its own role is done.
 // GEMM tiles never wait on the reducers and a GEMM2 tile only waits on GEMM1
 // tiles earlier in the global order, so with all CTAs resident (the cooperative
 // launch guarantees it) every wait ends; each is still bounded by timeout_ns.
@@ -111,6 +111,25 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
     T.phase = 1;
     const int G = T.k == f.mu - 1 ? (f.tiles_m < kLastChunkGroupM ? f.tiles_m : kLastChunkGroupM) : f.tiles_m;
     grouped_coords(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+  }
+  return T;
+}
+
+// Paired kernel: tiles of 256 rows (T.m counts 256-row blocks; the even CTA
+// owns 128-row block 2*T.m, the odd one 2*T.m + 1), same order as above.
+__device__ __forceinline__ FusedTile fused_pair_tile(const FusedParams& f, int t) {
+  FusedTile T;
+  const int per_chunk = f.tiles_a2 + f.tiles_b2;
+  T.k = t / per_chunk;
+  int r = t - T.k * per_chunk;
+  if (r < f.tiles_a2) {
+    T.phase = 0;
+    grouped_coords(r, f.tiles_m2, f.P, f.tiles_m2, f.tiles_n1, T.p, T.m, T.n);
+  } else {
+    T.phase = 1;
+    const int g2 = kLastChunkGroupM / 2;
+    const int G = T.k == f.mu - 1 ? (f.tiles_m2 < g2 ? f.tiles_m2 : g2) : f.tiles_m2;
+    grouped_coords(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
   }
   return T;
 }
@@ -245,30 +264,38 @@ __device__ __forceinline__ void reduce_dispatch(const FusedParams& f, int64_t ro
   }
 }
 
-// Takes reduction pieces (32 rows x 256 columns of one output tile: the zcnt
-// entry j) from the kernel-wide queue in order and sums each one once its P
-// partials are stored.  Run by the reducer warps from the start and by the
-// epilogue warps once their own GEMM tiles are done (so a piece never waits on
-// work of the warp that holds it).  Returns false if a wait gave up.
+// Takes reduction pieces (8 rows x 256 columns of one output tile) from the
+// kernel-wide queue in order and sums each one once the P partials of its
+// 32-row quarter (counter zcnt[j / 4]) are stored.  Pieces are small so that
+// the last ones, which nothing else overlaps, finish quickly: one warp keeps
+// about 8 KB of loads in flight.  Run by the reducer warps from the start and by
+// every other warp once its own role is done (so a piece never waits on work of
+// the warp that holds it).  Returns false if a wait gave up.
+constexpr int kPieceRows = 8;
+
 template <bool F32>
 __device__ __forceinline__ bool run_reduction_pieces(const FusedParams& f, volatile int* abort, int lane) {
-  const int num_pieces = f.num_red_items * 4;
+  constexpr int kPiecesPerQuarter = 32 / kPieceRows;
+  const int num_pieces = f.num_red_items * 4 * kPiecesPerQuarter;
   const int per_k = f.tiles_m * f.tiles_n2;
   while (!*abort) {
     int j = 0;
     if (lane == 0) j = static_cast<int>(atomicAdd(f.red_next, 1u));
     j = __shfl_sync(0xffffffffu, j, 0);
     if (j >= num_pieces) break;
-    const int item = j >> 2, q = j & 3;
+    const int quarter_id = j / kPiecesPerQuarter;  // index into zcnt
+    const int sub = j - quarter_id * kPiecesPerQuarter;
+    const int item = quarter_id >> 2, q = quarter_id & 3;
     const int k = item / per_k;
     const int r = item - k * per_k;
     const int m = r / f.tiles_n2;
     const int n = r - m * f.tiles_n2;
-    if (!wait_counter(f.zcnt + j, static_cast<uint32_t>(f.P), abort, f.timeout_ns, f.status, kSiteFusedZ, j))
+    if (!wait_counter(f.zcnt + quarter_id, static_cast<uint32_t>(f.P), abort, f.timeout_ns, f.status, kSiteFusedZ,
+                      quarter_id))
       return false;
-    const int row_lo = m * kBM + q * 32;
+    const int row_lo = m * kBM + q * 32 + sub * kPieceRows;
     int nrows = f.Mc - row_lo;
-    nrows = nrows > 32 ? 32 : nrows;
+    nrows = nrows > kPieceRows ? kPieceRows : nrows;
     const int64_t col = static_cast<int64_t>(n) * kBN + lane * 8;
     if (nrows > 0 && col < f.d) reduce_dispatch<F32>(f, static_cast<int64_t>(k) * f.Mc + row_lo, nrows, col);
     __syncwarp();
@@ -471,6 +498,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
   }
 
   __syncwarp();
+  if (warp < 2) {
+    // the producer and MMA warps join the shard-sum once their roles are done
+    run_reduction_pieces<EPI_B == EPI_Z_F32>(f, abort_flag, lane);
+  }
+  __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -480,9 +512,254 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
   }
 }
 
+
+// The fused forward pass with paired-CTA tiles: each 2-CTA cluster computes
+// 256-row tiles with tcgen05 cta_group::2 MMAs issued by its even CTA (see
+// gemm_pair.cu for the operand split and the barrier protocol).  Each CTA's
+// epilogue drains, stores and publishes its own 128-row block, so the counters
+// and the shard-sum pieces are the same as in the one-CTA kernel.  The odd
+// CTA's warp 1, which issues no MMAs, works on the shard-sum from the start.
+template <int EPI_A, int EPI_B>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
+    fused_fwd_pair_kernel(const __grid_constant__ FusedParams f) {
+  constexpr int kPStages = 6;
+  constexpr int kPA = 128 * kBK * 2, kPB = 128 * kBK * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem_a = smem;
+  uint8_t* smem_b = smem + kPStages * kPA;
+  uint8_t* smem_out = smem_b + kPStages * kPB;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem_out + kStageOutBytes);
+  uint64_t* empty_bar = full_bar + kPStages;
+  uint64_t* tfull_bar = empty_bar + kPStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* final_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 2 * 4 * 32);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    atomicMin(reinterpret_cast<unsigned long long*>(&f.timeline[0]),
+              static_cast<unsigned long long>(globaltimer_ns()));
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_alloc_permit_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = f.num_pair_tiles;
+  const uint64_t tmo = f.timeout_ns;
+  const int num_clusters = gridDim.x >> 1;
+  const int cluster_id = blockIdx.x >> 1;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    prefetch_tmap(&f.map_x);
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
+    for (int t = cluster_id; t < num_tiles && !*abort_flag; t += num_clusters) {
+      const FusedTile T = fused_pair_tile(f, t);
+      const int m = 2 * T.m + static_cast<int>(rank);  // this CTA's 128-row block
+      const CUtensorMap *ma, *mb;
+      int ya, yb, nkb;
+      if (T.phase == 0) {
+        ma = &f.map_x;
+        mb = leader ? &f.map_w1a[T.p] : &f.map_w1b[T.p];
+        ya = T.k * f.Mc + m * kBM;
+        yb = T.n * f.n_tile1 + (leader ? 0 : f.b1_off1);
+        nkb = f.kb1;
+      } else {
+        if (m < f.tiles_m) {
+          const uint32_t* ctr = f.hcnt + (T.k * f.P + T.p) * f.tiles_m + m;
+          if (!wait_counter(ctr, static_cast<uint32_t>(f.tiles_n1) * 4, abort_flag, tmo, f.status, kSiteFusedH, t))
+            break;
+          fence_proxy_async_global();
+        }
+        ma = &f.map_h[T.p];
+        mb = &f.map_w2[T.p];
+        ya = T.k * f.Mc + m * kBM;
+        yb = T.n * kBN + (leader ? 0 : kBN / 2);
+        nkb = f.kb2;
+      }
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, tmo, f.status, kSiteProducerEmpty, t)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem_a + stage * kPA;
+        uint8_t* sb = smem_b + stage * kPB;
+        if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * (kPA + kPB));
+        const uint32_t bar = full0 + stage * 8;
+        const int k0 = kb * kBK;
+        tma_load_2d_pair(sa, ma, bar, k0, ya);
+        tma_load_2d_pair(sb, mb, bar, k0, yb);
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kPStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+    if (leader) {
+      for (int s = 0; s < kPStages; ++s) {
+        if (issued_mask & (1u << s)) {
+          volatile int no_abort = 0;
+          mbar_wait_cluster(&full_bar[s], (issued_parity >> s) & 1u, &no_abort, tmo, f.status, kSiteDrain, s);
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------- MMA issuer (even CTA)
+    constexpr uint32_t idesc = idesc_bf16_f32(256, kBN);
+    uint32_t stage = 0, phase = 0;
+    int i = 0;
+    for (int t = cluster_id; t < num_tiles && !*abort_flag; t += num_clusters, ++i) {
+      const FusedTile T = fused_pair_tile(f, t);
+      const int nkb = T.phase == 0 ? f.kb1 : f.kb2;
+      const uint32_t acc = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1, abort_flag, tmo, f.status, kSiteMmaTmemEmpty, t)) break;
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + acc * kBN;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag, tmo, f.status, kSiteMmaFull, t)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t adesc = smem_desc_k128(smem_u32(smem_a + stage * kPA));
+        const uint64_t bdesc = smem_desc_k128(smem_u32(smem_b + stage * kPB));
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          mma_bf16_ss_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+        mma_commit_pair_multicast(&empty_bar[stage], 0x3);
+        if (++stage == kPStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair_multicast(&tfull_bar[acc], 0x3);
+    }
+    mma_commit_pair_multicast(final_bar, 0x1);
+    volatile int no_abort = 0;
+    mbar_wait(final_bar, 0, &no_abort, tmo, f.status, kSiteDrain, 99);
+  } else if (warp >= 2 && warp < kFirstReducerWarp) {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    uint8_t* stage = smem_out + (warp - 2) * kStageOutBytesPerWarp;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty_bar[0]), 0);
+    int sbuf = 0;
+    int i = 0;
+    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++i) {
+      const uint32_t acc = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, tmo, f.status, kSiteEpilogueTmemFull, t)) break;
+      tc_fence_after_sync();
+      const FusedTile T = fused_pair_tile(f, t);
+      const int m = 2 * T.m + static_cast<int>(rank);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+      if (T.phase == 0) {
+        const EpiArgs e{f.h[T.p], f.aux[T.p], f.Fp, f.ld_aux, f.aux_u_off, 0,
+                        f.Mc, static_cast<int32_t>(T.k * f.Mc), static_cast<int32_t>(f.Fp),
+                        &f.map_hout[T.p], stage};
+        epilogue_tile<EPI_A>(e, tacc, m, T.n * f.n_tile1, row_in_tile, sbuf);
+      } else {
+        const EpiArgs e{f.z[T.p], nullptr, f.d, 0, 0, 0, f.Mc, static_cast<int32_t>(T.k * f.Mc),
+                        static_cast<int32_t>(f.d), &f.map_zout[T.p], stage};
+        epilogue_tile<EPI_B>(e, tacc, m, T.n * kBN, row_in_tile, sbuf);
+      }
+      tc_fence_before_sync();
+      if (leader)
+        mbar_arrive(&tempty_bar[acc]);
+      else
+        mbar_arrive_cluster(tempty_leader + acc * 8);
+      if (m < f.tiles_m) {
+        // publish: this quarter's stores are complete, then release its counter
+        if (lane == 0) bulk_wait_group<0>();
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          if (T.phase == 0)
+            red_release_gpu_add(f.hcnt + (T.k * f.P + T.p) * f.tiles_m + m, 1);
+          else
+            red_release_gpu_add(
+                f.zcnt + ((static_cast<int64_t>(T.k) * f.tiles_m + m) * f.tiles_n2 + T.n) * 4 + quarter, 1);
+        }
+      }
+    }
+    if (lane == 0) {
+      bulk_wait_group<0>();
+      atomicMax(reinterpret_cast<unsigned long long*>(&f.timeline[1]),
+                static_cast<unsigned long long>(globaltimer_ns()));
+    }
+    __syncwarp();
+    run_reduction_pieces<EPI_B == EPI_Z_F32>(f, abort_flag, lane);
+  } else if (warp >= kFirstReducerWarp || (warp == 1 && !leader)) {
+    // -------------------------------------------------------------- reducers
+    run_reduction_pieces<EPI_B == EPI_Z_F32>(f, abort_flag, lane);
+  }
+
+  __syncwarp();
+  if (warp == 0 || (warp == 1 && leader)) run_reduction_pieces<EPI_B == EPI_Z_F32>(f, abort_flag, lane);
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 template <int A, int B>
 void* fused_ptr() {
   return reinterpret_cast<void*>(&fused_fwd_kernel<A, B>);
+}
+
+template <int A, int B>
+void* fused_pair_ptr() {
+  return reinterpret_cast<void*>(&fused_fwd_pair_kernel<A, B>);
+}
+
+void* fused_pair_kernel_for(int epi_a, bool f32) {
+  switch (epi_a) {
+    case EPI_H_GELU: return f32 ? fused_pair_ptr<EPI_H_GELU, EPI_Z_F32>() : fused_pair_ptr<EPI_H_GELU, EPI_Z_BF16>();
+    case EPI_H_GELU_TANH:
+      return f32 ? fused_pair_ptr<EPI_H_GELU_TANH, EPI_Z_F32>() : fused_pair_ptr<EPI_H_GELU_TANH, EPI_Z_BF16>();
+    case EPI_H_IDENTITY:
+      return f32 ? fused_pair_ptr<EPI_H_IDENTITY, EPI_Z_F32>() : fused_pair_ptr<EPI_H_IDENTITY, EPI_Z_BF16>();
+    case EPI_H_SWIGLU:
+      return f32 ? fused_pair_ptr<EPI_H_SWIGLU, EPI_Z_F32>() : fused_pair_ptr<EPI_H_SWIGLU, EPI_Z_BF16>();
+    default: return nullptr;
+  }
 }
 
 void* fused_kernel_for(int epi_a, bool f32) {
@@ -505,8 +782,25 @@ size_t fused_sync_bytes(int64_t Mc, int64_t d, int P, int mu) {
   return static_cast<size_t>(4 * (mu * P * tiles_m + mu * tiles_m * tiles_n2 * 4 + 1));
 }
 
-cudaError_t prepare_fused_kernels(int* max_ctas_per_sm) {
+cudaError_t prepare_fused_kernels(int* max_ctas_per_sm, int* max_pair_clusters) {
   const int epis[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_IDENTITY, EPI_H_SWIGLU};
+  int clusters = 1 << 30;
+  for (int a = 0; a < 4; ++a) {
+    for (int f32 = 0; f32 < 2; ++f32) {
+      void* fn = fused_pair_kernel_for(epis[a], f32 != 0);
+      cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+      if (st != cudaSuccess) return st;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * 512);
+      cfg.blockDim = dim3(kFusedThreads);
+      cfg.dynamicSmemBytes = kGemmSmemBytes;
+      int n = 0;
+      st = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+      if (st != cudaSuccess) return st;
+      clusters = n < clusters ? n : clusters;
+    }
+  }
+  *max_pair_clusters = clusters;
   int occ = 1 << 30;
   for (int a = 0; a < 4; ++a) {
     for (int f32 = 0; f32 < 2; ++f32) {
@@ -523,7 +817,8 @@ cudaError_t prepare_fused_kernels(int* max_ctas_per_sm) {
   return cudaSuccess;
 }
 
-domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, cudaStream_t stream, std::string* err) {
+domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pair_clusters, cudaStream_t stream,
+                                 std::string* err) {
   FusedParams f;
   memset(&f, 0, sizeof f);
   const int64_t Fp = L.Fp;
@@ -567,9 +862,33 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, cudaStream_
   f.num_red_items = L.mu * f.tiles_m * f.tiles_n2;
   f.kb1 = static_cast<int32_t>((L.d + kBK - 1) / kBK);
   f.kb2 = static_cast<int32_t>((Fp + kBK - 1) / kBK);
+  f.tiles_m2 = (f.tiles_m + 1) / 2;
+  f.tiles_a2 = L.P * f.tiles_m2 * f.tiles_n1;
+  f.tiles_b2 = L.P * f.tiles_m2 * f.tiles_n2;
+  f.num_pair_tiles = L.mu * (f.tiles_a2 + f.tiles_b2);
   f.status = L.status;
   f.timeout_ns = L.timeout_ns;
   if (f.num_gemm_tiles == 0) return DOMINO_OK;
+  if (L.pair && max_pair_clusters > 0) {
+    // paired tiles: 2-CTA clusters, launched cooperatively (all CTAs resident)
+    void* fn = fused_pair_kernel_for(L.epi_a, L.partial_f32);
+    const int clusters = f.num_pair_tiles < max_pair_clusters ? f.num_pair_tiles : max_pair_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&f};
+    cudaError_t st = cudaLaunchKernelExC(&cfg, fn, args);
+    if (st == cudaSuccess) return DOMINO_OK;
+    if (err) *err = std::string("paired fused launch: ") + cudaGetErrorString(st);
+    return DOMINO_ERR_UNSUPPORTED;
+  }
   void* fn = fused_kernel_for(L.epi_a, L.partial_f32);
   if (!fn) {
     if (err) *err = "launch_fused_fwd: bad activation";

@@ -43,6 +43,9 @@ struct GemmLaunch {
 };
 
 cudaError_t prepare_gemm_kernels();
+cudaError_t prepare_pair_kernels(int* max_clusters);
+// Paired-CTA GEMM (gemm_pair.cu): same launch description, 2-CTA clusters.
+domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStream_t stream, std::string* err);
 bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err);
 bool encode_store_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool f32,
                       std::string* err);
@@ -63,12 +66,15 @@ struct FusedLaunch {
   int mu = 1, P = 1;
   int epi_a = EPI_H_GELU;
   bool partial_f32 = true;
+  bool pair = false;  // paired-CTA tiles (2-CTA clusters)
   DeviceStatus* status = nullptr;
   uint64_t timeout_ns = 0;
 };
 size_t fused_sync_bytes(int64_t Mc, int64_t d, int P, int mu);
-cudaError_t prepare_fused_kernels(int* max_ctas_per_sm);
-domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
+cudaError_t prepare_fused_kernels(int* max_ctas_per_sm, int* max_pair_clusters);
+// Returns DOMINO_ERR_UNSUPPORTED (with nothing launched) if a paired launch is refused.
+domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pair_clusters, cudaStream_t stream,
+                                 std::string* err);
 
 // Records a detailed message for domino_last_error() (api.cu).
 void set_last_error(const std::string& msg);

@@ -105,7 +105,11 @@ typedef enum domino_schedule {
 
 /* desc->flags */
 #define DOMINO_FLAG_KERNEL_TIMES 1u /* record CUDA events around every launch; read them
-                                       back with domino_last_kernel_times()             */
+                                       back with domino_kernel_times()                  */
+#define DOMINO_FLAG_ONE_CTA 2u      /* SERIAL/STREAMS schedules (and the backward) run their
+                                       GEMMs as 2-CTA clusters computing 256x256 tiles with
+                                       paired tensor-core MMAs (tcgen05 cta_group::2); this
+                                       flag selects one-CTA 128x256 tiles instead          */
 
 typedef struct domino_mlp_desc {
   int64_t M;              /* tokens (rows of X and Y), >= 0                      */
