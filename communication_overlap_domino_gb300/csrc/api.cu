@@ -561,6 +561,8 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
         L.aux[p] = const_cast<void*>(pre[p]);
       }
       L.ldo = nF;
+      L.out_rows = s.M;
+      L.out_cols = nF;
       L.ld_aux = nF;
       L.aux_u_off = s.Fp;
       L.out_u_off = s.Fp;

@@ -239,7 +239,10 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&q)[4], float (&v)[3
 // is computed, so their load latency overlaps the tensor-memory reads and math.
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc, int mb, int col0,
-                                                 int row_in_tile) {
+                                                 int row_in_tile, int& sbuf) {
+  const int lane = row_in_tile & 31;
+  const int64_t warp_row0 = static_cast<int64_t>(mb) * kBM + (row_in_tile & ~31);
+  const bool warp_rows_full = warp_row0 + 32 <= e.rows;  // uniform across the warp
   constexpr bool kSwiglu = EPI == EPI_DG_SWIGLU;
   constexpr int kChunks = kBN / 32;
   const int64_t grow = static_cast<int64_t>(mb) * kBM + row_in_tile;
@@ -277,8 +280,10 @@ __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc
     uint32_t r0[32];
     tmem_ld_32x32b_x32(tacc + c * 32, r0);
     tmem_ld_wait();
+    float g[32], u[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) g[j] = u[j] = 0.0f;
     if (row_ok) {
-      float g[32], u[32];
       if (n >= 32) {
         unpack_bf16x32(gc, g);
         if constexpr (kSwiglu) unpack_bf16x32(uc, u);
@@ -286,23 +291,33 @@ __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc
         load_row_bf16(pre_row + col, g, n);
         if constexpr (kSwiglu) load_row_bf16(pre_row + e.aux_u_off + col, u, n);
       }
-      if constexpr (kSwiglu) {
-        float dg[32], du[32];
+    }
+    const bool tma = e.out_map != nullptr && warp_rows_full && n >= 32;  // uniform
+    const int32_t y = static_cast<int32_t>(e.out_row0 + warp_row0);
+    if constexpr (kSwiglu) {
+      float dg[32], du[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float dh = __uint_as_float(r0[j]);
-          const float sg = 1.0f / (1.0f + __expf(-g[j]));
-          du[j] = dh * g[j] * sg;                               // dH * silu(g)
-          dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
-        }
+      for (int j = 0; j < 32; ++j) {
+        const float dh = __uint_as_float(r0[j]);
+        const float sg = 1.0f / (1.0f + __expf(-g[j]));
+        du[j] = dh * g[j] * sg;                               // dH * silu(g)
+        dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
+      }
+      if (tma) {
+        stage_and_store<false>(e, dg, lane, sbuf, col, y);
+        stage_and_store<false>(e, du, lane, sbuf, static_cast<int32_t>(e.out_u_off + col), y);
+      } else if (row_ok) {
         store_row_bf16(dst_row + col, dg, n);
         store_row_bf16(dst_row + e.out_u_off + col, du, n);
-      } else {
-        float dgv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dgv[j] = __uint_as_float(r0[j]) * activate_grad<EPI>(g[j]);
-        store_row_bf16(dst_row + col, dgv, n);
       }
+    } else {
+      float dgv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dgv[j] = __uint_as_float(r0[j]) * activate_grad<EPI>(g[j]);
+      if (tma)
+        stage_and_store<false>(e, dgv, lane, sbuf, col, y);
+      else if (row_ok)
+        store_row_bf16(dst_row + col, dgv, n);
     }
   }
 }

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(cons
                       p.rows, p.out_row0, p.n_end, p.use_tma_store ? &p.map_out[shard] : nullptr, stage};
       const int col0 = p.n_base + nb * p.n_tile;
       if constexpr (is_dg(EPI))
-        epilogue_tile_dg<EPI>(e, tacc, mb, col0, row_in_tile);
+        epilogue_tile_dg<EPI>(e, tacc, mb, col0, row_in_tile, sbuf);
       else
         epilogue_tile<EPI>(e, tacc, mb, col0, row_in_tile, sbuf);
       tc_fence_before_sync();
@@ -374,7 +374,9 @@ domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stre
     p.aux[s] = L.aux[s];
   }
   const bool store_epi = L.epi == EPI_H_GELU || L.epi == EPI_H_GELU_TANH || L.epi == EPI_H_IDENTITY ||
-                         L.epi == EPI_H_SWIGLU || L.epi == EPI_Z_F32 || L.epi == EPI_Z_BF16;
+                         L.epi == EPI_H_SWIGLU || L.epi == EPI_Z_F32 || L.epi == EPI_Z_BF16 ||
+                         L.epi == EPI_DG_GELU || L.epi == EPI_DG_GELU_TANH || L.epi == EPI_DG_IDENTITY ||
+                         L.epi == EPI_DG_SWIGLU;
   if (store_epi && L.out_rows > 0 && L.out_cols > 0) {
     for (int s = 0; s < L.num_shards; ++s)
       if (!encode_store_map(&p.map_out[s], L.out[s], L.out_rows, L.out_cols, L.ldo, L.epi == EPI_Z_F32, err))
