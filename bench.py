@@ -42,7 +42,7 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("common.h", "epilogue.cuh", "fused.cu", "gemm.cu", "gemm.h", "ptx.cuh", "shard_sum.cu")
+KERNEL_SOURCES = ("common.h", "epilogue.cuh", "fused.cu", "gemm.cu", "gemm.h", "gemm_pair.cu", "ptx.cuh", "shard_sum.cu")
 
 
 def kernel_source_hash():
@@ -413,7 +413,7 @@ def run_ours(args, w, rank, world, local_rank):
     def launch_flops(r):  # algorithmic GEMM flops of one launch (all shards)
         return {"fused": float(w.fwd_flops()),
                 "gemm1": 2.0 * w.Mc * w.d * w.F * nact, "gemm2": 2.0 * w.Mc * w.F * ds_,
-                "bwd_dh": 2.0 * w.Mc * w.d * w.F, "bwd_dx": 2.0 * w.Mc * nact * w.F * ds_,
+                "bwd_dh": 2.0 * w.M * w.d * w.F, "bwd_dx": 2.0 * w.Mc * nact * w.F * ds_,
                 "bwd_dw": 2.0 * w.M * w.d * w.F * (nact if r["slice"] == 0 else 1)}.get(r["kind"], 0.0)
 
     psize = 4 if w.partial == "f32" else 2

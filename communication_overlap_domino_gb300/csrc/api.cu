@@ -545,38 +545,41 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
     cudaEventRecord(ds->ev_fork, s0);
     cudaStreamWaitEvent(sr, ds->ev_fork, 0);
   }
+  // ---- dH_p = dY B_p^T with the activation derivative fused -> dG_p, over all
+  // M tokens in one launch: it exchanges nothing, so it needs no chunking, and
+  // one launch over M fills the GPU's clusters better than mu launches over M/mu.
+  {
+    GemmLaunch L;
+    L.epi = kDgEpi[s.act];
+    L.b_mn = true;
+    L.num_shards = s.P;
+    for (int p = 0; p < s.P; ++p) {
+      L.a[p] = {dY, s.M, s.d, s.d};
+      L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};  // stored [d][Fp]: K = d rows, N = Fp contiguous
+      L.b1[p] = L.b0[p];
+      L.out[p] = dG[p];
+      L.aux[p] = const_cast<void*>(pre[p]);
+    }
+    L.ldo = nF;
+    L.out_rows = s.M;
+    L.out_cols = nF;
+    L.ld_aux = nF;
+    L.aux_u_off = s.Fp;
+    L.out_u_off = s.Fp;
+    L.a_row0 = 0;
+    L.out_row0 = 0;
+    L.rows = static_cast<int32_t>(s.M);
+    L.group_rows = static_cast<int32_t>(s.Mc);  // dY rows of a group stay in L2 across all column tiles
+    L.n_base = 0;
+    L.n_end = static_cast<int32_t>(s.Fp);
+    L.K = s.d;
+    L.status = dstat;
+    L.timeout_ns = tmo;
+    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DH, 0, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
+    if (st != DOMINO_OK) return fail(st, err);
+  }
   for (int k = 0; k < s.mu; ++k) {
     const int32_t row0 = static_cast<int32_t>(k * s.Mc);
-    // ---- dH_{k,p} = dY_k B_p^T with the activation derivative fused -> dG_{k,p}
-    {
-      GemmLaunch L;
-      L.epi = kDgEpi[s.act];
-      L.b_mn = true;
-      L.num_shards = s.P;
-      for (int p = 0; p < s.P; ++p) {
-        L.a[p] = {dY, s.M, s.d, s.d};
-        L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};  // stored [d][Fp]: K = d rows, N = Fp contiguous
-        L.b1[p] = L.b0[p];
-        L.out[p] = dG[p];
-        L.aux[p] = const_cast<void*>(pre[p]);
-      }
-      L.ldo = nF;
-      L.out_rows = s.M;
-      L.out_cols = nF;
-      L.ld_aux = nF;
-      L.aux_u_off = s.Fp;
-      L.out_u_off = s.Fp;
-      L.a_row0 = row0;
-      L.out_row0 = row0;
-      L.rows = static_cast<int32_t>(s.Mc);
-      L.n_base = 0;
-      L.n_end = static_cast<int32_t>(s.Fp);
-      L.K = s.d;
-      L.status = dstat;
-      L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DH, k, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
-      if (st != DOMINO_OK) return fail(st, err);
-    }
     for (int sl = 0; sl < s.S; ++sl) {
       const int32_t col0 = static_cast<int32_t>(sl * s.ds);
       // ---- partial input gradient of shard p: dG_{k,p} A_p^T -> Z_p

@@ -72,7 +72,7 @@ struct GemmParams {  // CUtensorMap members carry 64-byte alignment
   CUtensorMap map_a[kMaxShards];   // A operand
   CUtensorMap map_b0[kMaxShards];  // B operand rows [n0, n0+128)
   CUtensorMap map_b1[kMaxShards];  // B operand rows for accumulator columns 128..255
-  CUtensorMap map_out[kMaxShards]; // output store map (box 32 x 32), when use_tma_store
+  CUtensorMap map_out[kMaxShards]; // output store map (box 32 rows x 32 or 64 columns), when use_tma_store
   void* out[kMaxShards];           // output matrix per shard
   void* aux[kMaxShards];           // optional copy of the pre-activation(s) (bf16), or null
   int64_t ldo;                     // leading dimension of out (elements)
@@ -88,7 +88,8 @@ struct GemmParams {  // CUtensorMap members carry 64-byte alignment
   int32_t b1_off;                  // B row of the second 128-row box relative to the first
   int32_t num_kb;                  // K blocks of 64
   int32_t tiles_m, tiles_n, num_shards, num_tiles;
-  int32_t use_tma_store;           // epilogue writes full 32 x 32 chunks through map_out
+  int32_t group_m;                 // paired kernel: row blocks per group of the tile order
+  int32_t use_tma_store;           // epilogue writes full chunks through map_out
   DeviceStatus* status;
   uint64_t timeout_ns;
 };

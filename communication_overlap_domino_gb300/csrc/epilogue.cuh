@@ -121,8 +121,8 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], 
 // Writes one 32-row x 32-column chunk (this lane: row `lane`, values v) through
 // shared memory and a TMA store at output coordinates (x, y).  The staging
 // layout is the store map's swizzle: 128-byte rows (fp32) with the 128-byte
-// swizzle, or 64-byte rows (bf16) with the 64-byte swizzle, so the 16-byte
-// writes of a warp spread over all banks.  Two buffers alternate; before one is
+// swizzle, or 64-byte rows (bf16, the backward dG outputs) with the 64-byte
+// swizzle, so the 16-byte writes of a warp spread over all banks.  Two buffers alternate; before one is
 // rewritten, lane 0 waits until the store that last read it is done reading.
 template <bool F32>
 __device__ __forceinline__ void stage_and_store(const EpiArgs& e, const float (&v)[32], int lane, int& sbuf,
@@ -157,12 +157,78 @@ __device__ __forceinline__ void stage_and_store(const EpiArgs& e, const float (&
   ++sbuf;
 }
 
-// Drains one accumulator tile (this thread: one row) through the epilogue.
+// Writes one 32-row x 64-column bf16 chunk (this lane: row `lane`, columns
+// v0 then v1) through shared memory and a TMA store at (x, y): 128-byte rows
+// with the 128-byte swizzle, two alternating 4 KB buffers per warp.
+__device__ __forceinline__ void stage_and_store_bf16x64(const EpiArgs& e, const float (&v0)[32],
+                                                        const float (&v1)[32], int lane, int& sbuf, int32_t x,
+                                                        int32_t y) {
+  uint8_t* buf = e.stage + (sbuf & 1) * 4096;
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float* v = j < 4 ? v0 : v1;
+    const int q = j & 3;
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(e.out_map, buf, x, y);
+    bulk_commit_group();
+  }
+  ++sbuf;
+}
+
+// One 32-column chunk of the accumulator row: tensor-memory load, the saved
+// pre-activations (when e.aux is set) and the activation.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, uint32_t tacc, int c, int col, int n, bool row_ok,
+                                               int64_t orow, float (&h)[32]) {
+  uint32_t r0[32];
+  tmem_ld_32x32b_x32(tacc + c * 32, r0);
+  if constexpr (EPI == EPI_H_SWIGLU) {
+    uint32_t r1[32];
+    tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) h[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+    if (row_ok && e.aux != nullptr) {
+      float g[32], u[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = __uint_as_float(r0[j]);
+        u[j] = __uint_as_float(r1[j]);
+      }
+      __nv_bfloat16* a = static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col;
+      store_row_bf16(a, g, n);
+      store_row_bf16(a + e.aux_u_off, u, n);
+    }
+  } else {
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) h[j] = __uint_as_float(r0[j]);
+    if constexpr (EPI != EPI_Z_F32 && EPI != EPI_Z_BF16) {
+      if (row_ok && e.aux != nullptr)
+        store_row_bf16(static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col, h, n);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(h[j]);
+    }
+  }
+}
+
 // Drains one 128 x 256 accumulator tile (this thread: one row) through the
-// epilogue.  Full 32 x 32 chunks inside the valid rows and columns go out
-// through shared memory and TMA stores when e.out_map is set; edge chunks (and
-// the saved pre-activations) use direct stores.  sbuf: the warp's staging
-// buffer counter.
+// epilogue.  fp32 outputs go out in 32 x 32 chunks, bf16 outputs in 32 x 64
+// chunks (128-byte rows either way); full chunks inside the valid rows and
+// columns go through shared memory and TMA stores when e.out_map is set, edge
+// chunks (and the saved pre-activations) use direct stores.  sbuf: the warp's
+// staging buffer counter.
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const EpiArgs& e, uint32_t tacc, int mb, int col0, int row_in_tile,
                                               int& sbuf) {
@@ -172,52 +238,37 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& e, uint32_t tacc, i
   const int64_t orow = e.out_row0 + grow;
   const int64_t warp_row0 = static_cast<int64_t>(mb) * kBM + (row_in_tile & ~31);
   const bool warp_rows_full = warp_row0 + 32 <= e.rows;  // uniform across the warp
-  constexpr bool kF32Out = EPI == EPI_Z_F32;
+  const int32_t y = static_cast<int32_t>(e.out_row0 + warp_row0);
   constexpr int kChunks = (EPI == EPI_H_SWIGLU) ? (kBN / 2) / 32 : kBN / 32;
+  if constexpr (EPI == EPI_Z_F32) {
 #pragma unroll 1
-  for (int c = 0; c < kChunks; ++c) {
-    const int col = col0 + c * 32;
-    if (col >= e.n_end) break;  // uniform across the warp
-    const int n = e.n_end - col;
-    const bool tma = e.out_map != nullptr && warp_rows_full && n >= 32;  // uniform
-    uint32_t r0[32];
-    tmem_ld_32x32b_x32(tacc + c * 32, r0);
-    float h[32];
-    if constexpr (EPI == EPI_H_SWIGLU) {
-      uint32_t r1[32];
-      tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) h[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
-      if (row_ok && e.aux != nullptr) {
-        float g[32], u[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          g[j] = __uint_as_float(r0[j]);
-          u[j] = __uint_as_float(r1[j]);
-        }
-        __nv_bfloat16* a = static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col;
-        store_row_bf16(a, g, n);
-        store_row_bf16(a + e.aux_u_off, u, n);
-      }
-    } else {
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) h[j] = __uint_as_float(r0[j]);
-      if constexpr (EPI != EPI_Z_F32 && EPI != EPI_Z_BF16) {
-        if (row_ok && e.aux != nullptr)
-          store_row_bf16(static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col, h, n);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(h[j]);
-      }
-    }
-    if (tma) {
-      stage_and_store<kF32Out>(e, h, lane, sbuf, col, static_cast<int32_t>(e.out_row0 + warp_row0));
-    } else if (row_ok) {
-      if constexpr (kF32Out)
+    for (int c = 0; c < kChunks; ++c) {
+      const int col = col0 + c * 32;
+      if (col >= e.n_end) break;  // uniform across the warp
+      const int n = e.n_end - col;
+      float h[32];
+      epilogue_chunk<EPI>(e, tacc, c, col, n, row_ok, orow, h);
+      if (e.out_map != nullptr && warp_rows_full && n >= 32)
+        stage_and_store<true>(e, h, lane, sbuf, col, y);
+      else if (row_ok)
         store_row_f32(static_cast<float*>(e.out) + orow * e.ldo + col, h, n);
-      else
-        store_row_bf16(static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col, h, n);
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < kChunks; c += 2) {
+      const int col = col0 + c * 32;
+      if (col >= e.n_end) break;  // uniform across the warp
+      const int n = e.n_end - col;
+      float h0[32], h1[32];
+      epilogue_chunk<EPI>(e, tacc, c, col, n, row_ok, orow, h0);
+      if (n > 32) epilogue_chunk<EPI>(e, tacc, c + 1, col + 32, n - 32, row_ok, orow, h1);
+      if (e.out_map != nullptr && warp_rows_full && n >= 64) {
+        stage_and_store_bf16x64(e, h0, h1, lane, sbuf, col, y);
+      } else if (row_ok) {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(e.out) + orow * e.ldo + col;
+        store_row_bf16(o, h0, n);
+        if (n > 32) store_row_bf16(o + 32, h1, n - 32);
+      }
     }
   }
 }

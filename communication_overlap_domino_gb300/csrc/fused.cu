@@ -833,8 +833,9 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pai
     if (!encode_bf16_sw128(&f.map_h[p], Operand2D{L.H[p], L.M, Fp, Fp}, kBM, err)) return DOMINO_ERR_CUDA;
     if (!encode_bf16_sw128(&f.map_w2[p], Operand2D{L.B_shards[p], L.d, Fp, Fp}, kBN / 2, err))
       return DOMINO_ERR_CUDA;
-    if (!encode_store_map(&f.map_hout[p], L.H[p], L.M, Fp, Fp, false, err)) return DOMINO_ERR_CUDA;
-    if (!encode_store_map(&f.map_zout[p], L.Z[p], L.M, L.d, L.d, L.partial_f32, err)) return DOMINO_ERR_CUDA;
+    if (!encode_store_map(&f.map_hout[p], L.H[p], L.M, Fp, Fp, false, 64, err)) return DOMINO_ERR_CUDA;
+    if (!encode_store_map(&f.map_zout[p], L.Z[p], L.M, L.d, L.d, L.partial_f32, L.partial_f32 ? 32 : 64, err))
+      return DOMINO_ERR_CUDA;
     f.h[p] = L.H[p];
     f.aux[p] = L.aux[p];
     f.z[p] = L.Z[p];

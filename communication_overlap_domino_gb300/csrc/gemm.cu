@@ -323,17 +323,18 @@ bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std:
 // elements): box 32 x 32, 128-byte swizzle for fp32 (128-byte rows), 64-byte
 // swizzle for bf16 (64-byte rows), matching stage_and_store's staging layout.
 bool encode_store_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool f32,
-                      std::string* err) {
+                      int box_cols, std::string* err) {
   EncodeTiledFn enc = get_encode_fn(err);
   if (!enc) return false;
   const int esz = f32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 32};
+  const bool row128 = box_cols * esz == 128;
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   row128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     if (err) {
@@ -379,7 +380,8 @@ domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stre
                          L.epi == EPI_DG_SWIGLU;
   if (store_epi && L.out_rows > 0 && L.out_cols > 0) {
     for (int s = 0; s < L.num_shards; ++s)
-      if (!encode_store_map(&p.map_out[s], L.out[s], L.out_rows, L.out_cols, L.ldo, L.epi == EPI_Z_F32, err))
+      if (!encode_store_map(&p.map_out[s], L.out[s], L.out_rows, L.out_cols, L.ldo, L.epi == EPI_Z_F32,
+                            store_box_cols(L.epi, L.epi == EPI_Z_F32), err))
         return DOMINO_ERR_CUDA;
     p.use_tma_store = 1;
   }

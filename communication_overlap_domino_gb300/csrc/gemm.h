@@ -37,6 +37,9 @@ struct GemmLaunch {
   int64_t out_rows = 0, out_cols = 0;  // extent of each out[s]; 0: no TMA stores (direct stores only)
   int32_t a_row0 = 0, out_row0 = 0, rows = 0;
   int32_t n_base = 0, n_end = 0, n_tile = kBN, b1_off = kBN / 2;
+  // Paired kernel tile order: rows in groups of group_rows (0: all rows in one
+  // group), and within a group every shard and column block, rows innermost.
+  int32_t group_rows = 0;
   int64_t K = 0;
   DeviceStatus* status = nullptr;
   uint64_t timeout_ns = 0;
@@ -47,8 +50,16 @@ cudaError_t prepare_pair_kernels(int* max_clusters);
 // Paired-CTA GEMM (gemm_pair.cu): same launch description, 2-CTA clusters.
 domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStream_t stream, std::string* err);
 bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err);
+// TMA store map of a row-major output: box 32 rows x box_cols, 128-byte rows
+// (fp32 x 32 or bf16 x 64, 128-byte swizzle) or 64-byte rows (bf16 x 32, the
+// backward dG outputs, 64-byte swizzle).
 bool encode_store_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool f32,
-                      std::string* err);
+                      int box_cols, std::string* err);
+// Store-box width the epilogue of `epi` writes.
+inline int store_box_cols(int epi, bool f32) {
+  if (f32) return 32;
+  return (epi == EPI_DG_GELU || epi == EPI_DG_GELU_TANH || epi == EPI_DG_IDENTITY || epi == EPI_DG_SWIGLU) ? 32 : 64;
+}
 domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stream, std::string* err);
 
 // The fused forward pass (fused.cu).

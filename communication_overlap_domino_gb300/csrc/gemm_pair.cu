@@ -43,12 +43,24 @@ static_assert(kPairSmemBytes <= 232448, "shared memory budget");
 constexpr int kPairAccBufs = 2;
 constexpr uint32_t kPairTmemCols = 256 * kPairAccBufs;
 
+// Tile t -> (shard, 256-row block, column block).  Rows go in groups of
+// group_m blocks; within a group: for each shard, for each column block, the
+// group's row blocks.  Consecutive tiles (run at the same time by the clusters)
+// share a column block of B; a group's rows of A stay in L2 while every shard
+// and column block passes over them, so A is read about once and B once per
+// group.
 __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int& shard, int& mb2, int& nb) {
-  const int per = p.tiles_m * p.tiles_n;  // tiles_m counts 256-row blocks here
-  shard = t / per;
-  const int r = t - shard * per;
-  nb = r / p.tiles_m;
-  mb2 = r - nb * p.tiles_m;
+  const int G = p.group_m;
+  const int per_group = G * p.tiles_n * p.num_shards;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int rows_left = p.tiles_m - g * G;
+  const int gm = rows_left < G ? rows_left : G;
+  const int per_shard = gm * p.tiles_n;
+  shard = r / per_shard;
+  const int r2 = r - shard * per_shard;
+  nb = r2 / gm;
+  mb2 = g * G + (r2 - nb * gm);
 }
 
 template <int EPI, bool A_MN, bool B_MN>
@@ -314,7 +326,8 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStre
                          L.epi == EPI_DG_SWIGLU;
   if (store_epi && L.out_rows > 0 && L.out_cols > 0) {
     for (int s = 0; s < L.num_shards; ++s)
-      if (!encode_store_map(&p.map_out[s], L.out[s], L.out_rows, L.out_cols, L.ldo, L.epi == EPI_Z_F32, err))
+      if (!encode_store_map(&p.map_out[s], L.out[s], L.out_rows, L.out_cols, L.ldo, L.epi == EPI_Z_F32,
+                            store_box_cols(L.epi, L.epi == EPI_Z_F32), err))
         return DOMINO_ERR_CUDA;
     p.use_tma_store = 1;
   }
@@ -334,6 +347,9 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStre
   p.tiles_n = (L.n_end - L.n_base + L.n_tile - 1) / L.n_tile;
   p.num_shards = L.num_shards;
   p.num_tiles = p.tiles_m * p.tiles_n * p.num_shards;
+  p.group_m = L.group_rows > 0 ? (L.group_rows + 255) / 256 : p.tiles_m;
+  if (p.group_m > p.tiles_m) p.group_m = p.tiles_m;
+  if (p.group_m < 1) p.group_m = 1;
   p.status = L.status;
   p.timeout_ns = L.timeout_ns;
   if (p.num_tiles == 0) return DOMINO_OK;

@@ -158,10 +158,11 @@ DOMINO_API domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const v
  * dY [M,d] in; dX [M,d] out; dA_shards[p] / dB_shards[p] out (bf16, the same
  * layouts as A_shards[p] / B_shards[p]).  `saved` must hold what domino_mlp_fwd
  * wrote for the same X and weights.  workspace: domino_mlp_workspace_size(desc, 1)
- * bytes.  Steps per chunk k (and slice s):
- *   dH_{k,p} = dY_k B_p^T, with the activation derivative fused into the
+ * bytes.  First, over all M in one launch (it exchanges nothing):
+ *   dH_p = dY B_p^T, with the activation derivative fused into the
  *     epilogue: dG = dH * act'(g) (SwiGLU: dg = dH * u * silu'(g),
- *     du = dH * silu(g)), from the saved pre-activations;
+ *     du = dH * silu(g)), from the saved pre-activations.
+ * Then per chunk k (and slice s):
  *   the partial input gradient of shard p, dG_{k,p} A_p^T, into shard p's partial
  *     buffer, then dX_k[:, s] = sum over p of the partials (the shard-sum, in fp32,
  *     shard order; it overlaps the next chunk's GEMMs);
