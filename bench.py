@@ -455,7 +455,8 @@ def run_ours(args, w, rank, world, local_rank):
         "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights, bf16",
         "config": {"workload": w.name, "M": w.M, "d": w.d, "F": w.F, "P": w.P, "mu": w.mu, "act": w.act,
                    "partials": w.partial, "out_slices": w.slices, "schedule": args.schedule,
-                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+                   "l2": "flushed between steps (256 MiB write outside the step events)",
+                   **({"plan": args.plan_result} if getattr(args, "plan_result", None) else {})},
         "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
         "exposed_reduce_us_per_layer": round(1e3 * exposed_ms, 2),
         "exposed_reduce_frac": round(exposed_ms / span_ms, 4) if span_ms > 0 else None,
@@ -566,6 +567,8 @@ def main():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--mu", type=int, default=None)
     ap.add_argument("--schedule", choices=("streams", "serial", "fused"), default="fused")
+    ap.add_argument("--plan", action="store_true",
+                    help="take mu and the schedule from domino_mlp_plan (overrides --mu and --schedule)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -588,6 +591,14 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
+    args.plan_result = None
+    if args.plan:
+        import torch
+        from communication_overlap_domino_gb300 import binding as b
+        torch.cuda.set_device(local_rank)
+        args.plan_result = b.plan(w.M, w.d, w.F, w.P, w.act, w.partial, w.slices)
+        w = w.with_(mu=args.plan_result["mu"])
+        args.schedule = args.plan_result["schedule"]
     if world > 1:
         import torch
         import torch.distributed as dist

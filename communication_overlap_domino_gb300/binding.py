@@ -65,6 +65,23 @@ class KernelTime(ctypes.Structure):
     ]
 
 
+class PlanHw(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int32), ("fused_available", ctypes.c_int32), ("l2_bytes", ctypes.c_int64)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("mu", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
+        ("reason", ctypes.c_int32),
+        ("gemm1_tiles_per_chunk", ctypes.c_int32),
+        ("chunk_h_bytes", ctypes.c_int64),
+        ("l2_budget_bytes", ctypes.c_int64),
+    ]
+
+
+PLAN_REASON = {0: "fits_l2", 1: "largest_filling", 2: "small"}
+
 _LIB: Optional[ctypes.CDLL] = None
 _VP = ctypes.c_void_p
 _VPP = ctypes.POINTER(ctypes.c_void_p)
@@ -86,6 +103,7 @@ SIGNATURES = [
     ("domino_mlp_fwd_noalloc", ctypes.c_int, [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP]),
     ("domino_kernel_times", ctypes.c_int32, [ctypes.POINTER(KernelTime), ctypes.c_int32]),
     ("domino_kernel_times_reset", None, []),
+    ("domino_mlp_plan", ctypes.c_int, [ctypes.POINTER(MlpDesc), ctypes.POINTER(PlanHw), ctypes.POINTER(Plan)]),
 ]
 
 
@@ -306,6 +324,20 @@ def selftest_wait_timeout(workspace, timeout_ns: int, stream=None) -> None:
 def query_device_status(workspace, stream=None) -> int:
     """Synchronises, returns and clears the device status word (0 = OK)."""
     return int(lib().domino_query_device_status(workspace.data_ptr(), _stream_handle(stream)))
+
+
+def plan(M: int, d: int, F: int, P: int, act: str, partial: str, out_slices: int = 1, *, num_sms: int = 0,
+         l2_bytes: int = 0, fused_available: int = -1) -> dict:
+    """domino_mlp_plan: the number of row chunks and the schedule for this problem.  Hardware
+    figures left at 0 (fused_available at -1) are read from the current CUDA device."""
+    desc = make_desc(M, d, F, P, 1, act, partial, out_slices)
+    hw = PlanHw(num_sms=num_sms, fused_available=fused_available, l2_bytes=l2_bytes)
+    out = Plan()
+    _check(lib().domino_mlp_plan(ctypes.byref(desc), ctypes.byref(hw), ctypes.byref(out)), "domino_mlp_plan")
+    sched = {v: k for k, v in SCHEDULE.items()}[out.schedule]
+    return {"mu": out.mu, "schedule": sched, "reason": PLAN_REASON.get(out.reason, out.reason),
+            "gemm1_tiles_per_chunk": out.gemm1_tiles_per_chunk, "chunk_h_bytes": out.chunk_h_bytes,
+            "l2_budget_bytes": out.l2_budget_bytes}
 
 
 def kernel_times_reset() -> None:

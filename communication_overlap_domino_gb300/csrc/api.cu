@@ -247,6 +247,10 @@ namespace domino {
 // Lets other translation units of the library report a detailed error through
 // domino_last_error().
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+domino_status_t validate_desc(const domino_mlp_desc_t* desc) {
+  Shape s;
+  return check_desc(desc, &s);
+}
 }  // namespace domino
 
 // ====================================================================== ABI

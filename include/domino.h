@@ -275,6 +275,50 @@ DOMINO_API int32_t domino_kernel_times(domino_kernel_time_t* out, int32_t max_re
 /* Empties the log (the pooled events are kept for reuse). */
 DOMINO_API void domino_kernel_times_reset(void);
 
+/* Schedule selection.  The FiCCO page ("Design Space Exploration of DMA based
+ * Finer-Grain Compute Communication Overlap", Abstract) picks a decomposition
+ * for each operator from its sizes with heuristics, because finer pieces cost
+ * GEMM efficiency; this entry point does that for the number of row chunks mu
+ * and the schedule.  The rule (host arithmetic only):
+ *   - schedule: DOMINO_SCHEDULE_FUSED when the fused cooperative forward can be
+ *     launched, else DOMINO_SCHEDULE_STREAMS;
+ *   - candidates: mu in {1, 2, 4, ...} with mu | M and mu * out_slices <=
+ *     DOMINO_MAX_PIECES; a candidate "fills" the GPU when one chunk's GEMM1 has
+ *     at least one paired 256 x 256 tile per 2-CTA cluster (num_sms / 2);
+ *   - mu = the smallest filling candidate whose chunk of hidden activations,
+ *     (M / mu) * F * 2 bytes over all shards, fits in 9/10 of the L2 (GEMM2 then
+ *     reads H from L2); if none fits, the largest filling candidate; if none
+ *     fills, mu = 1.
+ * problem: M, d, F, P, out_slices, act, partial_dtype as for domino_mlp_fwd (mu,
+ * schedule and flags are ignored).  hw: hardware figures; NULL, or a field <= 0
+ * (fused_available < 0), means "ask the current CUDA device".  out: the choice.
+ * Errors: DOMINO_ERR_INVALID_ARG / UNSUPPORTED / ALIGNMENT for a problem
+ * domino_mlp_fwd would reject (with mu = 1), DOMINO_ERR_CUDA when a device query
+ * fails.  Launches nothing and allocates nothing. */
+typedef struct domino_plan_hw {
+  int32_t num_sms;          /* streaming multiprocessors                            */
+  int32_t fused_available;  /* 1 / 0: the fused forward can / cannot be launched    */
+  int64_t l2_bytes;         /* L2 cache size in bytes                               */
+} domino_plan_hw_t;
+
+typedef enum domino_plan_reason {
+  DOMINO_PLAN_FITS_L2 = 0,        /* smallest filling mu whose chunk of H fits the budget */
+  DOMINO_PLAN_LARGEST_FILLING = 1,/* no filling mu fits: the largest filling one          */
+  DOMINO_PLAN_SMALL = 2           /* no mu fills the GPU: mu = 1                          */
+} domino_plan_reason_t;
+
+typedef struct domino_plan {
+  int32_t mu;                  /* chosen row chunks                                  */
+  int32_t schedule;            /* chosen domino_schedule_t                           */
+  int32_t reason;              /* domino_plan_reason_t                               */
+  int32_t gemm1_tiles_per_chunk; /* paired GEMM1 tiles of one chunk at the chosen mu */
+  int64_t chunk_h_bytes;       /* (M / mu) * F * 2 at the chosen mu                  */
+  int64_t l2_budget_bytes;     /* 9/10 of the L2 it was compared with                */
+} domino_plan_t;
+
+DOMINO_API domino_status_t domino_mlp_plan(const domino_mlp_desc_t* problem, const domino_plan_hw_t* hw,
+                                           domino_plan_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,6 +83,14 @@ def test_backward_llama_tail_bf16_partials():
     _check_full(w, seed=9, schedule="serial")
 
 
+def test_backward_partial_row_group():
+    # dH runs once over all M with its tiles in row groups of one chunk: chunk rows 640 -> groups of 3
+    # 256-row blocks over 5 blocks, so the last group is partial; F_p = 1376 leaves a 96-column tile
+    w = wl.Workload("group_tail_bwd", M=1280, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
+    _check_full(w, seed=13)
+    _check_full(w.with_(act="gelu", partial="f32"), seed=14)
+
+
 def test_backward_empty_batch_zeroes_weight_grads():
     w = wl.Workload("empty_bwd", M=1, d=512, F=1024, P=2, mu=1, act="swiglu", partial="bf16", bwd=True)
     t = wl.generate(w, 0, with_dy=True)

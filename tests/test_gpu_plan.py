@@ -1,0 +1,43 @@
+"""domino_mlp_plan on the GB300 itself: the hardware figures come from the
+device, and the planned configuration runs and matches the oracle."""
+import pytest
+import torch
+
+import oracle
+from communication_overlap_domino_gb300 import binding as b
+from communication_overlap_domino_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def test_plan_reads_the_device():
+    props = torch.cuda.get_device_properties(0)
+    w = wl.WORKLOADS["llama_swiglu_fwd"]
+    p = b.plan(w.M, w.d, w.F, w.P, w.act, w.partial, w.slices)
+    explicit = b.plan(w.M, w.d, w.F, w.P, w.act, w.partial, w.slices, num_sms=props.multi_processor_count,
+                      l2_bytes=props.L2_cache_size, fused_available=1)
+    assert p == explicit
+    assert p["l2_budget_bytes"] == props.L2_cache_size // 10 * 9
+    assert w.M % p["mu"] == 0 and p["schedule"] == "fused"
+
+
+def test_planned_configuration_runs():
+    w0 = wl.Workload("plan_small", M=2048, d=1024, F=4096, P=4, mu=1, act="gelu", partial="f32")
+    p = b.plan(w0.M, w0.d, w0.F, w0.P, w0.act, w0.partial, num_sms=16, l2_bytes=1 << 20, fused_available=1)
+    assert p["mu"] > 1  # the small L2 forces chunking
+    w = w0.with_(mu=p["mu"])
+    t = wl.generate(w, 21)
+    dev = torch.device("cuda:0")
+    A_sh, B_sh = b.shard_weights(t["A"].to(dev), t["B"].to(dev), w.P)
+    Y = b.mlp_fwd(t["X"].to(dev), A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, schedule=p["schedule"])
+    f = wl.to_float64(t)
+    err = oracle.max_rel_err(Y.double().cpu().numpy(), oracle.mlp_fwd(f["X"], f["A"], f["B"], w.act))
+    assert err <= 1e-2
