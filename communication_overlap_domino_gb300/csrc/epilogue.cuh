@@ -28,7 +28,23 @@ struct EpiArgs {
 
 // ------------------------------------------------------------------ epilogue
 
-__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+// erf from Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26: for z >= 0, erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5)
+// exp(-z^2) with t = 1 / (1 + p z), absolute error <= 1.5e-7; odd in z.  One
+// fast reciprocal and one fast exponential per value: cheaper in the epilogue
+// than the library erff, and far inside the bf16 rounding of H.
+__device__ __forceinline__ float erf_as(float z) {
+  const float az = fabsf(z);
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, az, 1.0f));
+  float poly = fmaf(t, 1.061405429f, -1.453152027f);
+  poly = fmaf(t, poly, 1.421413741f);
+  poly = fmaf(t, poly, -0.284496736f);
+  poly = fmaf(t, poly, 0.254829592f);
+  poly *= t;
+  return copysignf(fmaf(-poly, __expf(-az * az), 1.0f), z);
+}
+
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erf_as(x * 0.70710678118654752f)); }
 __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
 }
@@ -37,7 +53,7 @@ __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x));
 // Derivatives for the backward epilogue (product and chain rules).
 __device__ __forceinline__ float gelu_erf_grad(float x) {
   // d/dx [x Phi(x)] = Phi(x) + x phi(x)
-  return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * __expf(-0.5f * x * x);
+  return 0.5f * (1.0f + erf_as(x * 0.70710678118654752f)) + x * 0.39894228040143268f * __expf(-0.5f * x * x);
 }
 __device__ __forceinline__ float gelu_tanh_grad(float x) {
   const float k = 0.79788456080286536f;
