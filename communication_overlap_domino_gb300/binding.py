@@ -104,6 +104,9 @@ SIGNATURES = [
     ("domino_kernel_times", ctypes.c_int32, [ctypes.POINTER(KernelTime), ctypes.c_int32]),
     ("domino_kernel_times_reset", None, []),
     ("domino_mlp_plan", ctypes.c_int, [ctypes.POINTER(MlpDesc), ctypes.POINTER(PlanHw), ctypes.POINTER(Plan)]),
+    ("domino_mlp_interleaved_workspace_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc)]),
+    ("domino_mlp_fwd_bwd_interleaved", ctypes.c_int,
+     [ctypes.POINTER(MlpDesc), _VPP, _VPP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VPP, _VPP, _VP, ctypes.c_size_t, _VP]),
 ]
 
 
@@ -260,6 +263,41 @@ def mlp_bwd(X, A_shards: List, B_shards: List, dY, saved, *, F: int, mu: int, ac
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "domino_mlp_bwd")
     return dX, dA_shards, dB_shards
+
+
+def interleaved_workspace_size(desc: MlpDesc) -> int:
+    return int(lib().domino_mlp_interleaved_workspace_size(ctypes.byref(desc)))
+
+
+def mlp_fwd_bwd_interleaved(A_shards: List, B_shards: List, Xa, Xb, dYb, saved_b, *, F: int, mu: int, act: str,
+                            partial: str, out_slices: int = 1, schedule: str = "streams", Ya=None, saved_a=None,
+                            dXb=None, dA_shards=None, dB_shards=None, workspace=None, stream=None,
+                            kernel_times: bool = False, timeout_ns: int = 0, pair_cta: bool = True):
+    """domino_mlp_fwd_bwd_interleaved: the forward of strand a (Xa -> Ya, saved_a) and the backward
+    of strand b (Xb, dYb, saved_b -> dXb, dA_shards, dB_shards) in one call; returns
+    (Ya, dXb, dA_shards, dB_shards)."""
+    torch = _torch()
+    M, d = Xa.shape
+    P = len(A_shards)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
+    if Ya is None:
+        Ya = torch.empty((M, d), dtype=torch.bfloat16, device=Xa.device)
+    if dXb is None:
+        dXb = torch.empty((M, d), dtype=torch.bfloat16, device=Xa.device)
+    if dA_shards is None:
+        dA_shards = [torch.empty_like(a) for a in A_shards]
+    if dB_shards is None:
+        dB_shards = [torch.empty_like(x) for x in B_shards]
+    if workspace is None:
+        workspace = _workspace(max(interleaved_workspace_size(desc), 256), Xa.device)
+    st = lib().domino_mlp_fwd_bwd_interleaved(
+        ctypes.byref(desc), _ptr_array([a.data_ptr() for a in A_shards]),
+        _ptr_array([x.data_ptr() for x in B_shards]), Xa.data_ptr(), Ya.data_ptr(),
+        saved_a.data_ptr() if saved_a is not None else None, Xb.data_ptr(), dYb.data_ptr(), saved_b.data_ptr(),
+        dXb.data_ptr(), _ptr_array([a.data_ptr() for a in dA_shards]), _ptr_array([x.data_ptr() for x in dB_shards]),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "domino_mlp_fwd_bwd_interleaved")
+    return Ya, dXb, dA_shards, dB_shards
 
 
 def unshard_grads(dA_shards: List, dB_shards: List, act: str):

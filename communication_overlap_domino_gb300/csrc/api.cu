@@ -57,6 +57,7 @@ struct DeviceState {
   cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_join = nullptr;
   cudaEvent_t ev_piece[DOMINO_MAX_PIECES] = {};
+  cudaEvent_t ev_piece_b[DOMINO_MAX_PIECES] = {};  // the second strand of an interleaved call
   std::vector<cudaEvent_t> timing_pool;  // events with timing, reused after a log reset
   size_t timing_next = 0;
 };
@@ -96,8 +97,10 @@ domino_status_t device_state(DeviceState** out) {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ds.reduce_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_join, cudaEventDisableTiming);
-    for (int i = 0; i < DOMINO_MAX_PIECES && e == cudaSuccess; ++i)
+    for (int i = 0; i < DOMINO_MAX_PIECES && e == cudaSuccess; ++i) {
       e = cudaEventCreateWithFlags(&ds.ev_piece[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.ev_piece_b[i], cudaEventDisableTiming);
+    }
     if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("device setup: ") + cudaGetErrorString(e));
     ds.ready = true;
   }
@@ -241,6 +244,327 @@ domino_status_t run_gemm(const GemmLaunch& L, const DeviceState* ds, bool pair, 
   return pair ? launch_gemm_pair(L, ds->pair_max_clusters, st, err) : launch_gemm(L, ds->num_sms, st, err);
 }
 
+// ------------------------------------------------------- launch sequences
+
+// The forward of one batch as separate launches (SERIAL / STREAMS schedules):
+// per chunk k, GEMM1 of all shards, then per slice s GEMM2 and -- on the
+// reduction stream, after an event recorded behind that GEMM2 -- the shard-sum
+// of piece (k, s).  chunk(k) issues one chunk, so another sequence's launches
+// can be placed between chunks.
+struct FwdSeq {
+  Shape s{};
+  DeviceState* ds = nullptr;
+  Timer* T = nullptr;
+  cudaStream_t s0 = nullptr, sr = nullptr;
+  bool pair = true;
+  DeviceStatus* status = nullptr;
+  uint64_t tmo = 0;
+  const void* X = nullptr;
+  const void* const* A_shards = nullptr;
+  const void* const* B_shards = nullptr;
+  void* Y = nullptr;
+  void* H[kMaxShards] = {};
+  void* pre[kMaxShards] = {};
+  void* Z[kMaxShards] = {};
+  cudaEvent_t* ev_piece = nullptr;  // mu * S events, one per piece
+
+  // H and the pre-activations go to `saved` when it is given, else H to the workspace.
+  void bind(uint8_t* ws, const WsLayout& W, void* saved) {
+    for (int p = 0; p < s.P; ++p) {
+      if (saved) {
+        uint8_t* blk = static_cast<uint8_t*>(saved) + saved_shard_bytes(s) * p;
+        pre[p] = blk;
+        H[p] = blk + static_cast<size_t>(s.M) * s.Fp * s.nact * 2;
+      } else {
+        pre[p] = nullptr;
+        H[p] = ws + W.h_off + W.h_shard * p;
+      }
+      Z[p] = ws + W.z_off + W.z_shard * p;
+    }
+  }
+
+  domino_status_t chunk(int k, std::string* err) const {
+    static const int kEpiOfAct[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_SWIGLU, EPI_H_IDENTITY};
+    const bool swiglu = s.act == DOMINO_ACT_SWIGLU;
+    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
+    domino_status_t st;
+    // ---- GEMM1: H_{k,p} = act(X_k A_p), all shards in one launch
+    {
+      GemmLaunch L;
+      L.epi = kEpiOfAct[s.act];
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {X, s.M, s.d, s.d};
+        const uint8_t* Ap = static_cast<const uint8_t*>(A_shards[p]);
+        L.b0[p] = {Ap, s.Fp, s.d, s.d};
+        L.b1[p] = swiglu ? Operand2D{Ap + static_cast<size_t>(s.Fp) * s.d * 2, s.Fp, s.d, s.d} : L.b0[p];
+        L.out[p] = H[p];
+        L.aux[p] = pre[p];
+      }
+      L.n_tile = swiglu ? kBN / 2 : kBN;
+      L.b1_off = swiglu ? 0 : kBN / 2;
+      L.ldo = s.Fp;
+      L.out_rows = s.M;
+      L.out_cols = s.Fp;
+      L.ld_aux = s.Fp * s.nact;
+      L.aux_u_off = s.Fp;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = 0;
+      L.n_end = static_cast<int32_t>(s.Fp);
+      L.K = s.d;
+      L.status = status;
+      L.timeout_ns = tmo;
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      if (st != DOMINO_OK) return st;
+    }
+    for (int sl = 0; sl < s.S; ++sl) {
+      const int32_t col0 = static_cast<int32_t>(sl * s.ds);
+      // ---- GEMM2: Z_{k,p,s} = H_{k,p} B_p[:, slice s]
+      GemmLaunch L;
+      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {H[p], s.M, s.Fp, s.Fp};
+        L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};
+        L.b1[p] = L.b0[p];
+        L.out[p] = Z[p];
+      }
+      L.n_tile = kBN;
+      L.b1_off = kBN / 2;
+      L.ldo = s.d;
+      L.out_rows = s.M;
+      L.out_cols = s.d;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = col0;
+      L.n_end = static_cast<int32_t>(col0 + s.ds);
+      L.K = s.Fp;
+      L.status = status;
+      L.timeout_ns = tmo;
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return run_gemm(L, ds, pair, s0, err); });
+      if (st != DOMINO_OK) return st;
+      st = shard_sum_piece(k, sl, err);
+      if (st != DOMINO_OK) return st;
+    }
+    return DOMINO_OK;
+  }
+
+  // Y_k[:, s] = sum over p of Z_{k,p}[:, s], after the GEMM2 just issued on s0.
+  domino_status_t shard_sum_piece(int k, int sl, std::string* err) const {
+    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
+    const int32_t col0 = static_cast<int32_t>(sl * s.ds);
+    if (sr != s0) {
+      cudaEvent_t ev = ev_piece[k * s.S + sl];
+      cudaEventRecord(ev, s0);
+      cudaStreamWaitEvent(sr, ev, 0);
+    }
+    ShardSumParams q;
+    memset(&q, 0, sizeof q);
+    const size_t zoff = (static_cast<size_t>(row0) * s.d + col0) * s.psize;
+    for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
+    q.rows = s.Mc;
+    q.cols = s.ds;
+    q.ld_part = s.d;
+    q.ld_y = s.d;
+    q.y = static_cast<uint8_t*>(Y) + (static_cast<size_t>(row0) * s.d + col0) * 2;
+    q.P = s.P;
+    q.f32 = s.partial == DOMINO_PARTIAL_F32;
+    return timed(*T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
+                 [&] { return launch_shard_sum(q, ds->num_sms, sr, err); });
+  }
+};
+
+// The backward of one batch: dh() over all M, then per chunk dx_chunk(k) (the
+// partial input gradients of every slice and their shard-sums on the reduction
+// stream), then dw() over all M.
+struct BwdSeq {
+  Shape s{};
+  DeviceState* ds = nullptr;
+  Timer* T = nullptr;
+  cudaStream_t s0 = nullptr, sr = nullptr;
+  bool pair = true;
+  DeviceStatus* status = nullptr;
+  uint64_t tmo = 0;
+  const void* X = nullptr;
+  const void* const* A_shards = nullptr;
+  const void* const* B_shards = nullptr;
+  const void* dY = nullptr;
+  void* dX = nullptr;
+  void* const* dA_shards = nullptr;
+  void* const* dB_shards = nullptr;
+  const void* pre[kMaxShards] = {};
+  const void* H[kMaxShards] = {};
+  void* dG[kMaxShards] = {};
+  void* Z[kMaxShards] = {};
+  cudaEvent_t* ev_piece = nullptr;  // mu * S events, one per piece
+
+  int64_t nF() const { return s.nact * s.Fp; }  // columns of the pre-activation block / rows of A_shards[p]
+
+  void bind(uint8_t* ws, const WsLayout& W, const void* saved) {
+    for (int p = 0; p < s.P; ++p) {
+      const uint8_t* blk = static_cast<const uint8_t*>(saved) + saved_shard_bytes(s) * p;
+      pre[p] = blk;
+      H[p] = blk + static_cast<size_t>(s.M) * nF() * 2;
+      dG[p] = ws + W.dg_off + W.dg_shard * p;
+      Z[p] = ws + W.z_off + W.z_shard * p;
+    }
+  }
+
+  // dH_p = dY B_p^T with the activation derivative fused -> dG_p, over all M
+  // tokens in one launch: it exchanges nothing, so it needs no chunking, and one
+  // launch over M fills the GPU's clusters better than mu launches over M/mu.
+  domino_status_t dh(std::string* err) const {
+    static const int kDgEpi[4] = {EPI_DG_GELU, EPI_DG_GELU_TANH, EPI_DG_SWIGLU, EPI_DG_IDENTITY};
+    GemmLaunch L;
+    L.epi = kDgEpi[s.act];
+    L.b_mn = true;
+    L.num_shards = s.P;
+    for (int p = 0; p < s.P; ++p) {
+      L.a[p] = {dY, s.M, s.d, s.d};
+      L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};  // stored [d][Fp]: K = d rows, N = Fp contiguous
+      L.b1[p] = L.b0[p];
+      L.out[p] = dG[p];
+      L.aux[p] = const_cast<void*>(pre[p]);
+    }
+    L.ldo = nF();
+    L.out_rows = s.M;
+    L.out_cols = nF();
+    L.ld_aux = nF();
+    L.aux_u_off = s.Fp;
+    L.out_u_off = s.Fp;
+    L.a_row0 = 0;
+    L.out_row0 = 0;
+    L.rows = static_cast<int32_t>(s.M);
+    L.group_rows = static_cast<int32_t>(s.Mc);  // dY rows of a group stay in L2 across all column tiles
+    L.n_base = 0;
+    L.n_end = static_cast<int32_t>(s.Fp);
+    L.K = s.d;
+    L.status = status;
+    L.timeout_ns = tmo;
+    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DH, 0, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+  }
+
+  domino_status_t dx_chunk(int k, std::string* err) const {
+    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
+    for (int sl = 0; sl < s.S; ++sl) {
+      const int32_t col0 = static_cast<int32_t>(sl * s.ds);
+      // ---- partial input gradient of shard p: dG_{k,p} A_p^T -> Z_p
+      GemmLaunch L;
+      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
+      L.b_mn = true;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {dG[p], s.M, nF(), nF()};
+        L.b0[p] = {A_shards[p], nF(), s.d, s.d};  // stored [nF][d]: K = nF rows, N = d contiguous
+        L.b1[p] = L.b0[p];
+        L.out[p] = Z[p];
+      }
+      L.ldo = s.d;
+      L.out_rows = s.M;
+      L.out_cols = s.d;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = col0;
+      L.n_end = static_cast<int32_t>(col0 + s.ds);
+      L.K = nF();
+      L.status = status;
+      L.timeout_ns = tmo;
+      domino_status_t st =
+          timed(*T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return run_gemm(L, ds, pair, s0, err); });
+      if (st != DOMINO_OK) return st;
+      // ---- dX_k[:, s] = sum_p of the partials (the all-reduce of the input gradient)
+      if (sr != s0) {
+        cudaEvent_t ev = ev_piece[k * s.S + sl];
+        cudaEventRecord(ev, s0);
+        cudaStreamWaitEvent(sr, ev, 0);
+      }
+      ShardSumParams q;
+      memset(&q, 0, sizeof q);
+      const size_t zoff = (static_cast<size_t>(row0) * s.d + col0) * s.psize;
+      for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
+      q.rows = s.Mc;
+      q.cols = s.ds;
+      q.ld_part = s.d;
+      q.ld_y = s.d;
+      q.y = static_cast<uint8_t*>(dX) + (static_cast<size_t>(row0) * s.d + col0) * 2;
+      q.P = s.P;
+      q.f32 = s.partial == DOMINO_PARTIAL_F32;
+      st = timed(*T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
+                 [&] { return launch_shard_sum(q, ds->num_sms, sr, err); });
+      if (st != DOMINO_OK) return st;
+    }
+    return DOMINO_OK;
+  }
+
+  // Weight gradients over all M (they run while the last shard-sum drains).
+  domino_status_t dw(std::string* err) const {
+    {
+      GemmLaunch L;  // dA_p = dG_p^T X : [nF, d], contraction over tokens
+      L.epi = EPI_Z_BF16;
+      L.a_mn = true;
+      L.b_mn = true;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {dG[p], s.M, nF(), nF()};
+        L.b0[p] = {X, s.M, s.d, s.d};
+        L.b1[p] = L.b0[p];
+        L.out[p] = dA_shards[p];
+      }
+      L.ldo = s.d;
+      L.out_rows = nF();
+      L.out_cols = s.d;
+      L.rows = static_cast<int32_t>(nF());
+      L.n_base = 0;
+      L.n_end = static_cast<int32_t>(s.d);
+      L.K = s.M;
+      L.status = status;
+      L.timeout_ns = tmo;
+      domino_status_t st =
+          timed(*T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      if (st != DOMINO_OK) return st;
+    }
+    GemmLaunch L;  // dB_p = dY^T H_p : [d, Fp]
+    L.epi = EPI_Z_BF16;
+    L.a_mn = true;
+    L.b_mn = true;
+    L.num_shards = s.P;
+    for (int p = 0; p < s.P; ++p) {
+      L.a[p] = {dY, s.M, s.d, s.d};
+      L.b0[p] = {H[p], s.M, s.Fp, s.Fp};
+      L.b1[p] = L.b0[p];
+      L.out[p] = dB_shards[p];
+    }
+    L.ldo = s.Fp;
+    L.out_rows = s.d;
+    L.out_cols = s.Fp;
+    L.rows = static_cast<int32_t>(s.d);
+    L.n_base = 0;
+    L.n_end = static_cast<int32_t>(s.Fp);
+    L.K = s.M;
+    L.status = status;
+    L.timeout_ns = tmo;
+    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return run_gemm(L, ds, pair, s0, err); });
+  }
+};
+
+// Makes `sr` wait for everything issued on `s0` so far (before a sequence's first
+// reduction), and `s0` wait for everything on `sr` (before the call returns).
+void fork_streams(const DeviceState* ds, cudaStream_t s0, cudaStream_t sr) {
+  if (sr == s0) return;
+  cudaEventRecord(ds->ev_fork, s0);
+  cudaStreamWaitEvent(sr, ds->ev_fork, 0);
+}
+void join_streams(const DeviceState* ds, cudaStream_t s0, cudaStream_t sr) {
+  if (sr == s0) return;
+  cudaEventRecord(ds->ev_join, sr);
+  cudaStreamWaitEvent(s0, ds->ev_join, 0);
+}
+
+
 }  // namespace
 
 namespace domino {
@@ -321,24 +645,22 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
   const bool pair = (desc->flags & DOMINO_FLAG_ONE_CTA) == 0 && ds->pair_max_clusters > 0;
   if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
 
-  // Where H and the saved pre-activations go.
-  void* H[kMaxShards];
-  void* pre[kMaxShards];
-  for (int p = 0; p < s.P; ++p) {
-    if (saved) {
-      uint8_t* blk = static_cast<uint8_t*>(saved) + saved_shard_bytes(s) * p;
-      pre[p] = blk;
-      H[p] = blk + static_cast<size_t>(s.M) * s.Fp * s.nact * 2;
-    } else {
-      pre[p] = nullptr;
-      H[p] = ws + W.h_off + W.h_shard * p;
-    }
-  }
-  void* Z[kMaxShards];
-  for (int p = 0; p < s.P; ++p) Z[p] = ws + W.z_off + W.z_shard * p;
-
+  FwdSeq f;
+  f.s = s;
+  f.ds = ds;
+  f.T = &T;
+  f.s0 = s0;
+  f.sr = sr;
+  f.pair = pair;
+  f.status = dstat;
+  f.tmo = tmo;
+  f.X = X;
+  f.A_shards = A_shards;
+  f.B_shards = B_shards;
+  f.Y = Y;
+  f.ev_piece = ds->ev_piece;
+  f.bind(ws, W, saved);
   static const int kEpiOfAct[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_SWIGLU, EPI_H_IDENTITY};
-  const bool swiglu = s.act == DOMINO_ACT_SWIGLU;
   std::string err;
 
   if (s.schedule == DOMINO_SCHEDULE_FUSED) {
@@ -348,9 +670,9 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
     for (int p = 0; p < s.P; ++p) {
       F.A_shards[p] = A_shards[p];
       F.B_shards[p] = B_shards[p];
-      F.H[p] = H[p];
-      F.aux[p] = pre[p];
-      F.Z[p] = Z[p];
+      F.H[p] = f.H[p];
+      F.aux[p] = f.pre[p];
+      F.Z[p] = f.Z[p];
     }
     F.Y = Y;
     F.sync = reinterpret_cast<uint32_t*>(ws + W.sync_off);
@@ -383,104 +705,12 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
     return DOMINO_OK;
   }
 
-  if (sr != s0) {
-    cudaEventRecord(ds->ev_fork, s0);
-    cudaStreamWaitEvent(sr, ds->ev_fork, 0);
-  }
-
+  fork_streams(ds, s0, sr);
   for (int k = 0; k < s.mu; ++k) {
-    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
-    // ---- GEMM1: H_{k,p} = act(X_k A_p), all shards in one launch
-    {
-      GemmLaunch L;
-      L.epi = kEpiOfAct[s.act];
-      L.num_shards = s.P;
-      for (int p = 0; p < s.P; ++p) {
-        L.a[p] = {X, s.M, s.d, s.d};
-        const uint8_t* Ap = static_cast<const uint8_t*>(A_shards[p]);
-        if (swiglu) {
-          L.b0[p] = {Ap, s.Fp, s.d, s.d};
-          L.b1[p] = {Ap + static_cast<size_t>(s.Fp) * s.d * 2, s.Fp, s.d, s.d};
-        } else {
-          L.b0[p] = {Ap, s.Fp, s.d, s.d};
-          L.b1[p] = L.b0[p];
-        }
-        L.out[p] = H[p];
-        L.aux[p] = pre[p];
-      }
-      L.n_tile = swiglu ? kBN / 2 : kBN;
-      L.b1_off = swiglu ? 0 : kBN / 2;
-      L.ldo = s.Fp;
-      L.out_rows = s.M;
-      L.out_cols = s.Fp;
-      L.ld_aux = s.Fp * s.nact;
-      L.aux_u_off = s.Fp;
-      L.a_row0 = row0;
-      L.out_row0 = row0;
-      L.rows = static_cast<int32_t>(s.Mc);
-      L.n_base = 0;
-      L.n_end = static_cast<int32_t>(s.Fp);
-      L.K = s.d;
-      L.status = dstat;
-      L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
-      if (st != DOMINO_OK) return fail(st, err);
-    }
-    for (int sl = 0; sl < s.S; ++sl) {
-      const int32_t col0 = static_cast<int32_t>(sl * s.ds);
-      // ---- GEMM2: Z_{k,p,s} = H_{k,p} B_p[:, slice s]
-      GemmLaunch L;
-      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
-      L.num_shards = s.P;
-      for (int p = 0; p < s.P; ++p) {
-        L.a[p] = {H[p], s.M, s.Fp, s.Fp};
-        L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};
-        L.b1[p] = L.b0[p];
-        L.out[p] = Z[p];
-      }
-      L.n_tile = kBN;
-      L.b1_off = kBN / 2;
-      L.ldo = s.d;
-      L.out_rows = s.M;
-      L.out_cols = s.d;
-      L.a_row0 = row0;
-      L.out_row0 = row0;
-      L.rows = static_cast<int32_t>(s.Mc);
-      L.n_base = col0;
-      L.n_end = static_cast<int32_t>(col0 + s.ds);
-      L.K = s.Fp;
-      L.status = dstat;
-      L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return run_gemm(L, ds, pair, s0, &err); });
-      if (st != DOMINO_OK) return fail(st, err);
-
-      // ---- shard-sum of piece (k, s)
-      if (sr != s0) {
-        cudaEvent_t ev = ds->ev_piece[k * s.S + sl];
-        cudaEventRecord(ev, s0);
-        cudaStreamWaitEvent(sr, ev, 0);
-      }
-      ShardSumParams q;
-      memset(&q, 0, sizeof q);
-      const size_t zoff = (static_cast<size_t>(row0) * s.d + col0) * s.psize;
-      for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
-      q.rows = s.Mc;
-      q.cols = s.ds;
-      q.ld_part = s.d;
-      q.ld_y = s.d;
-      q.y = static_cast<uint8_t*>(Y) + (static_cast<size_t>(row0) * s.d + col0) * 2;
-      q.P = s.P;
-      q.f32 = s.partial == DOMINO_PARTIAL_F32;
-      st = timed(T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
-                 [&] { return launch_shard_sum(q, ds->num_sms, sr, &err); });
-      if (st != DOMINO_OK) return fail(st, err);
-    }
+    st = f.chunk(k, &err);
+    if (st != DOMINO_OK) return fail(st, err);
   }
-
-  if (sr != s0) {
-    cudaEventRecord(ds->ev_join, sr);
-    cudaStreamWaitEvent(s0, ds->ev_join, 0);
-  }
+  join_streams(ds, s0, sr);
   return DOMINO_OK;
 }
 
@@ -531,160 +761,139 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   const bool pair = (desc->flags & DOMINO_FLAG_ONE_CTA) == 0 && ds->pair_max_clusters > 0;
   if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
 
-  const int64_t nF = s.nact * s.Fp;  // columns of the pre-activation block / rows of A_shards[p]
-  const void* pre[kMaxShards];
-  const void* H[kMaxShards];
-  void* dG[kMaxShards];
-  void* Z[kMaxShards];
-  for (int p = 0; p < s.P; ++p) {
-    const uint8_t* blk = static_cast<const uint8_t*>(saved) + saved_shard_bytes(s) * p;
-    pre[p] = blk;
-    H[p] = blk + static_cast<size_t>(s.M) * nF * 2;
-    dG[p] = ws + W.dg_off + W.dg_shard * p;
-    Z[p] = ws + W.z_off + W.z_shard * p;
-  }
-  static const int kDgEpi[4] = {EPI_DG_GELU, EPI_DG_GELU_TANH, EPI_DG_SWIGLU, EPI_DG_IDENTITY};
+  BwdSeq g;
+  g.s = s;
+  g.ds = ds;
+  g.T = &T;
+  g.s0 = s0;
+  g.sr = sr;
+  g.pair = pair;
+  g.status = dstat;
+  g.tmo = tmo;
+  g.X = X;
+  g.A_shards = A_shards;
+  g.B_shards = B_shards;
+  g.dY = dY;
+  g.dX = dX;
+  g.dA_shards = dA_shards;
+  g.dB_shards = dB_shards;
+  g.ev_piece = ds->ev_piece;
+  g.bind(ws, W, saved);
   std::string err;
-  if (sr != s0) {
-    cudaEventRecord(ds->ev_fork, s0);
-    cudaStreamWaitEvent(sr, ds->ev_fork, 0);
+  fork_streams(ds, s0, sr);
+  st = g.dh(&err);
+  for (int k = 0; k < s.mu && st == DOMINO_OK; ++k) st = g.dx_chunk(k, &err);
+  if (st == DOMINO_OK) st = g.dw(&err);
+  if (st != DOMINO_OK) return fail(st, err);
+  join_streams(ds, s0, sr);
+  return DOMINO_OK;
+}
+
+size_t domino_mlp_interleaved_workspace_size(const domino_mlp_desc_t* desc) {
+  Shape s;
+  if (check_desc(desc, &s) != DOMINO_OK) return 0;
+  return align_up(ws_layout(s, false).total, 256) + ws_layout(s, true).total;
+}
+
+domino_status_t domino_mlp_fwd_bwd_interleaved(const domino_mlp_desc_t* desc, const void* const* A_shards,
+                                               const void* const* B_shards, const void* Xa, void* Ya,
+                                               void* saved_a, const void* Xb, const void* dYb, const void* saved_b,
+                                               void* dXb, void* const* dA_shards, void* const* dB_shards,
+                                               void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  domino_status_t st = check_desc(desc, &s);
+  if (st != DOMINO_OK) return st;
+  if (s.schedule == DOMINO_SCHEDULE_FUSED)
+    return fail(DOMINO_ERR_UNSUPPORTED, "interleaving places launches between pieces: use SERIAL or STREAMS");
+  if (!A_shards || !B_shards || !dA_shards || !dB_shards)
+    return fail(DOMINO_ERR_INVALID_ARG, "A_shards, B_shards, dA_shards and dB_shards must be non-NULL");
+  for (int p = 0; p < s.P; ++p) {
+    if (!A_shards[p] || !B_shards[p] || !dA_shards[p] || !dB_shards[p])
+      return fail(DOMINO_ERR_INVALID_ARG, "NULL shard pointer");
+    if (!aligned16(A_shards[p]) || !aligned16(B_shards[p]) || !aligned16(dA_shards[p]) || !aligned16(dB_shards[p]))
+      return fail(DOMINO_ERR_ALIGNMENT, "shard pointers must be 16-byte aligned");
   }
-  // ---- dH_p = dY B_p^T with the activation derivative fused -> dG_p, over all
-  // M tokens in one launch: it exchanges nothing, so it needs no chunking, and
-  // one launch over M fills the GPU's clusters better than mu launches over M/mu.
-  {
-    GemmLaunch L;
-    L.epi = kDgEpi[s.act];
-    L.b_mn = true;
-    L.num_shards = s.P;
+  cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  if (s.M == 0) {
+    // both strands are empty: strand b's weight gradients are zero, nothing else is touched
     for (int p = 0; p < s.P; ++p) {
-      L.a[p] = {dY, s.M, s.d, s.d};
-      L.b0[p] = {B_shards[p], s.d, s.Fp, s.Fp};  // stored [d][Fp]: K = d rows, N = Fp contiguous
-      L.b1[p] = L.b0[p];
-      L.out[p] = dG[p];
-      L.aux[p] = const_cast<void*>(pre[p]);
+      cudaError_t e = cudaMemsetAsync(dA_shards[p], 0, static_cast<size_t>(s.nact) * s.Fp * s.d * 2, s0);
+      if (e == cudaSuccess) e = cudaMemsetAsync(dB_shards[p], 0, static_cast<size_t>(s.d) * s.Fp * 2, s0);
+      if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("memset: ") + cudaGetErrorString(e));
     }
-    L.ldo = nF;
-    L.out_rows = s.M;
-    L.out_cols = nF;
-    L.ld_aux = nF;
-    L.aux_u_off = s.Fp;
-    L.out_u_off = s.Fp;
-    L.a_row0 = 0;
-    L.out_row0 = 0;
-    L.rows = static_cast<int32_t>(s.M);
-    L.group_rows = static_cast<int32_t>(s.Mc);  // dY rows of a group stay in L2 across all column tiles
-    L.n_base = 0;
-    L.n_end = static_cast<int32_t>(s.Fp);
-    L.K = s.d;
-    L.status = dstat;
-    L.timeout_ns = tmo;
-    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DH, 0, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
-    if (st != DOMINO_OK) return fail(st, err);
+    return DOMINO_OK;
   }
-  for (int k = 0; k < s.mu; ++k) {
-    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
-    for (int sl = 0; sl < s.S; ++sl) {
-      const int32_t col0 = static_cast<int32_t>(sl * s.ds);
-      // ---- partial input gradient of shard p: dG_{k,p} A_p^T -> Z_p
-      GemmLaunch L;
-      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
-      L.b_mn = true;
-      L.num_shards = s.P;
-      for (int p = 0; p < s.P; ++p) {
-        L.a[p] = {dG[p], s.M, nF, nF};
-        L.b0[p] = {A_shards[p], nF, s.d, s.d};  // stored [nF][d]: K = nF rows, N = d contiguous
-        L.b1[p] = L.b0[p];
-        L.out[p] = Z[p];
-      }
-      L.ldo = s.d;
-      L.out_rows = s.M;
-      L.out_cols = s.d;
-      L.a_row0 = row0;
-      L.out_row0 = row0;
-      L.rows = static_cast<int32_t>(s.Mc);
-      L.n_base = col0;
-      L.n_end = static_cast<int32_t>(col0 + s.ds);
-      L.K = nF;
-      L.status = dstat;
-      L.timeout_ns = tmo;
-      st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return run_gemm(L, ds, pair, s0, &err); });
-      if (st != DOMINO_OK) return fail(st, err);
-      // ---- dX_k[:, s] = sum_p of the partials (the all-reduce of the input gradient)
-      if (sr != s0) {
-        cudaEvent_t ev = ds->ev_piece[k * s.S + sl];
-        cudaEventRecord(ev, s0);
-        cudaStreamWaitEvent(sr, ev, 0);
-      }
-      ShardSumParams q;
-      memset(&q, 0, sizeof q);
-      const size_t zoff = (static_cast<size_t>(row0) * s.d + col0) * s.psize;
-      for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
-      q.rows = s.Mc;
-      q.cols = s.ds;
-      q.ld_part = s.d;
-      q.ld_y = s.d;
-      q.y = static_cast<uint8_t*>(dX) + (static_cast<size_t>(row0) * s.d + col0) * 2;
-      q.P = s.P;
-      q.f32 = s.partial == DOMINO_PARTIAL_F32;
-      st = timed(T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
-                 [&] { return launch_shard_sum(q, ds->num_sms, sr, &err); });
-      if (st != DOMINO_OK) return fail(st, err);
-    }
+  if (!Xa || !Ya || !Xb || !dYb || !saved_b || !dXb || !workspace)
+    return fail(DOMINO_ERR_INVALID_ARG, "Xa, Ya, Xb, dYb, saved_b, dXb and workspace must be non-NULL");
+  if (!aligned16(Xa) || !aligned16(Ya) || (saved_a && !aligned16(saved_a)) || !aligned16(Xb) || !aligned16(dYb) ||
+      !aligned16(saved_b) || !aligned16(dXb) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(DOMINO_ERR_ALIGNMENT, "tensors must be 16-byte and workspace 256-byte aligned");
+  const WsLayout Wa = ws_layout(s, false);
+  const WsLayout Wb = ws_layout(s, true);
+  const size_t off_b = align_up(Wa.total, 256);
+  if (workspace_bytes < off_b + Wb.total)
+    return fail(DOMINO_ERR_WORKSPACE, "workspace smaller than domino_mlp_interleaved_workspace_size()");
+
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != DOMINO_OK) return st;
+  cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
+  const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DeviceStatus* dstat = reinterpret_cast<DeviceStatus*>(ws);  // both strands report here
+  Timer T;
+  T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
+  T.ds = ds;
+  const bool pair = (desc->flags & DOMINO_FLAG_ONE_CTA) == 0 && ds->pair_max_clusters > 0;
+  if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
+
+  FwdSeq f;
+  f.s = s;
+  f.ds = ds;
+  f.T = &T;
+  f.s0 = s0;
+  f.sr = sr;
+  f.pair = pair;
+  f.status = dstat;
+  f.tmo = tmo;
+  f.X = Xa;
+  f.A_shards = A_shards;
+  f.B_shards = B_shards;
+  f.Y = Ya;
+  f.ev_piece = ds->ev_piece;
+  f.bind(ws, Wa, saved_a);
+  BwdSeq g;
+  g.s = s;
+  g.ds = ds;
+  g.T = &T;
+  g.s0 = s0;
+  g.sr = sr;
+  g.pair = pair;
+  g.status = dstat;
+  g.tmo = tmo;
+  g.X = Xb;
+  g.A_shards = A_shards;
+  g.B_shards = B_shards;
+  g.dY = dYb;
+  g.dX = dXb;
+  g.dA_shards = dA_shards;
+  g.dB_shards = dB_shards;
+  g.ev_piece = ds->ev_piece_b;
+  g.bind(ws + off_b, Wb, saved_b);
+
+  // strand b's dH first (no exchange), then the two strands' chunks alternate:
+  // the shard-sums of one strand's chunk k run on the reduction stream beside
+  // the other strand's GEMMs; strand b's weight gradients cover the last ones.
+  std::string err;
+  fork_streams(ds, s0, sr);
+  st = g.dh(&err);
+  for (int k = 0; k < s.mu && st == DOMINO_OK; ++k) {
+    st = f.chunk(k, &err);
+    if (st == DOMINO_OK) st = g.dx_chunk(k, &err);
   }
-  // ---- weight gradients over all M (they run while the last shard-sum drains)
-  {
-    GemmLaunch L;  // dA_p = dG_p^T X : [nF, d], contraction over tokens
-    L.epi = EPI_Z_BF16;
-    L.a_mn = true;
-    L.b_mn = true;
-    L.num_shards = s.P;
-    for (int p = 0; p < s.P; ++p) {
-      L.a[p] = {dG[p], s.M, nF, nF};
-      L.b0[p] = {X, s.M, s.d, s.d};
-      L.b1[p] = L.b0[p];
-      L.out[p] = dA_shards[p];
-    }
-    L.ldo = s.d;
-    L.out_rows = nF;
-    L.out_cols = s.d;
-    L.rows = static_cast<int32_t>(nF);
-    L.n_base = 0;
-    L.n_end = static_cast<int32_t>(s.d);
-    L.K = s.M;
-    L.status = dstat;
-    L.timeout_ns = tmo;
-    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return run_gemm(L, ds, pair, s0, &err); });
-    if (st != DOMINO_OK) return fail(st, err);
-  }
-  {
-    GemmLaunch L;  // dB_p = dY^T H_p : [d, Fp]
-    L.epi = EPI_Z_BF16;
-    L.a_mn = true;
-    L.b_mn = true;
-    L.num_shards = s.P;
-    for (int p = 0; p < s.P; ++p) {
-      L.a[p] = {dY, s.M, s.d, s.d};
-      L.b0[p] = {H[p], s.M, s.Fp, s.Fp};
-      L.b1[p] = L.b0[p];
-      L.out[p] = dB_shards[p];
-    }
-    L.ldo = s.Fp;
-    L.out_rows = s.d;
-    L.out_cols = s.Fp;
-    L.rows = static_cast<int32_t>(s.d);
-    L.n_base = 0;
-    L.n_end = static_cast<int32_t>(s.Fp);
-    L.K = s.M;
-    L.status = dstat;
-    L.timeout_ns = tmo;
-    st = timed(T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return run_gemm(L, ds, pair, s0, &err); });
-    if (st != DOMINO_OK) return fail(st, err);
-  }
-  if (sr != s0) {
-    cudaEventRecord(ds->ev_join, sr);
-    cudaStreamWaitEvent(s0, ds->ev_join, 0);
-  }
+  if (st == DOMINO_OK) st = g.dw(&err);
+  if (st != DOMINO_OK) return fail(st, err);
+  join_streams(ds, s0, sr);
   return DOMINO_OK;
 }
 

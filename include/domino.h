@@ -275,6 +275,32 @@ DOMINO_API int32_t domino_kernel_times(domino_kernel_time_t* out, int32_t max_re
 /* Empties the log (the pooled events are kept for reuse). */
 DOMINO_API void domino_kernel_times_reset(void);
 
+/* Strand interleaving: the forward of one micro-batch (strand a) and the
+ * backward of another (strand b) of the same layer in one call, their launches
+ * interleaved so that the shard-sums of each strand run beside the other
+ * strand's GEMMs (the DHelix review page, "Hiding Communication Cost in
+ * Distributed LLM Training via Micro-batch Co-execution": two strands co-run so
+ * that one strand's communication hides under the other's computation).
+ * Order on `stream`: strand b's dH over all M; then for k = 0..mu-1 strand a's
+ * chunk k (GEMM1, GEMM2 per slice) and strand b's chunk k (dX partials per
+ * slice); then strand b's weight gradients.  Every shard-sum goes to the
+ * reduction stream after an event behind its GEMM (schedule STREAMS) or runs in
+ * order (SERIAL); DOMINO_SCHEDULE_FUSED is rejected with
+ * DOMINO_ERR_UNSUPPORTED.  Results are bit-identical to domino_mlp_fwd(strand a)
+ * and domino_mlp_bwd(strand b) with the same descriptor.
+ * Arguments as for those two calls: A_shards/B_shards shared; Xa -> Ya (and
+ * saved_a, may be NULL); Xb, dYb, saved_b (what the forward of strand b saved)
+ * -> dXb, dA_shards, dB_shards.  workspace: domino_mlp_interleaved_workspace_size()
+ * bytes; device errors are reported in its first header (read it with
+ * domino_query_device_status). */
+DOMINO_API size_t domino_mlp_interleaved_workspace_size(const domino_mlp_desc_t* desc);
+DOMINO_API domino_status_t domino_mlp_fwd_bwd_interleaved(const domino_mlp_desc_t* desc, const void* const* A_shards,
+                                                          const void* const* B_shards, const void* Xa, void* Ya,
+                                                          void* saved_a, const void* Xb, const void* dYb,
+                                                          const void* saved_b, void* dXb, void* const* dA_shards,
+                                                          void* const* dB_shards, void* workspace,
+                                                          size_t workspace_bytes, void* stream);
+
 /* Schedule selection.  The FiCCO page ("Design Space Exploration of DMA based
  * Finer-Grain Compute Communication Overlap", Abstract) picks a decomposition
  * for each operator from its sizes with heuristics, because finer pieces cost

@@ -131,3 +131,16 @@ def test_backward_validates(lib):
     st = lib.domino_mlp_bwd(ctypes.byref(d), 0x30000, arr, arr, None, 0x50000, 0x60000, arr, arr, 0x10000,
                             1 << 40, None)
     assert st == 1
+
+
+def test_interleaved_validates(lib):
+    d = desc(schedule="fused")
+    arr = b._ptr_array([0x20000] * 2)
+    args = (arr, arr, 0x30000, 0x40000, None, 0x30000, 0x50000, 0x60000, 0x70000, arr, arr, 0x10000, 1 << 40, None)
+    assert lib.domino_mlp_fwd_bwd_interleaved(ctypes.byref(d), *args) == 2  # FUSED: not interleavable
+    d = desc(schedule="streams")
+    assert b.interleaved_workspace_size(d) >= b.workspace_size(d) + b.workspace_size(d, with_bwd=True)
+    bad = (arr, arr, 0x30000, None) + args[4:]
+    assert lib.domino_mlp_fwd_bwd_interleaved(ctypes.byref(d), *bad) == 1
+    small = args[:-2] + (b.interleaved_workspace_size(d) - 1, None)
+    assert lib.domino_mlp_fwd_bwd_interleaved(ctypes.byref(d), *small) == 4

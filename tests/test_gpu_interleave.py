@@ -1,0 +1,52 @@
+"""Strand interleaving (domino_mlp_fwd_bwd_interleaved) on the GB300: the forward
+of strand a and the backward of strand b in one call give bit-for-bit the
+results of a separate domino_mlp_fwd(a) and domino_mlp_bwd(b)."""
+import pytest
+import torch
+
+from communication_overlap_domino_gb300 import binding as b
+from communication_overlap_domino_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _strands(w):
+    dev = torch.device("cuda:0")
+    ta, tb = wl.generate(w, 31, with_dy=True), wl.generate(w, 32, with_dy=True)
+    A = (ta["Wg"].to(dev), ta["Wu"].to(dev)) if w.act == "swiglu" else ta["A"].to(dev)
+    A_sh, B_sh = b.shard_weights(A, ta["B"].to(dev), w.P)
+    return A_sh, B_sh, ta["X"].to(dev), tb["X"].to(dev), tb["dY"].to(dev)
+
+
+@pytest.mark.parametrize("schedule", ["streams", "serial"])
+@pytest.mark.parametrize("w", [
+    wl.Workload("interleave_ragged", M=600, d=336, F=984, P=3, mu=3, act="gelu", partial="f32", slices=2, bwd=True),
+    wl.Workload("interleave_glu", M=1024, d=512, F=2752, P=2, mu=4, act="swiglu", partial="bf16", bwd=True),
+], ids=lambda w: w.name if isinstance(w, wl.Workload) else w)
+def test_interleaved_equals_separate_calls(w, schedule):
+    A_sh, B_sh, Xa, Xb, dYb = _strands(w)
+    kw = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, schedule)
+    saved_b = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device=Xa.device)
+    b.mlp_fwd(Xb, A_sh, B_sh, schedule="streams", saved=saved_b, **kw)
+    # separate calls
+    saved_a_ref = torch.zeros_like(saved_b)
+    Ya_ref = b.mlp_fwd(Xa, A_sh, B_sh, schedule="streams", saved=saved_a_ref, **kw)
+    dXb_ref, dA_ref, dB_ref = b.mlp_bwd(Xb, A_sh, B_sh, dYb, saved_b, schedule="streams", **kw)
+    # one interleaved call
+    saved_a = torch.zeros_like(saved_b)
+    ws = torch.zeros(b.interleaved_workspace_size(desc), dtype=torch.uint8, device=Xa.device)
+    Ya, dXb, dA, dB = b.mlp_fwd_bwd_interleaved(A_sh, B_sh, Xa, Xb, dYb, saved_b, schedule=schedule,
+                                                saved_a=saved_a, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert b.query_device_status(ws) == 0
+    assert torch.equal(Ya, Ya_ref) and torch.equal(saved_a, saved_a_ref) and torch.equal(dXb, dXb_ref)
+    assert all(torch.equal(x, y) for x, y in zip(dA, dA_ref)) and all(torch.equal(x, y) for x, y in zip(dB, dB_ref))
