@@ -20,7 +20,7 @@ STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTE
 ACT = {"gelu": 0, "gelu_tanh": 1, "swiglu": 2, "identity": 3}
 PARTIAL = {"f32": 0, "bf16": 1}
 SCHEDULE = {"serial": 0, "streams": 1, "fused": 2}
-KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused"}
+KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused", 7: "attn"}
 FLAG_KERNEL_TIMES = 1
 FLAG_ONE_CTA = 2
 MAX_SHARDS = 16
@@ -65,6 +65,23 @@ class KernelTime(ctypes.Structure):
     ]
 
 
+class AttnDesc(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64),
+        ("S", ctypes.c_int64),
+        ("d", ctypes.c_int64),
+        ("H", ctypes.c_int32),
+        ("dh", ctypes.c_int32),
+        ("P", ctypes.c_int32),
+        ("mu", ctypes.c_int32),
+        ("partial_dtype", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+        ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
 class PlanHw(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("fused_available", ctypes.c_int32), ("l2_bytes", ctypes.c_int64)]
 
@@ -105,6 +122,8 @@ SIGNATURES = [
     ("domino_kernel_times_reset", None, []),
     ("domino_mlp_plan", ctypes.c_int, [ctypes.POINTER(MlpDesc), ctypes.POINTER(PlanHw), ctypes.POINTER(Plan)]),
     ("domino_mlp_interleaved_workspace_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc)]),
+    ("domino_attn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(AttnDesc)]),
+    ("domino_attn_fwd", ctypes.c_int, [ctypes.POINTER(AttnDesc), _VP, _VPP, _VPP, _VP, _VP, ctypes.c_size_t, _VP]),
     ("domino_mlp_fwd_bwd_interleaved", ctypes.c_int,
      [ctypes.POINTER(MlpDesc), _VPP, _VPP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VPP, _VPP, _VP, ctypes.c_size_t, _VP]),
 ]
@@ -263,6 +282,56 @@ def mlp_bwd(X, A_shards: List, B_shards: List, dY, saved, *, F: int, mu: int, ac
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "domino_mlp_bwd")
     return dX, dA_shards, dB_shards
+
+
+def make_attn_desc(B: int, S: int, d: int, H: int, P: int, mu: int, partial: str, schedule: str = "streams",
+                   dh: int = 128, kernel_times: bool = False, timeout_ns: int = 0, pair_cta: bool = True) -> AttnDesc:
+    flags = (FLAG_KERNEL_TIMES if kernel_times else 0) | (0 if pair_cta else FLAG_ONE_CTA)
+    return AttnDesc(B=B, S=S, d=d, H=H, dh=dh, P=P, mu=mu, partial_dtype=PARTIAL[partial],
+                    schedule=SCHEDULE[schedule], flags=flags, reserved=0, timeout_ns=timeout_ns)
+
+
+def attn_workspace_size(desc: AttnDesc) -> int:
+    return int(lib().domino_attn_workspace_size(ctypes.byref(desc)))
+
+
+def shard_attn_weights(Wqkv, Wo, H: int, P: int):
+    """Splits mathematical-layout attention weights into the ABI's per-shard layout.
+
+    Wqkv: [d, 3 H dh] (query heads, then key heads, then value heads); Wo: [H dh, d].
+    Returns (Wqkv_shards, Wo_shards): Wqkv_shards[p] = [3 Hp dh, d], shard p's query,
+    key and value heads' columns of Wqkv transposed; Wo_shards[p] = Wo[rows_p, :]^T
+    [d, Hp dh]; each contiguous.  A one-time parameter re-layout."""
+    torch = _torch()
+    d, n = Wqkv.shape
+    dh = n // (3 * H)
+    Hp = H // P
+    w = Hp * dh
+    qkv_sh, o_sh = [], []
+    for p in range(P):
+        cols = [Wqkv[:, j * H * dh + p * w: j * H * dh + (p + 1) * w] for j in range(3)]
+        qkv_sh.append(torch.cat(cols, dim=1).t().contiguous())
+        o_sh.append(Wo[p * w:(p + 1) * w, :].t().contiguous())
+    return qkv_sh, o_sh
+
+
+def attn_fwd(X, Wqkv_shards: List, Wo_shards: List, *, S: int, H: int, mu: int, partial: str,
+             schedule: str = "streams", Y=None, workspace=None, stream=None, kernel_times: bool = False,
+             timeout_ns: int = 0, pair_cta: bool = True):
+    """domino_attn_fwd on torch tensors; returns Y [B S, d] bf16."""
+    torch = _torch()
+    M, d = X.shape
+    P = len(Wqkv_shards)
+    desc = make_attn_desc(M // S, S, d, H, P, mu, partial, schedule, 128, kernel_times, timeout_ns, pair_cta)
+    if Y is None:
+        Y = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        workspace = _workspace(max(attn_workspace_size(desc), 256), X.device)
+    st = lib().domino_attn_fwd(ctypes.byref(desc), X.data_ptr(), _ptr_array([w.data_ptr() for w in Wqkv_shards]),
+                               _ptr_array([w.data_ptr() for w in Wo_shards]), Y.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "domino_attn_fwd")
+    return Y
 
 
 def interleaved_workspace_size(desc: MlpDesc) -> int:

@@ -20,6 +20,7 @@
 #include <string>
 #include <vector>
 
+#include "attn.h"
 #include "gemm.h"
 
 using namespace domino;
@@ -91,6 +92,7 @@ domino_status_t device_state(DeviceState** out) {
     e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = prepare_gemm_kernels();
     if (e == cudaSuccess) e = prepare_pair_kernels(&ds.pair_max_clusters);
+    if (e == cudaSuccess) e = prepare_attn_kernel();
     int per_sm = 0;
     if (e == cudaSuccess) e = prepare_fused_kernels(&per_sm, &ds.fused_pair_clusters);
     ds.fused_max_ctas = per_sm * ds.num_sms;
@@ -564,6 +566,187 @@ void join_streams(const DeviceState* ds, cudaStream_t s0, cudaStream_t sr) {
   cudaStreamWaitEvent(s0, ds->ev_join, 0);
 }
 
+// ------------------------------------------------------- attention block
+
+struct AttnShape {
+  int64_t B, S, d, M, Mc;
+  int H, dh, P, Hp, mu, partial, schedule;
+  size_t psize;
+  int64_t qkv_cols() const { return 3 * static_cast<int64_t>(Hp) * dh; }
+  int64_t o_cols() const { return static_cast<int64_t>(Hp) * dh; }
+};
+
+domino_status_t check_attn_desc(const domino_attn_desc_t* desc, AttnShape* s) {
+  if (desc == nullptr) return fail(DOMINO_ERR_INVALID_ARG, "desc is NULL");
+  const domino_attn_desc_t& a = *desc;
+  if (a.B < 0 || a.S <= 0 || a.d <= 0 || a.H < 1 || a.dh < 1)
+    return fail(DOMINO_ERR_INVALID_ARG, "B must be >= 0 and S, d, H, dh > 0");
+  if (a.P < 1 || a.P > DOMINO_MAX_SHARDS) return fail(DOMINO_ERR_INVALID_ARG, "P must be in 1..DOMINO_MAX_SHARDS");
+  if (a.mu < 1) return fail(DOMINO_ERR_INVALID_ARG, "mu must be >= 1");
+  if (a.partial_dtype != DOMINO_PARTIAL_F32 && a.partial_dtype != DOMINO_PARTIAL_BF16)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown partial_dtype");
+  if (a.schedule != DOMINO_SCHEDULE_SERIAL && a.schedule != DOMINO_SCHEDULE_STREAMS &&
+      a.schedule != DOMINO_SCHEDULE_FUSED)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
+  if (a.reserved != 0) return fail(DOMINO_ERR_INVALID_ARG, "reserved must be 0");
+  if ((a.flags & ~(DOMINO_FLAG_KERNEL_TIMES | DOMINO_FLAG_ONE_CTA)) != 0)
+    return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
+  if (a.schedule == DOMINO_SCHEDULE_FUSED)
+    return fail(DOMINO_ERR_UNSUPPORTED, "the attention block runs the SERIAL or STREAMS schedule");
+  if (a.dh != 128) return fail(DOMINO_ERR_UNSUPPORTED, "head width dh must be 128");
+  if (a.S % 128) return fail(DOMINO_ERR_UNSUPPORTED, "S must be a multiple of 128");
+  if (a.H % a.P) return fail(DOMINO_ERR_UNSUPPORTED, "P must divide H");
+  if (a.B % a.mu) return fail(DOMINO_ERR_UNSUPPORTED, "mu must divide B");
+  if (a.mu > DOMINO_MAX_PIECES) return fail(DOMINO_ERR_UNSUPPORTED, "mu exceeds DOMINO_MAX_PIECES");
+  if (a.d % 8) return fail(DOMINO_ERR_ALIGNMENT, "d must be a multiple of 8 (16-byte rows)");
+  const int64_t lim = int64_t(1) << 30;
+  if (a.B * a.S >= lim || a.d >= lim || static_cast<int64_t>(a.H) * a.dh * 3 >= lim)
+    return fail(DOMINO_ERR_UNSUPPORTED, "dimension too large");
+  s->B = a.B;
+  s->S = a.S;
+  s->d = a.d;
+  s->M = a.B * a.S;
+  s->Mc = a.B / a.mu * a.S;
+  s->H = a.H;
+  s->dh = a.dh;
+  s->P = a.P;
+  s->Hp = a.H / a.P;
+  s->mu = a.mu;
+  s->partial = a.partial_dtype;
+  s->schedule = a.schedule;
+  s->psize = a.partial_dtype == DOMINO_PARTIAL_F32 ? 4 : 2;
+  return DOMINO_OK;
+}
+
+struct AttnWs {
+  size_t qkv_off, qkv_shard, o_off, o_shard, z_off, z_shard, total;
+};
+
+AttnWs attn_ws_layout(const AttnShape& s) {
+  AttnWs W;
+  size_t off = kHeaderBytes;
+  W.qkv_shard = static_cast<size_t>(s.M) * s.qkv_cols() * 2;
+  W.qkv_off = off;
+  off = align_up(off + W.qkv_shard * s.P, 256);
+  W.o_shard = static_cast<size_t>(s.M) * s.o_cols() * 2;
+  W.o_off = off;
+  off = align_up(off + W.o_shard * s.P, 256);
+  W.z_shard = static_cast<size_t>(s.M) * s.d * s.psize;
+  W.z_off = off;
+  off = align_up(off + W.z_shard * s.P, 256);
+  W.total = off;
+  return W;
+}
+
+// One chunk of the attention block: projection, attention core, output
+// projection into the partials (caller's stream), shard-sum (reduction stream).
+struct AttnSeq {
+  AttnShape s{};
+  DeviceState* ds = nullptr;
+  Timer* T = nullptr;
+  cudaStream_t s0 = nullptr, sr = nullptr;
+  bool pair = true;
+  DeviceStatus* status = nullptr;
+  uint64_t tmo = 0;
+  const void* X = nullptr;
+  const void* const* Wqkv = nullptr;
+  const void* const* Wo = nullptr;
+  void* Y = nullptr;
+  void* qkv[kMaxShards] = {};
+  void* o[kMaxShards] = {};
+  void* Z[kMaxShards] = {};
+
+  domino_status_t chunk(int k, std::string* err) const {
+    const int32_t row0 = static_cast<int32_t>(k * s.Mc);
+    domino_status_t st;
+    {  // ---- Q | K | V of every shard's heads: X_k Wqkv_p
+      GemmLaunch L;
+      L.epi = EPI_H_IDENTITY;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {X, s.M, s.d, s.d};
+        L.b0[p] = {Wqkv[p], s.qkv_cols(), s.d, s.d};
+        L.b1[p] = L.b0[p];
+        L.out[p] = qkv[p];
+      }
+      L.ldo = s.qkv_cols();
+      L.out_rows = s.M;
+      L.out_cols = s.qkv_cols();
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = 0;
+      L.n_end = static_cast<int32_t>(s.qkv_cols());
+      L.K = s.d;
+      L.status = status;
+      L.timeout_ns = tmo;
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      if (st != DOMINO_OK) return st;
+    }
+    {  // ---- attention core of every (shard, sequence, head, query tile) of the chunk
+      AttnLaunch L;
+      for (int p = 0; p < s.P; ++p) {
+        L.qkv[p] = qkv[p];
+        L.o[p] = o[p];
+      }
+      L.M = s.M;
+      L.S = s.S;
+      L.row0 = row0;
+      L.seqs = static_cast<int32_t>(s.B / s.mu);
+      L.Hp = s.Hp;
+      L.dh = s.dh;
+      L.P = s.P;
+      L.status = status;
+      L.timeout_ns = tmo;
+      st = timed(*T, s0, 0, DOMINO_KERNEL_ATTN, k, 0, [&] { return launch_attn_fwd(L, ds->num_sms, s0, err); });
+      if (st != DOMINO_OK) return st;
+    }
+    {  // ---- output projection of every shard into its partial buffer: O_p Wo_p
+      GemmLaunch L;
+      L.epi = s.partial == DOMINO_PARTIAL_F32 ? EPI_Z_F32 : EPI_Z_BF16;
+      L.num_shards = s.P;
+      for (int p = 0; p < s.P; ++p) {
+        L.a[p] = {o[p], s.M, s.o_cols(), s.o_cols()};
+        L.b0[p] = {Wo[p], s.d, s.o_cols(), s.o_cols()};
+        L.b1[p] = L.b0[p];
+        L.out[p] = Z[p];
+      }
+      L.ldo = s.d;
+      L.out_rows = s.M;
+      L.out_cols = s.d;
+      L.a_row0 = row0;
+      L.out_row0 = row0;
+      L.rows = static_cast<int32_t>(s.Mc);
+      L.n_base = 0;
+      L.n_end = static_cast<int32_t>(s.d);
+      L.K = s.o_cols();
+      L.status = status;
+      L.timeout_ns = tmo;
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      if (st != DOMINO_OK) return st;
+    }
+    // ---- Y_k = sum over p of the partials (the all-reduce of the row-parallel projection)
+    if (sr != s0) {
+      cudaEvent_t ev = ds->ev_piece[k];
+      cudaEventRecord(ev, s0);
+      cudaStreamWaitEvent(sr, ev, 0);
+    }
+    ShardSumParams q;
+    memset(&q, 0, sizeof q);
+    const size_t zoff = static_cast<size_t>(row0) * s.d * s.psize;
+    for (int p = 0; p < s.P; ++p) q.part[p] = static_cast<uint8_t*>(Z[p]) + zoff;
+    q.rows = s.Mc;
+    q.cols = s.d;
+    q.ld_part = s.d;
+    q.ld_y = s.d;
+    q.y = static_cast<uint8_t*>(Y) + static_cast<size_t>(row0) * s.d * 2;
+    q.P = s.P;
+    q.f32 = s.partial == DOMINO_PARTIAL_F32;
+    return timed(*T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, 0,
+                 [&] { return launch_shard_sum(q, ds->num_sms, sr, err); });
+  }
+};
+
 
 }  // namespace
 
@@ -893,6 +1076,71 @@ domino_status_t domino_mlp_fwd_bwd_interleaved(const domino_mlp_desc_t* desc, co
   }
   if (st == DOMINO_OK) st = g.dw(&err);
   if (st != DOMINO_OK) return fail(st, err);
+  join_streams(ds, s0, sr);
+  return DOMINO_OK;
+}
+
+size_t domino_attn_workspace_size(const domino_attn_desc_t* desc) {
+  AttnShape s;
+  if (check_attn_desc(desc, &s) != DOMINO_OK) return 0;
+  return attn_ws_layout(s).total;
+}
+
+domino_status_t domino_attn_fwd(const domino_attn_desc_t* desc, const void* X, const void* const* Wqkv_shards,
+                                const void* const* Wo_shards, void* Y, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  AttnShape s;
+  domino_status_t st = check_attn_desc(desc, &s);
+  if (st != DOMINO_OK) return st;
+  if (s.M == 0) return DOMINO_OK;
+  if (!X || !Wqkv_shards || !Wo_shards || !Y || !workspace)
+    return fail(DOMINO_ERR_INVALID_ARG, "X, Wqkv_shards, Wo_shards, Y and workspace must be non-NULL");
+  for (int p = 0; p < s.P; ++p) {
+    if (!Wqkv_shards[p] || !Wo_shards[p]) return fail(DOMINO_ERR_INVALID_ARG, "NULL shard pointer");
+    if (!aligned16(Wqkv_shards[p]) || !aligned16(Wo_shards[p]))
+      return fail(DOMINO_ERR_ALIGNMENT, "shard pointers must be 16-byte aligned");
+  }
+  if (!aligned16(X) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(DOMINO_ERR_ALIGNMENT, "X, Y must be 16-byte and workspace 256-byte aligned");
+  const AttnWs W = attn_ws_layout(s);
+  if (workspace_bytes < W.total)
+    return fail(DOMINO_ERR_WORKSPACE, "workspace smaller than domino_attn_workspace_size()");
+
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != DOMINO_OK) return st;
+  cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Timer T;
+  T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
+  T.ds = ds;
+  if (T.on && !T.start(s0)) return fail(DOMINO_ERR_CUDA, "cudaEventCreate failed");
+
+  AttnSeq a;
+  a.s = s;
+  a.ds = ds;
+  a.T = &T;
+  a.s0 = s0;
+  a.sr = sr;
+  a.pair = (desc->flags & DOMINO_FLAG_ONE_CTA) == 0 && ds->pair_max_clusters > 0;
+  a.status = reinterpret_cast<DeviceStatus*>(ws);
+  a.tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
+  a.X = X;
+  a.Wqkv = Wqkv_shards;
+  a.Wo = Wo_shards;
+  a.Y = Y;
+  for (int p = 0; p < s.P; ++p) {
+    a.qkv[p] = ws + W.qkv_off + W.qkv_shard * p;
+    a.o[p] = ws + W.o_off + W.o_shard * p;
+    a.Z[p] = ws + W.z_off + W.z_shard * p;
+  }
+  std::string err;
+  fork_streams(ds, s0, sr);
+  for (int k = 0; k < s.mu; ++k) {
+    st = a.chunk(k, &err);
+    if (st != DOMINO_OK) return fail(st, err);
+  }
   join_streams(ds, s0, sr);
   return DOMINO_OK;
 }

@@ -1,0 +1,414 @@
+// Causal multi-head attention core of the sliced tensor-parallel attention
+// block, flash-style on the tensor cores (tcgen05).
+//
+// One work item = one head of one sequence of one shard and one 128-query
+// tile: O = softmax(Q K^T / sqrt(dh) + causal mask) V for those 128 queries,
+// dh = 128.  The keys are visited in blocks of 128 (only the blocks at or below
+// the diagonal); the softmax is kept online (running row maximum m and sum l,
+// the output rescaled by exp2(m_old - m_new) when the maximum grows), so no
+// score matrix ever reaches global memory.
+//
+// Persistent kernel, one CTA per SM, 10 warps:
+//   warp 0      TMA producer: the Q tile once per item, then K_j and V_j of
+//               every key block into a 2-stage ring.
+//   warp 1      tensor-memory allocation; lane 0 issues the MMAs:
+//               S_j = Q K_j^T (M 128, N 128, K 128) into one of two TMEM score
+//               buffers, and PV_j = P_j V_j into the TMEM PV buffer.  S_{j+1} is
+//               issued before PV_j, so the next scores are computed while the
+//               softmax of block j runs.
+//   warps 2-9   two threads per query row (warps w and w + 4 read the same
+//               tensor-memory lanes), each owning 64 of the row's 128 key and
+//               output columns: both take the row maximum over all 128 scores,
+//               each writes its 64 probabilities p = exp2(s * c - m) as bf16 into
+//               shared memory in the MMA's operand layout and keeps its 64
+//               running outputs O = O * alpha + PV_j and its part of the row sum;
+//               after the last block the two parts of the sum are added through
+//               shared memory and O / l is stored as bf16.
+//
+// Barriers (all waits bounded, as in the GEMMs): q_full / q_empty, kv_full[s] /
+// kv_empty[s], s_full[b] / s_empty[b] (256 arrivals), p_full (256), pv_full,
+// pv_empty (256), l_ready[2] (256), final.
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "attn.h"
+#include "ptx.cuh"
+
+namespace domino {
+
+namespace {
+
+constexpr int kAttnThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kTile = 128;                        // queries per item, keys per block, head width
+constexpr int kSub = kTile * 64 * 2;              // 16 KB: 128 rows x 64 bf16 (one 128-byte-swizzled box)
+constexpr int kQBytes = 2 * kSub;                 // Q tile: dh halves 0-63 and 64-127
+constexpr int kPBytes = 2 * kSub;                 // P tile: key halves 0-63 and 64-127
+constexpr int kKBytes = 2 * kSub;                 // K tile: dh halves
+constexpr int kVBytes = 2 * kSub;                 // V tile: 2 blocks of 64 keys x (2 boxes of 64 dh x 64 keys)
+constexpr int kStageBytes = kKBytes + kVBytes;    // 64 KB
+constexpr int kStages = 2;
+constexpr int kLsumBytes = 2 * 2 * kTile * 4;        // row-sum halves, double-buffered by item
+constexpr int kAttnSmemBytes = kQBytes + kPBytes + kStages * kStageBytes + kLsumBytes + 1024 + 256;
+static_assert(kAttnSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kAttnTmemCols = 512;           // S buffers at 0 and 128, PV at 256
+constexpr uint32_t kPvCol = 256;
+
+struct AttnItem {
+  int p, b, h, i;  // shard, sequence of the chunk, head of the shard, query tile
+};
+
+// Items in order of decreasing query tile: the diagonal makes tile i cost i + 1
+// key blocks, so the longest items start first on the persistent CTAs.
+__device__ __forceinline__ AttnItem attn_item(const AttnParams& a, int t) {
+  const int per_tile = a.P * a.seqs * a.Hp;
+  AttnItem it;
+  it.i = a.nq - 1 - t / per_tile;
+  int r = t - (a.nq - 1 - it.i) * per_tile;
+  it.p = r / (a.seqs * a.Hp);
+  r -= it.p * a.seqs * a.Hp;
+  it.b = r / a.Hp;
+  it.h = r - it.b * a.Hp;
+  return it;
+}
+
+// Issues S = Q K^T for the key block in ring stage kv_idx % 2 into score
+// buffer s_idx % 2, once the block has landed and the buffer is free.
+__device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_base, uint32_t qa, uint8_t* skv,
+                                             uint64_t* kv_full, uint64_t* s_empty, uint64_t* s_full,
+                                             uint32_t kv_idx, uint32_t s_idx, volatile int* abort_flag, int t) {
+  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+  const uint32_t st = kv_idx & 1, sb = s_idx & 1;
+  if (!mbar_wait(&kv_full[st], (kv_idx >> 1) & 1, abort_flag, a.timeout_ns, a.status, kSiteMmaFull, t)) return false;
+  if (!mbar_wait(&s_empty[sb], ((s_idx >> 1) & 1) ^ 1, abort_flag, a.timeout_ns, a.status, kSiteMmaTmemEmpty, t))
+    return false;
+  tc_fence_after_sync();
+  const uint32_t ka = smem_u32(skv + st * kStageBytes);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint64_t ad = smem_desc_k128(qa + (k >> 2) * kSub) + 2 * (k & 3);
+    const uint64_t bd = smem_desc_k128(ka + (k >> 2) * kSub) + 2 * (k & 3);
+    mma_bf16_ss(tmem_base + sb * kTile, ad, bd, idesc_s, k != 0 ? 1u : 0u);
+  }
+  mma_commit(&s_full[sb]);
+  return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem;
+  uint8_t* sp = sq + kQBytes;
+  uint8_t* skv = sp + kPBytes;
+  float* lsum = reinterpret_cast<float*>(skv + kStages * kStageBytes);  // [2 buffers][2 halves][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lsum + 2 * 2 * kTile);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;   // [2]
+  uint64_t* kv_empty = bars + 4;  // [2]
+  uint64_t* s_full = bars + 6;    // [2]
+  uint64_t* s_empty = bars + 8;   // [2]
+  uint64_t* p_full = bars + 10;
+  uint64_t* pv_full = bars + 11;
+  uint64_t* pv_empty = bars + 12;
+  uint64_t* final_bar = bars + 13;
+  uint64_t* l_ready = bars + 14;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kSoftmaxThreads);
+      mbar_init(&l_ready[s], kSoftmaxThreads);
+    }
+    mbar_init(p_full, kSoftmaxThreads);
+    mbar_init(pv_full, 1);
+    mbar_init(pv_empty, kSoftmaxThreads);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kAttnTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t q_phase = 0, kv_count = 0;
+    uint32_t issued_q = 0, issued_kv_mask = 0, kv_parity = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < a.num_items && ok && !*abort_flag; t += gridDim.x) {
+      const AttnItem it = attn_item(a, t);
+      const CUtensorMap* mqk = &a.map_qk[it.p];
+      const CUtensorMap* mv = &a.map_v[it.p];
+      const int seq_row0 = a.row0 + it.b * a.S;
+      if (!mbar_wait(q_empty, q_phase ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t)) break;
+      q_phase ^= 1;
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      const int qx = it.h * kTile;
+      const int qy = seq_row0 + it.i * kTile;
+      tma_load_2d(sq, mqk, q_full, qx, qy);
+      tma_load_2d(sq + kSub, mqk, q_full, qx + 64, qy);
+      issued_q = 1;
+      for (int j = 0; j <= it.i; ++j, ++kv_count) {
+        const uint32_t st = kv_count & 1;
+        const uint32_t ph = (kv_count >> 1) & 1;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sk = skv + st * kStageBytes;
+        uint8_t* sv = sk + kKBytes;
+        mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
+        const int ky = seq_row0 + j * kTile;
+        const int kx = (a.Hp + it.h) * kTile;
+        const int vx = (2 * a.Hp + it.h) * kTile;
+        tma_load_2d(sk, mqk, &kv_full[st], kx, ky);
+        tma_load_2d(sk + kSub, mqk, &kv_full[st], kx + 64, ky);
+        // V as the MN-major B operand: per 64-key block, two boxes of 64 dh x 64 keys
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_2d(sv + kb * kSub, mv, &kv_full[st], vx, ky + kb * 64);
+          tma_load_2d(sv + kb * kSub + 8192, mv, &kv_full[st], vx + 64, ky + kb * 64);
+        }
+        issued_kv_mask |= 1u << st;
+        kv_parity = (kv_parity & ~(1u << st)) | (ph << st);
+      }
+    }
+    // drain: every load issued has landed before the CTA can exit
+    volatile int no_abort = 0;
+    if (issued_q) mbar_wait(q_full, (q_phase ^ 1) & 1, &no_abort, tmo, a.status, kSiteDrain, 0);
+    for (int s = 0; s < kStages; ++s)
+      if (issued_kv_mask & (1u << s))
+        mbar_wait(&kv_full[s], (kv_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 1 + s);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+    uint32_t q_phase = 0, kv_count = 0, s_count = 0, p_phase = 0, pv_phase = 0;
+    const uint32_t qa = smem_u32(sq), pa = smem_u32(sp);
+    bool ok = true;
+    for (int t = blockIdx.x; t < a.num_items && ok && !*abort_flag; t += gridDim.x) {
+      const AttnItem it = attn_item(a, t);
+      if (!mbar_wait(q_full, q_phase, abort_flag, tmo, a.status, kSiteMmaFull, t)) break;
+      q_phase ^= 1;
+      const uint32_t kv0 = kv_count;
+      if (!attn_issue_s(a, tmem_base, qa, skv, kv_full, s_empty, s_full, kv_count, s_count, abort_flag, t)) break;
+      for (int j = 0; j <= it.i; ++j) {
+        if (j + 1 <= it.i && !attn_issue_s(a, tmem_base, qa, skv, kv_full, s_empty, s_full, kv0 + j + 1,
+                                           s_count + j + 1, abort_flag, t)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(p_full, p_phase, abort_flag, tmo, a.status, kSiteAttnP, t) ||
+            !mbar_wait(pv_empty, pv_phase ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, t)) {
+          ok = false;
+          break;
+        }
+        p_phase ^= 1;
+        pv_phase ^= 1;
+        tc_fence_after_sync();
+        const uint32_t st = (kv0 + j) & 1;
+        const uint32_t va = smem_u32(skv + st * kStageBytes + kKBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ad = smem_desc_k128(pa + (k >> 2) * kSub) + 2 * (k & 3);
+          const uint64_t bd = smem_desc_mn128(va + (k >> 2) * kSub) + (2048 >> 4) * (k & 3);
+          mma_bf16_ss(tmem_base + kPvCol, ad, bd, idesc_pv, k != 0 ? 1u : 0u);
+        }
+        mma_commit(pv_full);
+        mma_commit(&kv_empty[st]);
+      }
+      kv_count = kv0 + it.i + 1;
+      s_count += it.i + 1;
+      if (!ok) break;
+      mma_commit(q_empty);
+    }
+    mma_commit(final_bar);
+    volatile int no_abort = 0;
+    mbar_wait(final_bar, 0, &no_abort, tmo, a.status, kSiteDrain, 99);
+  } else if (warp >= 2) {
+    // --------------------------------------------------- softmax / output
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // key / output columns half * 64 .. + 64
+    const int r = quarter * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t s_count = 0, pv_phase = 0, item_count = 0;
+    for (int t = blockIdx.x; t < a.num_items && !*abort_flag; t += gridDim.x, ++item_count) {
+      const AttnItem it = attn_item(a, t);
+      float o[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) o[c] = 0.0f;
+      float m_run = -INFINITY, l_run = 0.0f;
+      bool ok = true;
+      for (int j = 0; j <= it.i; ++j, ++s_count) {
+        const uint32_t sb = s_count & 1;
+        if (!mbar_wait(&s_full[sb], (s_count >> 1) & 1, abort_flag, tmo, a.status, kSiteEpilogueTmemFull, t)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t ts = tmem_base + lane_off + sb * kTile;
+        const bool diag = j == it.i;
+        // pass 1: row maximum of the visible scores (all 128 keys)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(ts + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!diag || c * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v[e]));
+        }
+        const float m_new = fmaxf(m_run, mx * a.scale_log2);
+        // pass 2: this thread's 64 probabilities, written as the bf16 A operand of P V
+        float sum = 0.0f;
+        uint8_t* row = sp + half * kSub + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * half + cc;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(ts + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float pr[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int key = c * 32 + q4 * 8 + e;
+              pr[e] = (!diag || key <= r) ? exp2f(fmaf(__uint_as_float(v[q4 * 8 + e]), a.scale_log2, -m_new)) : 0.0f;
+              sum += pr[e];
+            }
+            const int chunk = cc * 4 + q4;  // 16-byte chunk of the 128-byte row
+            uint4 w;
+            w.x = pack_bf16(pr[0], pr[1]);
+            w.y = pack_bf16(pr[2], pr[3]);
+            w.z = pack_bf16(pr[4], pr[5]);
+            w.w = pack_bf16(pr[6], pr[7]);
+            *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w;
+          }
+        }
+        fence_proxy_async_shared();  // P is read by the tensor cores (async proxy)
+        tc_fence_before_sync();
+        mbar_arrive(&s_empty[sb]);
+        mbar_arrive(p_full);
+        const float alpha = exp2f(m_run - m_new);
+        l_run = l_run * alpha + sum;
+        m_run = m_new;
+        // O = O * alpha + P_j V_j, this thread's 64 output columns
+        if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
+          ok = false;
+          break;
+        }
+        pv_phase ^= 1;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_off + kPvCol + half * 64 + cc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[cc * 32 + e] = fmaf(o[cc * 32 + e], alpha, __uint_as_float(v[e]));
+        }
+        tc_fence_before_sync();
+        mbar_arrive(pv_empty);
+      }
+      if (!ok) break;
+      // the row sum: this thread's part plus its partner's, through shared memory
+      const uint32_t lb = item_count & 1;
+      float* lbuf = lsum + lb * 2 * kTile;
+      lbuf[half * kTile + r] = l_run;
+      mbar_arrive(&l_ready[lb]);
+      if (!mbar_wait(&l_ready[lb], (item_count >> 1) & 1, abort_flag, tmo, a.status, kSiteAttnPV, t)) break;
+      const float inv = 1.0f / (lbuf[r] + lbuf[kTile + r]);
+      // O / l as bf16: this thread's 128 contiguous bytes of the row
+      const int64_t grow = a.row0 + static_cast<int64_t>(it.b) * a.S + it.i * kTile + r;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o[it.p]) + grow * a.ldo + it.h * kTile +
+                                            half * 64);
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        uint4 w;
+        w.x = pack_bf16(o[8 * q8 + 0] * inv, o[8 * q8 + 1] * inv);
+        w.y = pack_bf16(o[8 * q8 + 2] * inv, o[8 * q8 + 3] * inv);
+        w.z = pack_bf16(o[8 * q8 + 4] * inv, o[8 * q8 + 5] * inv);
+        w.w = pack_bf16(o[8 * q8 + 6] * inv, o[8 * q8 + 7] * inv);
+        dst[q8] = w;
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kAttnTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_attn_kernel() {
+  return cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+}
+
+domino_status_t launch_attn_fwd(const AttnLaunch& L, int num_sms, cudaStream_t stream, std::string* err) {
+  AttnParams a;
+  memset(&a, 0, sizeof a);
+  if (L.P < 1 || L.P > kMaxShards || L.dh != kTile || L.S % kTile != 0) {
+    if (err) *err = "launch_attn_fwd: unsupported shape";
+    return DOMINO_ERR_UNSUPPORTED;
+  }
+  const int64_t qkv_cols = 3 * static_cast<int64_t>(L.Hp) * L.dh;
+  for (int p = 0; p < L.P; ++p) {
+    const Operand2D op{L.qkv[p], L.M, qkv_cols, qkv_cols};
+    if (!encode_bf16_sw128(&a.map_qk[p], op, kTile, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&a.map_v[p], op, 64, err)) return DOMINO_ERR_CUDA;
+    a.o[p] = L.o[p];
+  }
+  a.ldo = static_cast<int64_t>(L.Hp) * L.dh;
+  a.row0 = L.row0;
+  a.S = static_cast<int32_t>(L.S);
+  a.Hp = L.Hp;
+  a.seqs = L.seqs;
+  a.P = L.P;
+  a.nq = static_cast<int32_t>(L.S / kTile);
+  a.num_items = a.P * a.seqs * a.Hp * a.nq;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(L.dh)));
+  a.status = L.status;
+  a.timeout_ns = L.timeout_ns;
+  if (a.num_items == 0) return DOMINO_OK;
+  const int grid = a.num_items < num_sms ? a.num_items : num_sms;
+  void* args[] = {&a};
+  const cudaError_t st = cudaLaunchKernel(reinterpret_cast<const void*>(&attn_fwd_kernel), dim3(grid), dim3(kAttnThreads), args,
+                        kAttnSmemBytes, stream);
+  if (st != cudaSuccess) {
+    if (err) *err = std::string("attention launch: ") + cudaGetErrorString(st);
+    return DOMINO_ERR_CUDA;
+  }
+  return DOMINO_OK;
+}
+
+}  // namespace domino

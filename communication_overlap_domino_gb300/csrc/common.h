@@ -30,6 +30,8 @@ enum : uint32_t {
   kSiteFusedH = 6,  // fused kernel: GEMM2 producer waiting for H row block
   kSiteFusedZ = 7,  // fused kernel: reducer waiting for the P partials of a tile
   kSiteSelfTest = 8,  // domino_selftest_wait_timeout
+  kSiteAttnP = 9,     // attention: MMA waiting for the softmax's P tile
+  kSiteAttnPV = 10,   // attention: softmax waiting for P V
 };
 
 // Epilogue of the tcgen05 GEMM: what is done with each fp32 accumulator tile.

@@ -126,3 +126,64 @@ def generate(w: Workload, seed: int = 0, with_dy: Optional[bool] = None) -> Dict
 def to_float64(tensors: Dict[str, torch.Tensor]):
     """Exact widening of bf16 tensors to numpy float64 arrays (for the oracle)."""
     return {k: v.to(torch.float64).numpy() for k, v in tensors.items()}
+
+
+# ----------------------------------------------------------- attention block
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """One sliced attention problem: B sequences of S tokens, H heads of width dh."""
+
+    name: str
+    B: int          # sequences
+    S: int          # tokens per sequence
+    d: int          # model width
+    H: int          # heads
+    P: int          # simulated tensor-parallel shards (by heads)
+    mu: int         # chunks of whole sequences
+    partial: str    # "f32" | "bf16"
+    dh: int = 128
+    description: str = ""
+
+    @property
+    def M(self) -> int:
+        return self.B * self.S
+
+    def flops(self) -> int:
+        """Algorithmic flops of one forward pass: the two projections and the causal attention core
+        (Q K^T and P V over the S (S + 1) / 2 visible query-key pairs of each sequence and head)."""
+        proj = 2 * self.M * self.d * 3 * self.H * self.dh + 2 * self.M * self.H * self.dh * self.d
+        core = 2 * 2 * self.B * self.H * self.dh * (self.S * (self.S + 1) // 2)
+        return proj + core
+
+    def with_(self, **kw) -> "AttnWorkload":
+        return replace(self, **kw)
+
+
+ATTN_WORKLOADS: Dict[str, AttnWorkload] = {
+    w.name: w
+    for w in (
+        AttnWorkload("tiny_attn_fwd", B=2, S=128, d=256, H=2, P=2, mu=2, partial="f32",
+                     description="Tiny causal attention block: 2 sequences of 128 tokens, d=256, 2 heads; P=2, mu=2"),
+        AttnWorkload("gpt_attn_fwd", B=4, S=1024, d=2560, H=20, P=4, mu=2, partial="f32",
+                     description="Attention half of the GPT-style layer: 4 x 1024 tokens, d=2560, 20 heads of 128; "
+                                 "P=4, mu=2"),
+        AttnWorkload("llama_attn_fwd", B=4, S=2048, d=4096, H=32, P=8, mu=4, partial="bf16",
+                     description="Attention half of the Llama-style layer: 4 x 2048 tokens, d=4096, 32 heads of 128; "
+                                 "P=8, mu=4"),
+    )
+}
+
+
+def generate_attn(w: AttnWorkload, seed: int = 0) -> Dict[str, torch.Tensor]:
+    """Seeded bf16 CPU tensors in mathematical layout: ``X`` [B S, d] ~N(0, 1);
+    ``Wqkv`` [d, 3 H dh] (all query heads, then key heads, then value heads) and
+    ``Wo`` [H dh, d], ~N(0, 1/fan_in) so that projected entries have unit variance
+    (for d = 2560 that is the 0.02 of the MLP weights).  Tensor t (X, Wqkv, Wo) is
+    drawn with seed + t like ``generate``."""
+    return {
+        "X": _randn((w.M, w.d), seed, 1.0),
+        "Wqkv": _randn((w.d, 3 * w.H * w.dh), seed + 1, w.d ** -0.5),
+        "Wo": _randn((w.H * w.dh, w.d), seed + 2, (w.H * w.dh) ** -0.5),
+    }
+

@@ -254,7 +254,8 @@ typedef enum domino_kernel_kind {
   DOMINO_KERNEL_BWD_DH = 3,    /* backward: dH and the activation derivative           */
   DOMINO_KERNEL_BWD_DX = 4,    /* backward: partial input gradients                    */
   DOMINO_KERNEL_BWD_DW = 5,    /* backward: weight gradients                           */
-  DOMINO_KERNEL_FUSED = 6      /* the fused forward kernel (whole call)                */
+  DOMINO_KERNEL_FUSED = 6,     /* the fused forward kernel (whole call)                */
+  DOMINO_KERNEL_ATTN = 7       /* attention core of the attention block                */
 } domino_kernel_kind_t;
 
 typedef struct domino_kernel_time {
@@ -274,6 +275,56 @@ DOMINO_API int32_t domino_kernel_times(domino_kernel_time_t* out, int32_t max_re
 
 /* Empties the log (the pooled events are kept for reuse). */
 DOMINO_API void domino_kernel_times_reset(void);
+
+/* The sliced tensor-parallel attention block, the other half of the layer
+ * (Domino page, Abstract: the whole layer is sliced into independent pieces;
+ * Megatron-LM's split, titles under "Builds on" on that page):
+ *   Q | K | V = X Wqkv                              column-parallel, by heads
+ *   O_h = softmax(Q_h K_h^T / sqrt(dh) + causal mask) V_h    per sequence, head
+ *   Y = [O_0 | ... | O_{H-1}] Wo                    row-parallel, by heads
+ * X holds B sequences of S tokens ([B S, d] bf16, sequence b = rows b S ..
+ * (b+1) S - 1); token t attends to tokens 0..t of its own sequence.  The H heads
+ * are split into P shards of Hp = H / P heads (shard p: heads p Hp .. (p+1) Hp -
+ * 1), the sequences into mu chunks of B / mu whole sequences.  Per chunk k: the
+ * projection of every shard (one grouped GEMM launch), the attention core of
+ * every (shard, sequence, head, 128-query tile) (one launch, flash-style on the
+ * tensor cores: scores and P V in tensor memory, online softmax, no score matrix
+ * in global memory), the output projection of every shard into its partial
+ * buffer (one launch), and the shard-sum of the chunk -- on the library's
+ * reduction stream with DOMINO_SCHEDULE_STREAMS, so it overlaps chunk k+1.
+ * Weights, nn.Linear layout, per shard:
+ *   Wqkv_shards[p]  [3 Hp dh, d]: shard p's query heads' rows, then its key
+ *                   heads', then its value heads' (head h: rows h dh .. (h+1) dh)
+ *   Wo_shards[p]    Wo_p^T [d, Hp dh]
+ * Supported: dh = 128, S a multiple of 128, P | H, mu | B, d % 8 == 0;
+ * DOMINO_SCHEDULE_SERIAL or STREAMS.  Other shapes: DOMINO_ERR_UNSUPPORTED
+ * (ALIGNMENT for d).  Softmax in fp32; Q, K, V, P and O rounded to bf16. */
+typedef struct domino_attn_desc {
+  int64_t B;              /* sequences, >= 0                                     */
+  int64_t S;              /* tokens per sequence, multiple of 128                */
+  int64_t d;              /* model width, multiple of 8                          */
+  int32_t H;              /* heads, P | H                                        */
+  int32_t dh;             /* head width: 128                                     */
+  int32_t P;              /* shards, 1..DOMINO_MAX_SHARDS                        */
+  int32_t mu;             /* chunks of whole sequences, mu | B, <= DOMINO_MAX_PIECES */
+  int32_t partial_dtype;  /* domino_partial_dtype_t                              */
+  int32_t schedule;       /* DOMINO_SCHEDULE_SERIAL or DOMINO_SCHEDULE_STREAMS   */
+  uint32_t flags;         /* DOMINO_FLAG_KERNEL_TIMES, DOMINO_FLAG_ONE_CTA       */
+  uint32_t reserved;      /* must be 0                                           */
+  uint64_t timeout_ns;    /* bound on each device-side wait; 0 = 2 seconds       */
+} domino_attn_desc_t;
+
+/* Workspace bytes of domino_attn_fwd (0 for an invalid descriptor): a 256-byte
+ * header (device status), Q|K|V per shard [P][B S][3 Hp dh] bf16, the attention
+ * output per shard [P][B S][Hp dh] bf16, the partials [P][B S][d]. */
+DOMINO_API size_t domino_attn_workspace_size(const domino_attn_desc_t* desc);
+
+/* Forward pass: X [B S, d] -> Y [B S, d] bf16.  B == 0 returns DOMINO_OK having
+ * touched nothing.  Kernel kinds in the timing log: GEMM1 (projection), ATTN
+ * (attention core), GEMM2 (output projection), SHARD_SUM. */
+DOMINO_API domino_status_t domino_attn_fwd(const domino_attn_desc_t* desc, const void* X,
+                                           const void* const* Wqkv_shards, const void* const* Wo_shards, void* Y,
+                                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* Strand interleaving: the forward of one micro-batch (strand a) and the
  * backward of another (strand b) of the same layer in one call, their launches

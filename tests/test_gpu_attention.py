@@ -1,0 +1,92 @@
+"""The sliced tensor-parallel attention block (domino_attn_fwd) against the fp64
+attention oracle, through the C ABI on the GB300.
+
+Bar: max|Y - Y_ref| / max|Y_ref| <= 1e-2 (the block's own tolerance; Q, K, V, the
+probabilities P and the attention output are rounded to bf16 on the GPU).  Small
+problems are compared in full: one and several 128-query tiles per sequence
+(the diagonal block and the blocks below it), one and several heads per shard,
+one and several chunks, both partial precisions and both separate-launch
+schedules.  At full size the oracle computes sampled sequences exactly (the
+sequences are independent).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as att
+from oracle import max_rel_err
+from communication_overlap_domino_gb300 import binding as b
+from communication_overlap_domino_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _run(w, t, schedule="streams", ws=None):
+    dev = torch.device("cuda:0")
+    qkv_sh, o_sh = b.shard_attn_weights(t["Wqkv"].to(dev), t["Wo"].to(dev), w.H, w.P)
+    return b.attn_fwd(t["X"].to(dev), qkv_sh, o_sh, S=w.S, H=w.H, mu=w.mu, partial=w.partial, schedule=schedule,
+                      workspace=ws)
+
+
+def _f64(t):
+    return {k: v.to(torch.float64).numpy() for k, v in t.items()}
+
+
+@pytest.mark.parametrize("schedule", ["streams", "serial"])
+@pytest.mark.parametrize("w", [
+    wl.ATTN_WORKLOADS["tiny_attn_fwd"],
+    wl.AttnWorkload("attn_4tiles", B=2, S=512, d=512, H=4, P=2, mu=2, partial="bf16"),
+    wl.AttnWorkload("attn_one_shard", B=1, S=1024, d=256, H=1, P=1, mu=1, partial="f32"),
+    wl.AttnWorkload("attn_3shards", B=3, S=256, d=384, H=6, P=3, mu=3, partial="f32"),
+], ids=lambda w: w.name if hasattr(w, "name") else w)
+def test_attention_block_matches_oracle(w, schedule):
+    t = wl.generate_attn(w, seed=5)
+    Y = _run(w, t, schedule)
+    torch.cuda.synchronize()
+    f = _f64(t)
+    ref = att.attn_fwd(f["X"], f["Wqkv"], f["Wo"], w.S, w.H)
+    err = max_rel_err(Y.double().cpu().numpy(), ref)
+    assert err <= TOL, f"{w.name}/{schedule}: {err:.3e}"
+
+
+def test_attention_deterministic_and_schedule_independent():
+    w = wl.AttnWorkload("attn_det", B=2, S=384, d=256, H=2, P=2, mu=2, partial="f32")
+    t = wl.generate_attn(w, seed=6)
+    a = _run(w, t, "streams")
+    b2 = _run(w, t, "serial")
+    c = _run(w.with_(mu=1), t, "streams")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b2) and torch.equal(a, c)
+
+
+def test_attention_device_status_and_empty_batch():
+    w = wl.ATTN_WORKLOADS["tiny_attn_fwd"]
+    t = wl.generate_attn(w, seed=7)
+    desc = b.make_attn_desc(w.B, w.S, w.d, w.H, w.P, w.mu, w.partial)
+    ws = torch.zeros(b.attn_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    _run(w, t, "streams", ws=ws)
+    assert b.query_device_status(ws) == 0
+    empty = b.make_attn_desc(0, w.S, w.d, w.H, w.P, 1, w.partial)
+    assert b.lib().domino_attn_fwd(empty, None, None, None, None, None, 0, None) == 0
+
+
+def test_gpt_attention_full_size_sampled():
+    w = wl.ATTN_WORKLOADS["gpt_attn_fwd"]
+    t = wl.generate_attn(w, seed=0)
+    Y = _run(w, t).double().cpu().numpy()
+    f = _f64(t)
+    for seq in (0, w.B - 1):  # one sequence from each chunk
+        rows = slice(seq * w.S, (seq + 1) * w.S)
+        ref = att.attn_fwd(f["X"][rows], f["Wqkv"], f["Wo"], w.S, w.H)
+        err = max_rel_err(Y[rows], ref)
+        assert err <= TOL, f"sequence {seq}: {err:.3e}"
+    assert np.isfinite(Y).all()
