@@ -512,7 +512,178 @@ def run_ours(args, w, rank, world, local_rank):
     return line
 
 
+# --------------------------------------------------------- attention block
+
+def run_attn(args, w, rank, world, local_rank):
+    """The sliced tensor-parallel attention block (domino_attn_fwd): projection,
+    flash-style attention core, output projection, shard-sum, per chunk."""
+    import torch
+
+    from communication_overlap_domino_gb300 import binding as b
+    from communication_overlap_domino_gb300 import workloads as wl
+    import oracle.attention as att
+
+    schedule = args.schedule if args.schedule != "fused" else "streams"
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    t = wl.generate_attn(w, seed=0)
+    qkv_sh, o_sh = b.shard_attn_weights(t["Wqkv"].to(dev), t["Wo"].to(dev), w.H, w.P)
+    X = t["X"].to(dev)
+    Y = torch.empty((w.M, w.d), dtype=torch.bfloat16, device=dev)
+    desc = b.make_attn_desc(w.B, w.S, w.d, w.H, w.P, w.mu, w.partial, schedule)
+    ws = torch.zeros(b.attn_workspace_size(desc), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(timed=False, x=X, y=Y):
+        b.attn_fwd(x, qkv_sh, o_sh, S=w.S, H=w.H, mu=w.mu, partial=w.partial, schedule=schedule, Y=y,
+                   workspace=ws, kernel_times=timed)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if b.query_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    b.kernel_times_reset()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(timed=True)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if b.query_device_status(ws) != 0:
+        raise RuntimeError("device status after the timed region")
+    mean_ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in ev), world, dev)
+    records = b.kernel_times()
+
+    # end to end: X from pinned host memory in, Y out, every step
+    Xh = t["X"].pin_memory()
+    Yh = torch.empty((w.M, w.d), dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(X)
+    e2e_steps = max(3, min(args.steps, 50))
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        ev2[i][0].record(stream)
+        Xd.copy_(Xh, non_blocking=True)
+        step(x=Xd)
+        Yh.copy_(Y, non_blocking=True)
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in ev2), world, dev)
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    Mc = w.M // w.mu
+    core_flops_chunk = 2 * 2 * (w.B // w.mu) * w.H * w.dh * (w.S * (w.S + 1) // 2)
+    launch_flops = {"gemm1": 2.0 * Mc * w.d * 3 * w.H * w.dh, "attn": float(core_flops_chunk),
+                    "gemm2": 2.0 * Mc * w.H * w.dh * w.d}
+    kinds = {}
+    for r in records:
+        k = kinds.setdefault(r["kind"], {"launches": 0, "total_ms": 0.0, "flops": 0.0})
+        k["launches"] += 1
+        k["total_ms"] += r["end_ms"] - r["start_ms"]
+        k["flops"] += launch_flops.get(r["kind"], 0.0)
+    for k in kinds.values():
+        k["avg_us"] = 1e3 * k["total_ms"] / k["launches"]
+    a_tf = kinds["attn"]["flops"] / (kinds["attn"]["total_ms"] * 1e-3) / 1e12
+    span_ms, exposed_ms = timeline_stats(records)
+    value = whole_job_tflops(w.flops(), world, mean_ms)
+    line = {
+        "metric": "sliced TP attention block TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) activations, N(0,1/fan_in) weights, bf16",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "d": w.d, "H": w.H, "dh": w.dh, "P": w.P, "mu": w.mu,
+                   "partials": w.partial, "schedule": schedule, "causal": True,
+                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+        "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
+        "exposed_reduce_us_per_layer": round(1e3 * exposed_ms, 2),
+        "exposed_reduce_frac": round(exposed_ms / span_ms, 4) if span_ms > 0 else None,
+        "roofline": {
+            "kernel": "attn_fwd_kernel (causal attention core)",
+            "note": "achieved = causal attention flops (Q K^T and P V over the visible query-key pairs) of the "
+                    "kernel's launches / their summed event durations",
+            "bound": "tensor", "achieved": round(a_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": round(a_tf / peak_tf, 4), "peak_source": f"{peak_src} bf16_tflops_sustained",
+            "flops_per_launch": float(core_flops_chunk), "traffic": None,
+        },
+        "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
+                        "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["flops"] else None,
+                        "share": round(v["total_ms"] / sum(x["total_ms"] for x in kinds.values()), 4)}
+                    for k, v in kinds.items()},
+        "gpu_launches": len(records),
+        "e2e": {"value": round(whole_job_tflops(w.flops(), world, e2e_ms), 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": w.M * w.d * 2, "d2h_bytes_per_step": w.M * w.d * 2,
+                "ms_per_step": round(e2e_ms, 4),
+                "mode": "upload, compute, download in order on one stream each step (L2 flush outside the events)"},
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        # one sequence at a time (sequences are independent; flops scale with sequences)
+        f = {k: v.double().numpy() for k, v in t.items()}
+        t0, n = time.perf_counter(), 0
+        while n < w.B and (n == 0 or time.perf_counter() - t0 < args.cpu_seconds):
+            rows = slice(n * w.S, (n + 1) * w.S)
+            att.attn_fwd(f["X"][rows], f["Wqkv"], f["Wo"], w.S, w.H)
+            n += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(w.flops() * n / w.B / dt / 1e12, 5), "unit": "TFLOP/s",
+                                "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"fp64 attention oracle on {n} of {w.B} sequences ({dt:.1f} s)"}
+    return line
+
+
 # ---------------------------------------------------------- reference arm
+
+def run_reference_attn(args, w):
+    """The fp64 attention oracle as it stands on the host cores: one sequence per step."""
+    from communication_overlap_domino_gb300 import workloads as wl
+    import oracle.attention as att
+    t = wl.generate_attn(w, seed=0)
+    f = {k: v.double().numpy() for k, v in t.items()}
+    X = f["X"][:w.S]
+    for _ in range(args.warmup):
+        att.attn_fwd(X, f["Wqkv"], f["Wo"], w.S, w.H)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        att.attn_fwd(X, f["Wqkv"], f["Wo"], w.S, w.H)
+        times.append(time.perf_counter() - t0)
+    mean_s = statistics.mean(times)
+    value = w.flops() / w.B / mean_s / 1e12
+    return {
+        "impl": "reference",
+        "metric": "sliced TP attention block TFLOP/s at 1 GB300 (% BF16 peak); exposed shard-reduce time/layer",
+        "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * mean_s, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic: seeded bf16 values widened to fp64",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "d": w.d, "H": w.H, "dh": w.dh, "P": w.P, "mu": w.mu,
+                   "sequences_per_step": 1},
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"fp64 attention oracle on 1 of {w.B} sequences per step"},
+        "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
 
 def run_reference(args, w):
     """The fp64 CPU oracle as it stands, on the host cores: each step runs the
@@ -576,9 +747,11 @@ def main():
         ap.error("--warmup must be >= 3")
 
     from communication_overlap_domino_gb300 import workloads as wl
-    w = wl.WORKLOADS[args.workload or wl.BENCH_WORKLOAD]
+    name = args.workload or wl.BENCH_WORKLOAD
+    w = wl.ATTN_WORKLOADS[name] if name in wl.ATTN_WORKLOADS else wl.WORKLOADS[name]
     if args.mu is not None:
         w = w.with_(mu=args.mu)
+    attention = name in wl.ATTN_WORKLOADS
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -586,7 +759,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, w)), flush=True)
+            print(json.dumps((run_reference_attn if attention else run_reference)(args, w)), flush=True)
         return
 
     import __graft_entry__
@@ -605,7 +778,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        line = run_ours(args, w, rank, world, local_rank)
+        line = (run_attn if attention else run_ours)(args, w, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

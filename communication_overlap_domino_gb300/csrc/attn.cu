@@ -9,25 +9,31 @@
 // score matrix ever reaches global memory.
 //
 // Persistent kernel, one CTA per SM, 10 warps:
-//   warp 0      TMA producer: the Q tile once per item, then K_j and V_j of
-//               every key block into a 2-stage ring.
+//   warp 0      TMA producer: the Q tile once per item, then the key blocks K_j
+//               and value blocks V_j into two 2-slot rings, K one block ahead
+//               of V (K_{j+1} is needed for the next scores before V_j is
+//               needed for P_j V_j).
 //   warp 1      tensor-memory allocation; lane 0 issues the MMAs:
 //               S_j = Q K_j^T (M 128, N 128, K 128) into one of two TMEM score
-//               buffers, and PV_j = P_j V_j into the TMEM PV buffer.  S_{j+1} is
-//               issued before PV_j, so the next scores are computed while the
-//               softmax of block j runs.
+//               buffers, and O += P_j V_j into the TMEM output accumulator.
+//               S_{j+1} is issued before P_j V_j, so the next scores are
+//               computed while the softmax of block j runs.
 //   warps 2-9   two threads per query row (warps w and w + 4 read the same
 //               tensor-memory lanes), each owning 64 of the row's 128 key and
-//               output columns: both take the row maximum over all 128 scores,
-//               each writes its 64 probabilities p = exp2(s * c - m) as bf16 into
-//               shared memory in the MMA's operand layout and keeps its 64
-//               running outputs O = O * alpha + PV_j and its part of the row sum;
-//               after the last block the two parts of the sum are added through
-//               shared memory and O / l is stored as bf16.
+//               output columns.  Both take the row maximum over all 128 scores,
+//               so they agree on it.  Lazy rescaling: the running maximum m only
+//               moves when a block's maximum exceeds it by more than 2^8 (in the
+//               exp2 domain); then the thread rescales its half of the output
+//               row in tensor memory (after P_{j-1} V_{j-1} has landed) and its
+//               part of the row sum.  Each writes its 64 probabilities
+//               p = exp2(s * c - m) as bf16 into shared memory in the MMA's
+//               operand layout (once P_{j-1} V_{j-1} has finished reading the
+//               buffer).  After the last block the two parts of the row sum are
+//               added through shared memory and O / l is stored as bf16.
 //
-// Barriers (all waits bounded, as in the GEMMs): q_full / q_empty, kv_full[s] /
-// kv_empty[s], s_full[b] / s_empty[b] (256 arrivals), p_full (256), pv_full,
-// pv_empty (256), l_ready[2] (256), final.
+// Barriers (all waits bounded, as in the GEMMs): q_full / q_empty, k_full[s] /
+// k_empty[s], v_full[s] / v_empty[s], s_full[b] / s_empty[b] (256 arrivals),
+// p_full (256), pv_full, o_empty (256), l_ready[2] (256), final.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -50,13 +56,13 @@ constexpr int kQBytes = 2 * kSub;                 // Q tile: dh halves 0-63 and 
 constexpr int kPBytes = 2 * kSub;                 // P tile: key halves 0-63 and 64-127
 constexpr int kKBytes = 2 * kSub;                 // K tile: dh halves
 constexpr int kVBytes = 2 * kSub;                 // V tile: 2 blocks of 64 keys x (2 boxes of 64 dh x 64 keys)
-constexpr int kStageBytes = kKBytes + kVBytes;    // 64 KB
-constexpr int kStages = 2;
-constexpr int kLsumBytes = 2 * 2 * kTile * 4;        // row-sum halves, double-buffered by item
-constexpr int kAttnSmemBytes = kQBytes + kPBytes + kStages * kStageBytes + kLsumBytes + 1024 + 256;
+constexpr int kSlots = 2;                         // slots of the K ring and of the V ring
+constexpr int kLsumBytes = 2 * 2 * kTile * 4;     // row-sum halves, double-buffered by item
+constexpr int kAttnSmemBytes = kQBytes + kPBytes + kSlots * (kKBytes + kVBytes) + kLsumBytes + 1024 + 256;
 static_assert(kAttnSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kAttnTmemCols = 512;           // S buffers at 0 and 128, PV at 256
-constexpr uint32_t kPvCol = 256;
+constexpr uint32_t kAttnTmemCols = 512;           // S buffers at 0 and 128, the output O at 256
+constexpr uint32_t kOCol = 256;
+constexpr float kRescaleLog2 = 8.0f;              // lazy rescaling threshold: the maximum may lag by 2^8
 
 struct AttnItem {
   int p, b, h, i;  // shard, sequence of the chunk, head of the shard, query tile
@@ -76,18 +82,20 @@ __device__ __forceinline__ AttnItem attn_item(const AttnParams& a, int t) {
   return it;
 }
 
-// Issues S = Q K^T for the key block in ring stage kv_idx % 2 into score
-// buffer s_idx % 2, once the block has landed and the buffer is free.
-__device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_base, uint32_t qa, uint8_t* skv,
-                                             uint64_t* kv_full, uint64_t* s_empty, uint64_t* s_full,
-                                             uint32_t kv_idx, uint32_t s_idx, volatile int* abort_flag, int t) {
+// Issues S = Q K^T for the key block in K-ring slot k_idx % 2 into score
+// buffer s_idx % 2, once the block has landed and the buffer is free; the slot
+// is released when the MMAs have read it.
+__device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_base, uint32_t qa, uint8_t* sk,
+                                             uint64_t* k_full, uint64_t* k_empty, uint64_t* s_empty,
+                                             uint64_t* s_full, uint32_t k_idx, uint32_t s_idx,
+                                             volatile int* abort_flag, int t) {
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-  const uint32_t st = kv_idx & 1, sb = s_idx & 1;
-  if (!mbar_wait(&kv_full[st], (kv_idx >> 1) & 1, abort_flag, a.timeout_ns, a.status, kSiteMmaFull, t)) return false;
+  const uint32_t st = k_idx & 1, sb = s_idx & 1;
+  if (!mbar_wait(&k_full[st], (k_idx >> 1) & 1, abort_flag, a.timeout_ns, a.status, kSiteMmaFull, t)) return false;
   if (!mbar_wait(&s_empty[sb], ((s_idx >> 1) & 1) ^ 1, abort_flag, a.timeout_ns, a.status, kSiteMmaTmemEmpty, t))
     return false;
   tc_fence_after_sync();
-  const uint32_t ka = smem_u32(skv + st * kStageBytes);
+  const uint32_t ka = smem_u32(sk + st * kKBytes);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint64_t ad = smem_desc_k128(qa + (k >> 2) * kSub) + 2 * (k & 3);
@@ -95,6 +103,7 @@ __device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_
     mma_bf16_ss(tmem_base + sb * kTile, ad, bd, idesc_s, k != 0 ? 1u : 0u);
   }
   mma_commit(&s_full[sb]);
+  mma_commit(&k_empty[st]);
   return true;
 }
 
@@ -108,21 +117,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem;
   uint8_t* sp = sq + kQBytes;
-  uint8_t* skv = sp + kPBytes;
-  float* lsum = reinterpret_cast<float*>(skv + kStages * kStageBytes);  // [2 buffers][2 halves][128 rows]
+  uint8_t* sk = sp + kPBytes;             // K ring: kSlots x 32 KB
+  uint8_t* sv = sk + kSlots * kKBytes;    // V ring: kSlots x 32 KB
+  float* lsum = reinterpret_cast<float*>(sv + kSlots * kVBytes);  // [2 buffers][2 halves][128 rows]
   uint64_t* bars = reinterpret_cast<uint64_t*>(lsum + 2 * 2 * kTile);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;   // [2]
-  uint64_t* kv_empty = bars + 4;  // [2]
-  uint64_t* s_full = bars + 6;    // [2]
-  uint64_t* s_empty = bars + 8;   // [2]
-  uint64_t* p_full = bars + 10;
-  uint64_t* pv_full = bars + 11;
-  uint64_t* pv_empty = bars + 12;
-  uint64_t* final_bar = bars + 13;
-  uint64_t* l_ready = bars + 14;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars + 2;    // [2]
+  uint64_t* k_empty = bars + 4;   // [2]
+  uint64_t* v_full = bars + 6;    // [2]
+  uint64_t* v_empty = bars + 8;   // [2]
+  uint64_t* s_full = bars + 10;   // [2]
+  uint64_t* s_empty = bars + 12;  // [2]
+  uint64_t* p_full = bars + 14;
+  uint64_t* pv_full = bars + 15;
+  uint64_t* o_empty = bars + 16;
+  uint64_t* final_bar = bars + 17;
+  uint64_t* l_ready = bars + 18;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -130,16 +142,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], kSoftmaxThreads);
       mbar_init(&l_ready[s], kSoftmaxThreads);
     }
     mbar_init(p_full, kSoftmaxThreads);
     mbar_init(pv_full, 1);
-    mbar_init(pv_empty, kSoftmaxThreads);
+    mbar_init(o_empty, kSoftmaxThreads);
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -156,9 +170,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t q_phase = 0, kv_count = 0;
-    uint32_t issued_q = 0, issued_kv_mask = 0, kv_parity = 0;
+    uint32_t q_phase = 0, k_count = 0, v_count = 0;
+    uint32_t issued_q = 0, issued_k = 0, issued_v = 0, k_parity = 0, v_parity = 0;
     bool ok = true;
+    // one K or V block into its ring slot (waits until the slot's previous block has been read)
+    auto load_block = [&](bool is_k, uint32_t idx, const CUtensorMap* mqk, const CUtensorMap* mv, int col, int y,
+                          int t) -> bool {
+      const uint32_t st = idx & 1, ph = (idx >> 1) & 1;
+      uint64_t* full = is_k ? &k_full[st] : &v_full[st];
+      if (!mbar_wait(is_k ? &k_empty[st] : &v_empty[st], ph ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t))
+        return false;
+      if (is_k) {
+        uint8_t* dst = sk + st * kKBytes;
+        mbar_arrive_expect_tx(full, kKBytes);
+        tma_load_2d(dst, mqk, full, col, y);
+        tma_load_2d(dst + kSub, mqk, full, col + 64, y);
+        issued_k |= 1u << st;
+        k_parity = (k_parity & ~(1u << st)) | (ph << st);
+      } else {
+        // V as the MN-major B operand: per 64-key block, two boxes of 64 dh x 64 keys
+        uint8_t* dst = sv + st * kVBytes;
+        mbar_arrive_expect_tx(full, kVBytes);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_2d(dst + kb * kSub, mv, full, col, y + kb * 64);
+          tma_load_2d(dst + kb * kSub + 8192, mv, full, col + 64, y + kb * 64);
+        }
+        issued_v |= 1u << st;
+        v_parity = (v_parity & ~(1u << st)) | (ph << st);
+      }
+      return true;
+    };
     for (int t = blockIdx.x; t < a.num_items && ok && !*abort_flag; t += gridDim.x) {
       const AttnItem it = attn_item(a, t);
       const CUtensorMap* mqk = &a.map_qk[it.p];
@@ -172,77 +213,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       tma_load_2d(sq, mqk, q_full, qx, qy);
       tma_load_2d(sq + kSub, mqk, q_full, qx + 64, qy);
       issued_q = 1;
-      for (int j = 0; j <= it.i; ++j, ++kv_count) {
-        const uint32_t st = kv_count & 1;
-        const uint32_t ph = (kv_count >> 1) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t)) {
-          ok = false;
-          break;
-        }
-        uint8_t* sk = skv + st * kStageBytes;
-        uint8_t* sv = sk + kKBytes;
-        mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
-        const int ky = seq_row0 + j * kTile;
-        const int kx = (a.Hp + it.h) * kTile;
-        const int vx = (2 * a.Hp + it.h) * kTile;
-        tma_load_2d(sk, mqk, &kv_full[st], kx, ky);
-        tma_load_2d(sk + kSub, mqk, &kv_full[st], kx + 64, ky);
-        // V as the MN-major B operand: per 64-key block, two boxes of 64 dh x 64 keys
-        for (int kb = 0; kb < 2; ++kb) {
-          tma_load_2d(sv + kb * kSub, mv, &kv_full[st], vx, ky + kb * 64);
-          tma_load_2d(sv + kb * kSub + 8192, mv, &kv_full[st], vx + 64, ky + kb * 64);
-        }
-        issued_kv_mask |= 1u << st;
-        kv_parity = (kv_parity & ~(1u << st)) | (ph << st);
+      const int kx = (a.Hp + it.h) * kTile;
+      const int vx = (2 * a.Hp + it.h) * kTile;
+      // K runs one block ahead of V: K_0, K_1, V_0, K_2, V_1, ..., V_i
+      for (int j = 0; j <= it.i + 1 && ok; ++j) {
+        if (j <= it.i) ok = load_block(true, k_count++, mqk, mv, kx, seq_row0 + j * kTile, t);
+        if (ok && j >= 1) ok = load_block(false, v_count++, mqk, mv, vx, seq_row0 + (j - 1) * kTile, t);
       }
     }
     // drain: every load issued has landed before the CTA can exit
     volatile int no_abort = 0;
     if (issued_q) mbar_wait(q_full, (q_phase ^ 1) & 1, &no_abort, tmo, a.status, kSiteDrain, 0);
-    for (int s = 0; s < kStages; ++s)
-      if (issued_kv_mask & (1u << s))
-        mbar_wait(&kv_full[s], (kv_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 1 + s);
+    for (int s = 0; s < 2; ++s) {
+      if (issued_k & (1u << s)) mbar_wait(&k_full[s], (k_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 1 + s);
+      if (issued_v & (1u << s)) mbar_wait(&v_full[s], (v_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 3 + s);
+    }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
-    uint32_t q_phase = 0, kv_count = 0, s_count = 0, p_phase = 0, pv_phase = 0;
+    uint32_t q_phase = 0, kv_count = 0, s_count = 0, p_phase = 0, o_phase = 0;
     const uint32_t qa = smem_u32(sq), pa = smem_u32(sp);
     bool ok = true;
     for (int t = blockIdx.x; t < a.num_items && ok && !*abort_flag; t += gridDim.x) {
       const AttnItem it = attn_item(a, t);
       if (!mbar_wait(q_full, q_phase, abort_flag, tmo, a.status, kSiteMmaFull, t)) break;
       q_phase ^= 1;
-      const uint32_t kv0 = kv_count;
-      if (!attn_issue_s(a, tmem_base, qa, skv, kv_full, s_empty, s_full, kv_count, s_count, abort_flag, t)) break;
+      const uint32_t kv0 = kv_count;  // K and V blocks are counted alike
+      if (!attn_issue_s(a, tmem_base, qa, sk, k_full, k_empty, s_empty, s_full, kv_count, s_count, abort_flag, t))
+        break;
+      if (it.i == 0) mma_commit(q_empty);  // Q is read by the score MMAs only: free after the item's last one
+      // the output accumulator is free once the previous item's output has been read
+      if (!mbar_wait(o_empty, o_phase ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, t)) break;
+      o_phase ^= 1;
       for (int j = 0; j <= it.i; ++j) {
-        if (j + 1 <= it.i && !attn_issue_s(a, tmem_base, qa, skv, kv_full, s_empty, s_full, kv0 + j + 1,
-                                           s_count + j + 1, abort_flag, t)) {
-          ok = false;
-          break;
+        if (j + 1 <= it.i) {
+          if (!attn_issue_s(a, tmem_base, qa, sk, k_full, k_empty, s_empty, s_full, kv0 + j + 1, s_count + j + 1,
+                            abort_flag, t)) {
+            ok = false;
+            break;
+          }
+          if (j + 1 == it.i) mma_commit(q_empty);
         }
+        const uint32_t vi = kv0 + j, st = vi & 1;
         if (!mbar_wait(p_full, p_phase, abort_flag, tmo, a.status, kSiteAttnP, t) ||
-            !mbar_wait(pv_empty, pv_phase ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, t)) {
+            !mbar_wait(&v_full[st], (vi >> 1) & 1, abort_flag, tmo, a.status, kSiteMmaFull, t)) {
           ok = false;
           break;
         }
         p_phase ^= 1;
-        pv_phase ^= 1;
         tc_fence_after_sync();
-        const uint32_t st = (kv0 + j) & 1;
-        const uint32_t va = smem_u32(skv + st * kStageBytes + kKBytes);
+        const uint32_t va = smem_u32(sv + st * kVBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t ad = smem_desc_k128(pa + (k >> 2) * kSub) + 2 * (k & 3);
           const uint64_t bd = smem_desc_mn128(va + (k >> 2) * kSub) + (2048 >> 4) * (k & 3);
-          mma_bf16_ss(tmem_base + kPvCol, ad, bd, idesc_pv, k != 0 ? 1u : 0u);
+          mma_bf16_ss(tmem_base + kOCol, ad, bd, idesc_pv, (j | k) != 0 ? 1u : 0u);
         }
         mma_commit(pv_full);
-        mma_commit(&kv_empty[st]);
+        mma_commit(&v_empty[st]);
       }
       kv_count = kv0 + it.i + 1;
       s_count += it.i + 1;
       if (!ok) break;
-      mma_commit(q_empty);
     }
     mma_commit(final_bar);
     volatile int no_abort = 0;
@@ -253,12 +285,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     const int half = (warp - 2) >> 2;   // key / output columns half * 64 .. + 64
     const int r = quarter * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t to = tmem_base + lane_off + kOCol + half * 64;  // this thread's half of the output row
     uint32_t s_count = 0, pv_phase = 0, item_count = 0;
     for (int t = blockIdx.x; t < a.num_items && !*abort_flag; t += gridDim.x, ++item_count) {
       const AttnItem it = attn_item(a, t);
-      float o[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) o[c] = 0.0f;
       float m_run = -INFINITY, l_run = 0.0f;
       bool ok = true;
       for (int j = 0; j <= it.i; ++j, ++s_count) {
@@ -270,71 +300,103 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         tc_fence_after_sync();
         const uint32_t ts = tmem_base + lane_off + sb * kTile;
         const bool diag = j == it.i;
-        // pass 1: row maximum of the visible scores (all 128 keys)
+        // pass 1: row maximum of the visible scores (all 128 keys, 64 per wait)
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(ts + c * 32, v);
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(ts + hb * 64, v0);
+          tmem_ld_32x32b_x32(ts + hb * 64 + 32, v1);
+          tmem_ld_wait();
+          if (diag) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (hb * 64 + e <= r) mx = fmaxf(mx, __uint_as_float(v0[e]));
+              if (hb * 64 + 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v1[e]));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fmaxf(__uint_as_float(v0[e]), __uint_as_float(v1[e])));
+          }
+        }
+        const float m_blk = mx * a.scale_log2;
+        const bool rescale = m_blk > m_run + kRescaleLog2;
+        float alpha = 1.0f;
+        if (rescale) {
+          alpha = exp2f(m_run - m_blk);
+          m_run = m_blk;
+        }
+        // pass 2: this thread's 64 probabilities, packed as bf16 pairs
+        uint32_t pk[32];
+        float sum = 0.0f;
+        {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(ts + half * 64, v0);
+          tmem_ld_32x32b_x32(ts + half * 64 + 32, v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!diag || c * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v[e]));
+          for (int e = 0; e < 16; ++e) {
+            const int k0 = half * 64 + 2 * e, k1 = k0 + 32;
+            float p0 = exp2f(fmaf(__uint_as_float(v0[2 * e]), a.scale_log2, -m_run));
+            float p1 = exp2f(fmaf(__uint_as_float(v0[2 * e + 1]), a.scale_log2, -m_run));
+            float p2 = exp2f(fmaf(__uint_as_float(v1[2 * e]), a.scale_log2, -m_run));
+            float p3 = exp2f(fmaf(__uint_as_float(v1[2 * e + 1]), a.scale_log2, -m_run));
+            if (diag) {
+              p0 = k0 <= r ? p0 : 0.0f;
+              p1 = k0 + 1 <= r ? p1 : 0.0f;
+              p2 = k1 <= r ? p2 : 0.0f;
+              p3 = k1 + 1 <= r ? p3 : 0.0f;
+            }
+            sum += (p0 + p1) + (p2 + p3);
+            pk[e] = pack_bf16(p0, p1);
+            pk[16 + e] = pack_bf16(p2, p3);
+          }
         }
-        const float m_new = fmaxf(m_run, mx * a.scale_log2);
-        // pass 2: this thread's 64 probabilities, written as the bf16 A operand of P V
-        float sum = 0.0f;
+        // P_{j-1} V_{j-1} has landed: the P buffer is free and the output up to date
+        if (j > 0) {
+          if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
+            ok = false;
+            break;
+          }
+          pv_phase ^= 1;
+          tc_fence_after_sync();
+          if (rescale) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(to + cc * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tmem_st_32x32b_x32(to + cc * 32, v);
+            }
+            tmem_st_wait();
+          }
+        }
         uint8_t* row = sp + half * kSub + r * 128;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(ts + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            float pr[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int key = c * 32 + q4 * 8 + e;
-              pr[e] = (!diag || key <= r) ? exp2f(fmaf(__uint_as_float(v[q4 * 8 + e]), a.scale_log2, -m_new)) : 0.0f;
-              sum += pr[e];
-            }
-            const int chunk = cc * 4 + q4;  // 16-byte chunk of the 128-byte row
-            uint4 w;
-            w.x = pack_bf16(pr[0], pr[1]);
-            w.y = pack_bf16(pr[2], pr[3]);
-            w.z = pack_bf16(pr[4], pr[5]);
-            w.w = pack_bf16(pr[6], pr[7]);
-            *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w;
-          }
+        for (int c16 = 0; c16 < 8; ++c16) {  // 16-byte chunk c16 holds keys half*64 + 8 c16 .. + 8
+          const int e0 = (c16 & 3) * 4 + (c16 >> 2) * 16;
+          const uint4 w = make_uint4(pk[e0], pk[e0 + 1], pk[e0 + 2], pk[e0 + 3]);
+          *reinterpret_cast<uint4*>(row + ((c16 ^ (r & 7)) << 4)) = w;
         }
         fence_proxy_async_shared();  // P is read by the tensor cores (async proxy)
         tc_fence_before_sync();
         mbar_arrive(&s_empty[sb]);
         mbar_arrive(p_full);
-        const float alpha = exp2f(m_run - m_new);
         l_run = l_run * alpha + sum;
-        m_run = m_new;
-        // O = O * alpha + P_j V_j, this thread's 64 output columns
-        if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
-          ok = false;
-          break;
-        }
-        pv_phase ^= 1;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_base + lane_off + kPvCol + half * 64 + cc * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[cc * 32 + e] = fmaf(o[cc * 32 + e], alpha, __uint_as_float(v[e]));
-        }
-        tc_fence_before_sync();
-        mbar_arrive(pv_empty);
       }
       if (!ok) break;
+      // the last P V has landed: read this thread's half of the output row
+      if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) break;
+      pv_phase ^= 1;
+      tc_fence_after_sync();
+      uint32_t o0[32], o1[32];
+      tmem_ld_32x32b_x32(to, o0);
+      tmem_ld_32x32b_x32(to + 32, o1);
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(o_empty);
       // the row sum: this thread's part plus its partner's, through shared memory
       const uint32_t lb = item_count & 1;
       float* lbuf = lsum + lb * 2 * kTile;
@@ -347,13 +409,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o[it.p]) + grow * a.ldo + it.h * kTile +
                                             half * 64);
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        uint4 w;
-        w.x = pack_bf16(o[8 * q8 + 0] * inv, o[8 * q8 + 1] * inv);
-        w.y = pack_bf16(o[8 * q8 + 2] * inv, o[8 * q8 + 3] * inv);
-        w.z = pack_bf16(o[8 * q8 + 4] * inv, o[8 * q8 + 5] * inv);
-        w.w = pack_bf16(o[8 * q8 + 6] * inv, o[8 * q8 + 7] * inv);
-        dst[q8] = w;
+      for (int q8 = 0; q8 < 4; ++q8) {
+        dst[q8] = make_uint4(pack_bf16(__uint_as_float(o0[8 * q8 + 0]) * inv, __uint_as_float(o0[8 * q8 + 1]) * inv),
+                             pack_bf16(__uint_as_float(o0[8 * q8 + 2]) * inv, __uint_as_float(o0[8 * q8 + 3]) * inv),
+                             pack_bf16(__uint_as_float(o0[8 * q8 + 4]) * inv, __uint_as_float(o0[8 * q8 + 5]) * inv),
+                             pack_bf16(__uint_as_float(o0[8 * q8 + 6]) * inv, __uint_as_float(o0[8 * q8 + 7]) * inv));
+        dst[4 + q8] =
+            make_uint4(pack_bf16(__uint_as_float(o1[8 * q8 + 0]) * inv, __uint_as_float(o1[8 * q8 + 1]) * inv),
+                       pack_bf16(__uint_as_float(o1[8 * q8 + 2]) * inv, __uint_as_float(o1[8 * q8 + 3]) * inv),
+                       pack_bf16(__uint_as_float(o1[8 * q8 + 4]) * inv, __uint_as_float(o1[8 * q8 + 5]) * inv),
+                       pack_bf16(__uint_as_float(o1[8 * q8 + 6]) * inv, __uint_as_float(o1[8 * q8 + 7]) * inv));
       }
     }
   }
