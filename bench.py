@@ -42,7 +42,8 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("common.h", "epilogue.cuh", "fused.cu", "gemm.cu", "gemm.h", "gemm_pair.cu", "ptx.cuh", "shard_sum.cu")
+KERNEL_SOURCES = ("attn.cu", "attn.h", "common.h", "epilogue.cuh", "fused.cu", "gemm.cu", "gemm.h", "gemm_pair.cu", "ptx.cuh",
+                  "shard_sum.cu")
 
 
 def kernel_source_hash():
@@ -624,7 +625,7 @@ def run_attn(args, w, rank, world, local_rank):
                     "kernel's launches / their summed event durations",
             "bound": "tensor", "achieved": round(a_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
             "frac": round(a_tf / peak_tf, 4), "peak_source": f"{peak_src} bf16_tflops_sustained",
-            "flops_per_launch": float(core_flops_chunk), "traffic": None,
+            "flops_per_launch": float(core_flops_chunk), "traffic": ncu_traffic("attn", w.name),
         },
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
                         "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["flops"] else None,
