@@ -144,3 +144,37 @@ def test_interleaved_validates(lib):
     assert lib.domino_mlp_fwd_bwd_interleaved(ctypes.byref(d), *bad) == 1
     small = args[:-2] + (b.interleaved_workspace_size(d) - 1, None)
     assert lib.domino_mlp_fwd_bwd_interleaved(ctypes.byref(d), *small) == 4
+
+
+def attn_desc(**kw):
+    base = dict(B=2, S=256, d=512, H=4, P=2, mu=2, partial="f32", schedule="streams")
+    base.update(kw)
+    return b.make_attn_desc(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(P=0), 1), (dict(H=0), 1), (dict(mu=0), 1), (dict(B=-1), 1),
+    (dict(S=200), 2), (dict(dh=64), 2), (dict(H=3), 2), (dict(mu=3), 2), (dict(schedule="fused"), 2),
+    (dict(d=516), 3),
+])
+def test_attention_descriptor_validation(lib, kw, status):
+    d = attn_desc(**kw)
+    assert b.attn_workspace_size(d) == 0
+    arr = b._ptr_array([0x20000] * max(1, d.P))
+    assert lib.domino_attn_fwd(ctypes.byref(d), 0x30000, arr, arr, 0x40000, 0x10000, 1 << 40, None) == status
+
+
+def test_attention_workspace_and_arguments(lib):
+    d = attn_desc()
+    M, Hp, dh = 2 * 256, 2, 128
+    qkv = 2 * M * 3 * Hp * dh * 2
+    o = 2 * M * Hp * dh * 2
+    z = 2 * M * 512 * 4
+    align = lambda x: (x + 255) // 256 * 256
+    assert b.attn_workspace_size(d) == align(align(align(256 + qkv) + o) + z)
+    arr = b._ptr_array([0x20000] * 2)
+    ws = b.attn_workspace_size(d)
+    assert lib.domino_attn_fwd(ctypes.byref(d), None, arr, arr, 0x40000, 0x10000, ws, None) == 1
+    assert lib.domino_attn_fwd(ctypes.byref(d), 0x30008, arr, arr, 0x40000, 0x10000, ws, None) == 3
+    assert lib.domino_attn_fwd(ctypes.byref(d), 0x30000, arr, arr, 0x40000, 0x10000, ws - 1, None) == 4
+    assert lib.domino_attn_fwd(ctypes.byref(attn_desc(B=0, mu=1)), None, None, None, None, None, 0, None) == 0
