@@ -172,18 +172,21 @@ struct WsLayout {
 
 constexpr size_t kTimelineOff = 64;  // header offset of the fused kernel's 3 timeline words
 
+// The fused schedule's tile counters follow the timeline words directly, so one
+// memset clears both before a fused call.
+constexpr size_t kSyncOff = 128;
+
 WsLayout ws_layout(const Shape& s, bool with_bwd) {
   WsLayout L;
-  size_t off = kHeaderBytes;
+  L.sync_bytes = fused_sync_bytes(s.Mc, s.d, s.P, s.mu);
+  L.sync_off = kSyncOff;
+  size_t off = align_up(kSyncOff + L.sync_bytes, 256);
   L.h_shard = static_cast<size_t>(s.M) * s.Fp * 2;
   L.h_off = off;
   off = align_up(off + L.h_shard * s.P, 256);
   L.z_shard = static_cast<size_t>(s.M) * s.d * s.psize;
   L.z_off = off;
   off = align_up(off + L.z_shard * s.P, 256);
-  L.sync_bytes = fused_sync_bytes(s.Mc, s.d, s.P, s.mu);
-  L.sync_off = off;
-  off = align_up(off + L.sync_bytes, 256);
   L.dg_shard = static_cast<size_t>(s.M) * s.Fp * s.nact * 2;
   L.dg_off = off;
   if (with_bwd) off = align_up(off + L.dg_shard * s.P, 256);
@@ -869,9 +872,8 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
     F.partial_f32 = s.partial == DOMINO_PARTIAL_F32;
     F.status = dstat;
     F.timeout_ns = tmo;
-    cudaError_t e = cudaMemsetAsync(F.sync, 0, W.sync_bytes, s0);
-    if (e == cudaSuccess) e = cudaMemsetAsync(F.timeline, 0xFF, 8, s0);
-    if (e == cudaSuccess) e = cudaMemsetAsync(F.timeline + 1, 0, 16, s0);
+    static_assert(kTimelineOff + 24 <= kSyncOff, "timeline words precede the counters");
+    cudaError_t e = cudaMemsetAsync(ws + kTimelineOff, 0, kSyncOff - kTimelineOff + W.sync_bytes, s0);
     if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("counter reset: ") + cudaGetErrorString(e));
     F.pair = pair;
     st = timed(T, s0, 0, DOMINO_KERNEL_FUSED, 0, 0, [&] {
@@ -1199,6 +1201,7 @@ domino_status_t domino_read_timeline(const void* workspace, void* stream, domino
     e = cudaMemcpy(out, static_cast<const uint8_t*>(workspace) + kTimelineOff, sizeof(domino_timeline_t),
                    cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("timeline read: ") + cudaGetErrorString(e));
+  if (out->start_ns != 0) out->start_ns = ~out->start_ns;  // the kernel keeps the complement of the start
   return DOMINO_OK;
 }
 

@@ -113,7 +113,7 @@ struct FusedParams {
   uint32_t* hcnt;                    // [mu][P][tiles_m]: finished GEMM1 tile quarters
   uint32_t* zcnt;                    // [mu][tiles_m][tiles_n2][4]: finished GEMM2 tile quarters
   uint32_t* red_next;                // ticket of the next reduction piece
-  uint64_t* timeline;                // [0] first CTA start, [1] last GEMM tile end, [2] last reduction end (ns)
+  uint64_t* timeline;                // [0] ~(first CTA start), [1] last GEMM tile end, [2] last reduction end (ns)
   int64_t d, Fp;
   int64_t ld_aux, aux_u_off;
   int32_t Mc, mu, P;

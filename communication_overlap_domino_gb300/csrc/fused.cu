@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    atomicMin(reinterpret_cast<unsigned long long*>(&f.timeline[0]),
-              static_cast<unsigned long long>(globaltimer_ns()));
+    atomicMax(reinterpret_cast<unsigned long long*>(&f.timeline[0]),  // ~start: zero is the initial value
+              ~static_cast<unsigned long long>(globaltimer_ns()));
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -554,8 +554,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    atomicMin(reinterpret_cast<unsigned long long*>(&f.timeline[0]),
-              static_cast<unsigned long long>(globaltimer_ns()));
+    atomicMax(reinterpret_cast<unsigned long long*>(&f.timeline[0]),  // ~start: zero is the initial value
+              ~static_cast<unsigned long long>(globaltimer_ns()));
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);

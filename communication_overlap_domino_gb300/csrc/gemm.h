@@ -72,7 +72,7 @@ struct FusedLaunch {
   void* Z[kMaxShards] = {};
   void* Y = nullptr;
   uint32_t* sync = nullptr;      // fused_sync_bytes() of zeroed counters
-  uint64_t* timeline = nullptr;  // 3 words: {UINT64_MAX, 0, 0} before the launch
+  uint64_t* timeline = nullptr;  // 3 words, zero before the launch ([0] receives ~start)
   int64_t M = 0, d = 0, Fp = 0;
   int mu = 1, P = 1;
   int epi_a = EPI_H_GELU;

@@ -114,7 +114,7 @@ void* pick(int P) {
   }
 }
 
-// One warp waits for a flag word (header offset 128) that nothing sets, through
+// One warp waits for a flag word (header offset 32) that nothing sets, through
 // the same bounded-wait pattern as the kernels' inter-CTA waits.
 __global__ void selftest_wait_kernel(DeviceStatus* st, const uint32_t* flag, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -134,10 +134,10 @@ __global__ void selftest_wait_kernel(DeviceStatus* st, const uint32_t* flag, uin
 
 domino_status_t launch_selftest_wait(void* workspace, uint64_t timeout_ns, cudaStream_t stream, std::string* err) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaError_t st = cudaMemsetAsync(ws + 128, 0, 4, stream);
+  cudaError_t st = cudaMemsetAsync(ws + 32, 0, 4, stream);
   if (st == cudaSuccess) {
     selftest_wait_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<DeviceStatus*>(ws),
-                                               reinterpret_cast<const uint32_t*>(ws + 128), timeout_ns);
+                                               reinterpret_cast<const uint32_t*>(ws + 32), timeout_ns);
     st = cudaGetLastError();
   }
   if (st != cudaSuccess) {

@@ -129,11 +129,12 @@ typedef struct domino_mlp_desc {
 
 /* Bytes of device workspace domino_mlp_fwd/bwd need for this problem
  * (0 for an invalid descriptor).  Layout, all owned by the library while a call
- * runs: a 256-byte header (device status words, fused-kernel timeline), the
- * hidden activations [P][M][F_p] bf16 (unless `saved` is given to fwd), the P
- * partial outputs [P][M][d] in the partial dtype, and the fused schedule's tile
- * counters.  with_bwd != 0 adds what the backward pass
- * needs (the gradient of the hidden layer and the dX partials). */
+ * runs: the device status words (bytes 0-15), the fused kernel's timeline (bytes
+ * 64-87) and, from byte 128, the fused schedule's tile counters (one memset
+ * clears timeline and counters before a fused call); then the hidden activations
+ * [P][M][F_p] bf16 (unless `saved` is given to fwd) and the P partial outputs
+ * [P][M][d] in the partial dtype, each 256-byte aligned.  with_bwd != 0 adds
+ * what the backward pass needs (the gradient of the hidden layer). */
 DOMINO_API size_t domino_mlp_workspace_size(const domino_mlp_desc_t* desc, int32_t with_bwd);
 
 /* Bytes of the `saved` buffer that fwd fills for bwd (0 if invalid):

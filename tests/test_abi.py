@@ -59,11 +59,11 @@ def test_workspace_layout(lib):
     Fp = F // P
     tiles_m, tiles_n2 = (M // mu + 127) // 128, (dd + 255) // 256
     sync = 4 * (mu * P * tiles_m + mu * tiles_m * tiles_n2 * 4 + 1)
-    sync = (sync + 255) // 256 * 256
-    expect = 256 + P * M * Fp * 2 + P * M * dd * 4 + sync
+    head = (128 + sync + 255) // 256 * 256  # status, timeline, then the tile counters from byte 128
+    expect = head + P * M * Fp * 2 + P * M * dd * 4
     assert b.workspace_size(d) == expect
     d16 = desc(partial="bf16")
-    assert b.workspace_size(d16) == 256 + P * M * Fp * 2 + P * M * dd * 2 + sync
+    assert b.workspace_size(d16) == head + P * M * Fp * 2 + P * M * dd * 2
     assert b.saved_size(d) == P * M * Fp * 2 * 2
     assert b.saved_size(desc(act="swiglu")) == P * M * Fp * 3 * 2
     assert b.workspace_size(d, with_bwd=True) > b.workspace_size(d)
