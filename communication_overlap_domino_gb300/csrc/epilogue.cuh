@@ -48,7 +48,11 @@ __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + e
 __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
 }
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+// silu(x) = x * sigmoid(x) with the fast reciprocal: far inside the bf16
+// rounding of its result; for x -> -inf the denominator overflows to inf and
+// the quotient goes to 0 as it should.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float silu(float x) { return x * sigmoid_fast(x); }
 
 // Derivatives for the backward epilogue (product and chain rules).
 __device__ __forceinline__ float gelu_erf_grad(float x) {
@@ -366,7 +370,7 @@ __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float dh = __uint_as_float(r0[j]);
-        const float sg = 1.0f / (1.0f + __expf(-g[j]));
+        const float sg = sigmoid_fast(g[j]);
         du[j] = dh * g[j] * sg;                               // dH * silu(g)
         dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
       }
