@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         const bool rescale = m_blk > m_run + kRescaleLog2;
         float alpha = 1.0f;
         if (rescale) {
-          alpha = exp2f(m_run - m_blk);
+          alpha = ex2_approx(m_run - m_blk);
           m_run = m_blk;
         }
         // pass 2: this thread's 64 probabilities, packed as bf16 pairs
@@ -337,10 +337,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int k0 = half * 64 + 2 * e, k1 = k0 + 32;
-            float p0 = exp2f(fmaf(__uint_as_float(v0[2 * e]), a.scale_log2, -m_run));
-            float p1 = exp2f(fmaf(__uint_as_float(v0[2 * e + 1]), a.scale_log2, -m_run));
-            float p2 = exp2f(fmaf(__uint_as_float(v1[2 * e]), a.scale_log2, -m_run));
-            float p3 = exp2f(fmaf(__uint_as_float(v1[2 * e + 1]), a.scale_log2, -m_run));
+            float p0 = ex2_approx(fmaf(__uint_as_float(v0[2 * e]), a.scale_log2, -m_run));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v0[2 * e + 1]), a.scale_log2, -m_run));
+            float p2 = ex2_approx(fmaf(__uint_as_float(v1[2 * e]), a.scale_log2, -m_run));
+            float p3 = ex2_approx(fmaf(__uint_as_float(v1[2 * e + 1]), a.scale_log2, -m_run));
             if (diag) {
               p0 = k0 <= r ? p0 : 0.0f;
               p1 = k0 + 1 <= r ? p1 : 0.0f;
