@@ -32,8 +32,9 @@
 //               added through shared memory and O / l is stored as bf16.
 //
 // Barriers (all waits bounded, as in the GEMMs): q_full / q_empty, k_full[s] /
-// k_empty[s], v_full[s] / v_empty[s], s_full[b] / s_empty[b] (256 arrivals),
-// p_full (256), pv_full, o_empty (256), l_ready[2] (256), final.
+// k_empty[s], v_full[s] / v_empty[s], s_full[b] / s_empty[b], p_full, pv_full,
+// o_empty, l_ready[2], final; the softmax warps arrive once per warp, after
+// __syncwarp, on s_empty, p_full, o_empty and l_ready.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -49,7 +50,7 @@ namespace domino {
 namespace {
 
 constexpr int kAttnThreads = 320;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxWarps = 8;  // consumer barriers count one arrival per softmax warp
 constexpr int kTile = 128;                        // queries per item, keys per block, head width
 constexpr int kSub = kTile * 64 * 2;              // 16 KB: 128 rows x 64 bf16 (one 128-byte-swizzled box)
 constexpr int kQBytes = 2 * kSub;                 // Q tile: dh halves 0-63 and 64-127
@@ -148,12 +149,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], kSoftmaxThreads);
-      mbar_init(&l_ready[s], kSoftmaxThreads);
+      mbar_init(&s_empty[s], kSoftmaxWarps);
+      mbar_init(&l_ready[s], kSoftmaxWarps);
     }
-    mbar_init(p_full, kSoftmaxThreads);
+    mbar_init(p_full, kSoftmaxWarps);
     mbar_init(pv_full, 1);
-    mbar_init(o_empty, kSoftmaxThreads);
+    mbar_init(o_empty, kSoftmaxWarps);
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -382,8 +383,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         }
         fence_proxy_async_shared();  // P is read by the tensor cores (async proxy)
         tc_fence_before_sync();
-        mbar_arrive(&s_empty[sb]);
-        mbar_arrive(p_full);
+        __syncwarp();  // the warp's scores are read and its P stored: one arrival per warp
+        if (lane == 0) {
+          mbar_arrive(&s_empty[sb]);
+          mbar_arrive(p_full);
+        }
         l_run = l_run * alpha + sum;
       }
       if (!ok) break;
@@ -396,12 +400,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       tmem_ld_32x32b_x32(to + 32, o1);
       tmem_ld_wait();
       tc_fence_before_sync();
-      mbar_arrive(o_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
       // the row sum: this thread's part plus its partner's, through shared memory
       const uint32_t lb = item_count & 1;
       float* lbuf = lsum + lb * 2 * kTile;
       lbuf[half * kTile + r] = l_run;
-      mbar_arrive(&l_ready[lb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&l_ready[lb]);
       if (!mbar_wait(&l_ready[lb], (item_count >> 1) & 1, abort_flag, tmo, a.status, kSiteAttnPV, t)) break;
       const float inv = 1.0f / (lbuf[r] + lbuf[kTile + r]);
       // O / l as bf16: this thread's 128 contiguous bytes of the row
