@@ -85,6 +85,8 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.mark = 0
+        self.in_timed = None
 
     def start(self):
         try:
@@ -101,6 +103,26 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def ready(self, work, timeout_s=5.0):
+        """Runs `work` (one untimed step of the same load, synchronised) until nvidia-smi has
+        delivered its first sample, then marks where the timed region's samples begin."""
+        import torch
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout_s:
+            work()
+            torch.cuda.synchronize()
+        self.mark = len(self.lines)
+
+    def top_up(self, work, n=3, timeout_s=5.0):
+        """Ends the timed region's samples.  A region too short for n samples at the 100 ms
+        period is followed by untimed steps of the same load until n samples have arrived."""
+        import torch
+        self.in_timed = len(self.lines) - self.mark
+        t0 = time.perf_counter()
+        while self.proc is not None and len(self.lines) - self.mark < n and time.perf_counter() - t0 < timeout_s:
+            work()
+            torch.cuda.synchronize()
+
     def stop(self):
         if self.proc is None:
             return None
@@ -113,7 +135,7 @@ class ClockSampler:
             self.thread.join(timeout=5)
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        for ln in self.lines[self.mark:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -127,8 +149,33 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if self.in_timed is not None and self.in_timed < len(sm):
+            out["samples_in_timed_region"] = self.in_timed
+            out["note"] = "timed region shorter than the samples asked for: the rest come from untimed steps " \
+                          "of the same load right after it"
+        return out
+
+
+# ------------------------------------------------------ tensor-core probe
+
+def tensor_probe(clk, repeats=3, mmas=1 << 19):
+    """Best of `repeats` runs of domino_tensor_peak (paired tcgen05 MMAs alone, every co-resident
+    2-CTA cluster), with the per-SM rate per clock it measures and the theoretical rate
+    SMs x that rate x SM clock, at the clock sampled under the timed region's load and at the
+    maximum SM clock."""
+    from communication_overlap_domino_gb300 import binding as b
+    runs = [b.tensor_peak(mmas) for _ in range(repeats)]
+    best = max(runs, key=lambda r: r["tflops"])
+    fpc = max(r["flops_per_clk_sm"] for r in runs)
+    out = {"tflops": round(best["tflops"], 1), "sm_mhz_in_probe": round(best["sm_mhz"], 1),
+           "flops_per_clk_per_sm": round(fpc, 1), "clusters": best["clusters"], "num_sms": best["num_sms"],
+           "mmas_per_cluster": mmas, "mma": "tcgen05.mma cta_group::2 kind::f16 256x256x16, bf16 -> fp32"}
+    if clk:
+        out["theoretical_tflops_at_load_clock"] = round(best["num_sms"] * fpc * clk["sm_mhz"] * 1e6 / 1e12, 1)
+        out["theoretical_tflops_at_max_clock"] = round(best["num_sms"] * fpc * clk["sm_max_mhz"] * 1e6 / 1e12, 1)
+    return out
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -274,6 +321,8 @@ def run_ours(args, w, rank, world, local_rank):
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local_rank
     clocks = ClockSampler(gpu_index)
     clocks.start()
+    load = lambda: (flush.zero_(), step())  # noqa: E731
+    clocks.ready(load)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     wall0 = time.perf_counter()
@@ -284,7 +333,9 @@ def run_ours(args, w, rank, world, local_rank):
         ev[i][1].record(stream)
     barrier()
     wall = time.perf_counter() - wall0
+    clocks.top_up(load)
     clk = clocks.stop()
+    probe = tensor_probe(clk)
     st = b.query_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {b.STATUS.get(st)}")
@@ -474,7 +525,9 @@ def run_ours(args, w, rank, world, local_rank):
             "frac_of_burst": round(dom_tflops / float(peaks.get("bf16_tflops", peak_tf)), 4),
             "flops_per_launch": dom_flops_per_launch,
             "traffic": ncu_traffic(dominant, w.name),
+            "frac_of_mma_probe": round(dom_tflops / probe["tflops"], 4),
         },
+        "tensor_probe": probe,
         "shard_sum": None if ss_gbs is None else {
             "bound": "hbm",
             "achieved": round(ss_gbs, 1),
@@ -549,6 +602,8 @@ def run_attn(args, w, rank, world, local_rank):
     b.kernel_times_reset()
     clocks = ClockSampler(local_rank)
     clocks.start()
+    load = lambda: (flush.zero_(), step())  # noqa: E731
+    clocks.ready(load)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -559,7 +614,9 @@ def run_attn(args, w, rank, world, local_rank):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    clocks.top_up(load)
     clk = clocks.stop()
+    probe = tensor_probe(clk)
     if b.query_device_status(ws) != 0:
         raise RuntimeError("device status after the timed region")
     mean_ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in ev), world, dev)
@@ -626,7 +683,9 @@ def run_attn(args, w, rank, world, local_rank):
             "bound": "tensor", "achieved": round(a_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
             "frac": round(a_tf / peak_tf, 4), "peak_source": f"{peak_src} bf16_tflops_sustained",
             "flops_per_launch": float(core_flops_chunk), "traffic": ncu_traffic("attn", w.name),
+            "frac_of_mma_probe": round(a_tf / probe["tflops"], 4),
         },
+        "tensor_probe": probe,
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
                         "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["flops"] else None,
                         "share": round(v["total_ms"] / sum(x["total_ms"] for x in kinds.values()), 4)}

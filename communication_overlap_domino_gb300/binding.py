@@ -99,6 +99,22 @@ class Plan(ctypes.Structure):
 
 PLAN_REASON = {0: "fits_l2", 1: "largest_filling", 2: "small"}
 
+
+class TensorPeak(ctypes.Structure):
+    _fields_ = [
+        ("tflops", ctypes.c_double),
+        ("flops", ctypes.c_double),
+        ("ms", ctypes.c_double),
+        ("sm_mhz", ctypes.c_double),
+        ("flops_per_clk_sm", ctypes.c_double),
+        ("clusters", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+    ]
+
+
+TENSOR_PEAK_MAX_MMAS = 1 << 22
+TENSOR_PEAK_WS_BYTES = 256
+
 _LIB: Optional[ctypes.CDLL] = None
 _VP = ctypes.c_void_p
 _VPP = ctypes.POINTER(ctypes.c_void_p)
@@ -126,6 +142,8 @@ SIGNATURES = [
     ("domino_attn_fwd", ctypes.c_int, [ctypes.POINTER(AttnDesc), _VP, _VPP, _VPP, _VP, _VP, ctypes.c_size_t, _VP]),
     ("domino_mlp_fwd_bwd_interleaved", ctypes.c_int,
      [ctypes.POINTER(MlpDesc), _VPP, _VPP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VPP, _VPP, _VP, ctypes.c_size_t, _VP]),
+    ("domino_tensor_peak", ctypes.c_int,
+     [ctypes.c_int64, ctypes.c_int32, _VP, ctypes.c_size_t, ctypes.c_uint64, _VP, ctypes.POINTER(TensorPeak)]),
 ]
 
 
@@ -445,6 +463,20 @@ def plan(M: int, d: int, F: int, P: int, act: str, partial: str, out_slices: int
     return {"mu": out.mu, "schedule": sched, "reason": PLAN_REASON.get(out.reason, out.reason),
             "gemm1_tiles_per_chunk": out.gemm1_tiles_per_chunk, "chunk_h_bytes": out.chunk_h_bytes,
             "l2_budget_bytes": out.l2_budget_bytes}
+
+
+def tensor_peak(mmas_per_cluster: int = 1 << 18, clusters: int = 0, *, workspace=None, stream=None,
+                timeout_ns: int = 0) -> dict:
+    """domino_tensor_peak: dense bf16 rate of back-to-back paired tcgen05 MMAs on every
+    co-resident 2-CTA cluster (clusters=0), with the SM clock measured in the kernel."""
+    import torch
+    ws = workspace if workspace is not None else torch.zeros(TENSOR_PEAK_WS_BYTES, dtype=torch.uint8, device="cuda")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    out = TensorPeak()
+    _check(lib().domino_tensor_peak(mmas_per_cluster, clusters, ws.data_ptr(), ws.numel(), timeout_ns,
+                                    s.cuda_stream, ctypes.byref(out)), "domino_tensor_peak")
+    return {"tflops": out.tflops, "flops": out.flops, "ms": out.ms, "sm_mhz": out.sm_mhz,
+            "flops_per_clk_sm": out.flops_per_clk_sm, "clusters": out.clusters, "num_sms": out.num_sms}
 
 
 def kernel_times_reset() -> None:

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["api.cu", "gemm.cu", "gemm_pair.cu", "fused.cu", "shard_sum.cu", "noalloc.cu", "plan.cu", "attn.cu"]
+SOURCES = ["api.cu", "gemm.cu", "gemm_pair.cu", "fused.cu", "shard_sum.cu", "noalloc.cu", "plan.cu", "attn.cu", "tensor_peak.cu"]
 
 
 def _nvcc() -> str:

@@ -397,6 +397,39 @@ typedef struct domino_plan {
 DOMINO_API domino_status_t domino_mlp_plan(const domino_mlp_desc_t* problem, const domino_plan_hw_t* hw,
                                            domino_plan_t* out);
 
+/* Tensor-core rate probe: the dense bf16 throughput of this GPU's tcgen05 MMAs
+ * on their own, the ceiling the GEMM main loops approach.  Each 2-CTA cluster
+ * (one CTA per SM) issues `mmas_per_cluster` back-to-back paired MMAs of
+ * 256 x 256 x 16 (bf16 operands already in shared memory, fp32 accumulators in
+ * tensor memory); there are no loads, stores or epilogue.  The kernel also
+ * counts SM cycles and nanoseconds around the MMA stream of cluster 0, so the
+ * rate per SM per clock follows without an outside clock reading.
+ * mmas_per_cluster: 1 .. DOMINO_TENSOR_PEAK_MAX_MMAS.  clusters: 2-CTA
+ * clusters to launch, <= 0 for the most that can be co-resident (the paired
+ * GEMMs' grid); more than that is rejected with DOMINO_ERR_UNSUPPORTED.
+ * workspace: >= DOMINO_TENSOR_PEAK_WS_BYTES bytes of device memory, 256-byte
+ * aligned, its status words zero (as after domino_query_device_status).
+ * timeout_ns: bound on the wait for the MMAs to finish (0: 5 s).  stream: the
+ * launch stream; the call synchronises on it and returns the measurement in
+ * *out.  Errors: DOMINO_ERR_INVALID_ARG / ALIGNMENT for bad arguments (before
+ * any CUDA call), DOMINO_ERR_CUDA, DOMINO_ERR_TIMEOUT when the wait gave up. */
+#define DOMINO_TENSOR_PEAK_MAX_MMAS (1 << 22)
+#define DOMINO_TENSOR_PEAK_WS_BYTES 256
+
+typedef struct domino_tensor_peak {
+  double tflops;            /* flops / kernel duration, in TFLOP/s                     */
+  double flops;             /* 2 * 256 * 256 * 16 * mmas_per_cluster * clusters        */
+  double ms;                /* kernel duration (CUDA events on `stream`)               */
+  double sm_mhz;            /* SM clock during cluster 0's MMA stream (cycles / ns)    */
+  double flops_per_clk_sm;  /* cluster 0's flops / its cycles / 2 SMs                  */
+  int32_t clusters;         /* 2-CTA clusters launched                                 */
+  int32_t num_sms;          /* SMs of the device                                       */
+} domino_tensor_peak_t;
+
+DOMINO_API domino_status_t domino_tensor_peak(int64_t mmas_per_cluster, int32_t clusters, void* workspace,
+                                              size_t workspace_bytes, uint64_t timeout_ns, void* stream,
+                                              domino_tensor_peak_t* out);
+
 #ifdef __cplusplus
 }
 #endif

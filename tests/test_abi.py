@@ -178,3 +178,16 @@ def test_attention_workspace_and_arguments(lib):
     assert lib.domino_attn_fwd(ctypes.byref(d), 0x30008, arr, arr, 0x40000, 0x10000, ws, None) == 3
     assert lib.domino_attn_fwd(ctypes.byref(d), 0x30000, arr, arr, 0x40000, 0x10000, ws - 1, None) == 4
     assert lib.domino_attn_fwd(ctypes.byref(attn_desc(B=0, mu=1)), None, None, None, None, None, 0, None) == 0
+
+
+def test_tensor_peak_validates_before_cuda(lib):
+    out = b.TensorPeak()
+    ref = ctypes.byref(out)
+    ws = b.TENSOR_PEAK_WS_BYTES
+    assert lib.domino_tensor_peak(1, 0, None, ws, 0, None, ref) == 1
+    assert lib.domino_tensor_peak(1, 0, 0x40000, ws, 0, None, None) == 1
+    assert lib.domino_tensor_peak(0, 0, 0x40000, ws, 0, None, ref) == 1
+    assert lib.domino_tensor_peak(b.TENSOR_PEAK_MAX_MMAS + 1, 0, 0x40000, ws, 0, None, ref) == 1
+    assert lib.domino_tensor_peak(1, 0, 0x40000, ws - 1, 0, None, ref) == 4
+    assert lib.domino_tensor_peak(1, 0, 0x40010, ws, 0, None, ref) == 3
+    assert b"mmas_per_cluster" in lib.domino_last_error() or b"256-byte" in lib.domino_last_error()
