@@ -53,6 +53,7 @@ struct DeviceState {
   int num_sms = 0;
   int fused_max_ctas = 0;     // co-resident CTAs of the fused kernel (cooperative launch limit)
   int pair_max_clusters = 0;  // co-resident 2-CTA clusters of the paired GEMM
+  int quad_max_clusters = 0;  // co-resident 4-CTA clusters of its quad form (0: not used)
   int fused_pair_clusters = 0;  // co-resident 2-CTA clusters of the paired fused kernel (0: not usable)
   cudaStream_t reduce_stream = nullptr;
   cudaEvent_t ev_fork = nullptr;
@@ -91,7 +92,7 @@ domino_status_t device_state(DeviceState** out) {
     }
     e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = prepare_gemm_kernels();
-    if (e == cudaSuccess) e = prepare_pair_kernels(&ds.pair_max_clusters);
+    if (e == cudaSuccess) e = prepare_pair_kernels(&ds.pair_max_clusters, &ds.quad_max_clusters);
     if (e == cudaSuccess) e = prepare_attn_kernel();
     int per_sm = 0;
     if (e == cudaSuccess) e = prepare_fused_kernels(&per_sm, &ds.fused_pair_clusters);
@@ -246,7 +247,8 @@ domino_status_t timed(Timer& T, cudaStream_t st, int32_t stream_id, int32_t kind
 
 // One grouped GEMM launch, as one-CTA tiles or as paired-CTA clusters.
 domino_status_t run_gemm(const GemmLaunch& L, const DeviceState* ds, bool pair, cudaStream_t st, std::string* err) {
-  return pair ? launch_gemm_pair(L, ds->pair_max_clusters, st, err) : launch_gemm(L, ds->num_sms, st, err);
+  return pair ? launch_gemm_pair(L, ds->pair_max_clusters, ds->quad_max_clusters, st, err)
+              : launch_gemm(L, ds->num_sms, st, err);
 }
 
 // ------------------------------------------------------- launch sequences

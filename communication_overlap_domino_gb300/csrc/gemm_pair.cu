@@ -18,6 +18,15 @@
 //   tempty[a] in the even CTA, count 256: its own 128 epilogue threads plus the
 //            odd CTA's 128, which arrive remotely once they have read their rows.
 // Tensor memory is allocated collectively by warp 1 of both CTAs.
+//
+// Quad form (4-CTA clusters, two pairs on one 512 x 256 tile): the two pairs
+// share the tile's B column block, so each CTA loads only half of its 128 B
+// rows (a 64-row box) and multicasts it to the CTA in the same position of the
+// other pair.  Per SM this cuts the operand bytes loaded from L2 per MMA by a
+// quarter (A 16 KB + B 8 KB per stage instead of 16 + 16).  Each pair leader's
+// full[s] still receives 64 KB per stage (its pair's A halves, and its B halves
+// from both pairs' loads); empty[s] in every CTA counts one MMA completion from
+// each pair leader, since a stage slot is written by both pairs' producers.
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -43,7 +52,7 @@ static_assert(kPairSmemBytes <= 232448, "shared memory budget");
 constexpr int kPairAccBufs = 2;
 constexpr uint32_t kPairTmemCols = 256 * kPairAccBufs;
 
-// Tile t -> (shard, 256-row block, column block).  Rows go in groups of
+// Tile t -> (shard, cluster row block (256 rows per pair, 512 per quad), column block).  Rows go in groups of
 // group_m blocks; within a group: for each shard, for each column block, the
 // group's row blocks.  Consecutive tiles (run at the same time by the clusters)
 // share a column block of B; a group's rows of A stay in L2 while every shard
@@ -63,9 +72,10 @@ __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int
   mb2 = g * G + (r2 - nb * gm);
 }
 
-template <int EPI, bool A_MN, bool B_MN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+template <int EPI, bool A_MN, bool B_MN, bool QUAD>
+__device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
+  constexpr int kCluster = QUAD ? 4 : 2;
+  constexpr int kTileRows = 128 * kCluster;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;
@@ -82,12 +92,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
+  const bool leader = (rank & 1u) == 0;  // the pair's even CTA issues its MMAs
+  const uint32_t leader_rank = rank & ~1u;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader_rank);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], QUAD ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -109,18 +121,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
   const int num_tiles = p.num_tiles;
   const uint64_t tmo = p.timeout_ns;
-  const int num_clusters = gridDim.x >> 1;
-  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x / kCluster;
+  const int cluster_id = blockIdx.x / kCluster;
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- TMA producer
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
-    const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);  // the even CTA's full[0]
+    const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), leader_rank);  // the pair leader's full[0]
+    // quad: this CTA's 64-row share of the B rows it and its counterpart in the other pair use
+    const uint16_t b_mask = static_cast<uint16_t>(0x5u << (rank & 1u));
+    const int b_part = static_cast<int>(rank >> 1);
     for (int t = cluster_id; t < num_tiles && !*abort_flag; t += num_clusters) {
-      int shard, mb2, nb;
-      pair_tile_coords(p, t, shard, mb2, nb);
-      const int ya = p.a_row0 + mb2 * 256 + 128 * static_cast<int>(rank);
+      int shard, mbx, nb;
+      pair_tile_coords(p, t, shard, mbx, nb);
+      const int ya = p.a_row0 + mbx * kTileRows + 128 * static_cast<int>(rank);
       const int yb = p.n_base + nb * p.n_tile + (leader ? 0 : p.b1_off);
       const CUtensorMap* mapb = leader ? &p.map_b0[shard] : &p.map_b1[shard];
       bool ok = true;
@@ -140,7 +155,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         } else {
           tma_load_2d_pair(sa, &p.map_a[shard], bar, k0, ya);
         }
-        if constexpr (B_MN) {
+        if constexpr (QUAD) {
+          // 64 B rows (8 KB; a K-major map has 64-row boxes here) to both CTAs of this position
+          if constexpr (B_MN)
+            tma_load_2d_pair_multicast(sb + 8192 * b_part, mapb, bar, yb + 64 * b_part, k0, b_mask);
+          else
+            tma_load_2d_pair_multicast(sb + 8192 * b_part, mapb, bar, k0, yb + 64 * b_part, b_mask);
+        } else if constexpr (B_MN) {
           tma_load_2d_pair(sb, mapb, bar, yb, k0);
           tma_load_2d_pair(sb + 8192, mapb, bar, yb + 64, k0);
         } else {
@@ -156,8 +177,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
     }
     // Drain: the even CTA waits until every load counted on its barriers (its
-    // own and the odd CTA's) has landed; the odd CTA's loads complete no later
-    // than the cluster barrier below, which the even CTA reaches only after this.
+    // own, the odd CTA's and, in the quad form, the other pair's multicasts into
+    // this pair) has landed; loads into the odd CTA complete no later than the
+    // cluster barrier below, which the even CTA reaches only after this.
     if (leader) {
       for (int s = 0; s < kPairStages; ++s) {
         if (issued_mask & (1u << s)) {
@@ -193,16 +215,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
           mma_bf16_ss_pair(d_tmem, adesc + kAdvA * k, bdesc + kAdvB * k, idesc, (kb | k) != 0 ? 1u : 0u);
-        mma_commit_pair_multicast(&empty_bar[stage], 0x3);
+        // frees the stage in every CTA that wrote it: the pair, and in the quad form the other pair too
+        mma_commit_pair_multicast(&empty_bar[stage], QUAD ? 0xF : pair_mask);
         if (++stage == kPairStages) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (!ok) break;
-      mma_commit_pair_multicast(&tfull_bar[acc], 0x3);
+      mma_commit_pair_multicast(&tfull_bar[acc], pair_mask);
     }
-    mma_commit_pair_multicast(final_bar, 0x1);
+    mma_commit_pair_multicast(final_bar, static_cast<uint16_t>(1u << leader_rank));
     volatile int no_abort = 0;
     mbar_wait(final_bar, 0, &no_abort, tmo, p.status, kSiteDrain, 99);
   } else if (warp >= 2) {
@@ -217,13 +240,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint32_t acc_phase = kPairAccBufs == 2 ? ((i >> 1) & 1) : (i & 1);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, tmo, p.status, kSiteEpilogueTmemFull, t)) break;
       tc_fence_after_sync();
-      int shard, mb2, nb;
-      pair_tile_coords(p, t, shard, mb2, nb);
+      int shard, mbx, nb;
+      pair_tile_coords(p, t, shard, mbx, nb);
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
       const EpiArgs e{p.out[shard], p.aux[shard], p.ldo, p.ld_aux, p.aux_u_off, p.out_u_off,
                       p.rows, p.out_row0, p.n_end, p.use_tma_store ? &p.map_out[shard] : nullptr, stage};
       const int col0 = p.n_base + nb * p.n_tile;
-      const int mb = 2 * mb2 + static_cast<int>(rank);  // this CTA's 128-row block
+      const int mb = kCluster * mbx + static_cast<int>(rank);  // this CTA's 128-row block
       if constexpr (is_dg(EPI))
         epilogue_tile_dg<EPI>(e, tacc, mb, col0, row_in_tile, sbuf);
       else
@@ -232,7 +255,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (leader)
         mbar_arrive(&tempty_bar[acc]);
       else
-        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), leader_rank));
     }
     if (lane == 0) bulk_wait_group<0>();
   }
@@ -249,31 +272,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 template <int EPI, bool A_MN, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  gemm_pair_body<EPI, A_MN, B_MN, false>(p);
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_quad_kernel(const __grid_constant__ GemmParams p) {
+  gemm_pair_body<EPI, A_MN, B_MN, true>(p);
+}
+
+template <int EPI, bool A_MN, bool B_MN>
 void* pair_ptr() {
   return reinterpret_cast<void*>(&gemm_pair_kernel<EPI, A_MN, B_MN>);
+}
+template <int EPI, bool A_MN, bool B_MN>
+void* quad_ptr() {
+  return reinterpret_cast<void*>(&gemm_quad_kernel<EPI, A_MN, B_MN>);
 }
 
 struct PairEntry {
   int epi;
   bool a_mn, b_mn;
-  void* fn;
+  void* fn;   // 2-CTA clusters
+  void* fn4;  // 4-CTA clusters (two pairs sharing B)
 };
 
 const PairEntry* pair_table(int* n) {
   static const PairEntry table[] = {
-      {EPI_H_GELU, false, false, pair_ptr<EPI_H_GELU, false, false>()},
-      {EPI_H_GELU_TANH, false, false, pair_ptr<EPI_H_GELU_TANH, false, false>()},
-      {EPI_H_IDENTITY, false, false, pair_ptr<EPI_H_IDENTITY, false, false>()},
-      {EPI_H_SWIGLU, false, false, pair_ptr<EPI_H_SWIGLU, false, false>()},
-      {EPI_Z_F32, false, false, pair_ptr<EPI_Z_F32, false, false>()},
-      {EPI_Z_BF16, false, false, pair_ptr<EPI_Z_BF16, false, false>()},
-      {EPI_DG_GELU, false, true, pair_ptr<EPI_DG_GELU, false, true>()},
-      {EPI_DG_GELU_TANH, false, true, pair_ptr<EPI_DG_GELU_TANH, false, true>()},
-      {EPI_DG_IDENTITY, false, true, pair_ptr<EPI_DG_IDENTITY, false, true>()},
-      {EPI_DG_SWIGLU, false, true, pair_ptr<EPI_DG_SWIGLU, false, true>()},
-      {EPI_Z_F32, false, true, pair_ptr<EPI_Z_F32, false, true>()},
-      {EPI_Z_BF16, false, true, pair_ptr<EPI_Z_BF16, false, true>()},
-      {EPI_Z_BF16, true, true, pair_ptr<EPI_Z_BF16, true, true>()},
+      {EPI_H_GELU, false, false, pair_ptr<EPI_H_GELU, false, false>(), quad_ptr<EPI_H_GELU, false, false>()},
+      {EPI_H_GELU_TANH, false, false, pair_ptr<EPI_H_GELU_TANH, false, false>(), quad_ptr<EPI_H_GELU_TANH, false, false>()},
+      {EPI_H_IDENTITY, false, false, pair_ptr<EPI_H_IDENTITY, false, false>(), quad_ptr<EPI_H_IDENTITY, false, false>()},
+      {EPI_H_SWIGLU, false, false, pair_ptr<EPI_H_SWIGLU, false, false>(), quad_ptr<EPI_H_SWIGLU, false, false>()},
+      {EPI_Z_F32, false, false, pair_ptr<EPI_Z_F32, false, false>(), quad_ptr<EPI_Z_F32, false, false>()},
+      {EPI_Z_BF16, false, false, pair_ptr<EPI_Z_BF16, false, false>(), quad_ptr<EPI_Z_BF16, false, false>()},
+      {EPI_DG_GELU, false, true, pair_ptr<EPI_DG_GELU, false, true>(), quad_ptr<EPI_DG_GELU, false, true>()},
+      {EPI_DG_GELU_TANH, false, true, pair_ptr<EPI_DG_GELU_TANH, false, true>(), quad_ptr<EPI_DG_GELU_TANH, false, true>()},
+      {EPI_DG_IDENTITY, false, true, pair_ptr<EPI_DG_IDENTITY, false, true>(), quad_ptr<EPI_DG_IDENTITY, false, true>()},
+      {EPI_DG_SWIGLU, false, true, pair_ptr<EPI_DG_SWIGLU, false, true>(), quad_ptr<EPI_DG_SWIGLU, false, true>()},
+      {EPI_Z_F32, false, true, pair_ptr<EPI_Z_F32, false, true>(), quad_ptr<EPI_Z_F32, false, true>()},
+      {EPI_Z_BF16, false, true, pair_ptr<EPI_Z_BF16, false, true>(), quad_ptr<EPI_Z_BF16, false, true>()},
+      // the weight gradient dA = dG^T X (both operands MN-major) measured slower in the quad form
+      {EPI_Z_BF16, true, true, pair_ptr<EPI_Z_BF16, true, true>(), nullptr},
   };
   *n = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;
@@ -282,37 +323,60 @@ const PairEntry* pair_table(int* n) {
 }  // namespace
 
 // Sets the shared-memory attribute of every paired kernel and returns how many
-// 2-CTA clusters of them can be resident at once (the persistent grid size):
-// the GPU's SMs need not pair up evenly.
-cudaError_t prepare_pair_kernels(int* max_clusters) {
+// 2-CTA clusters, and 4-CTA clusters of the quad form, can be resident at once
+// (the persistent grid sizes): the GPU's SMs need not group evenly.  A device
+// that cannot hold a 4-CTA cluster of these kernels gets 0 and the 2-CTA form.
+cudaError_t prepare_pair_kernels(int* max_clusters, int* max_quad_clusters) {
   int n = 0;
   const PairEntry* t = pair_table(&n);
-  int best = 1 << 30;
+  int best = 1 << 30, best4 = 1 << 30;
   for (int i = 0; i < n; ++i) {
-    cudaError_t st = cudaFuncSetAttribute(t[i].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
-    if (st != cudaSuccess) return st;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 512);
-    cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = kPairSmemBytes;
-    int clusters = 0;
-    st = cudaOccupancyMaxActiveClusters(&clusters, t[i].fn, &cfg);
-    if (st != cudaSuccess) return st;
-    best = clusters < best ? clusters : best;
+    for (int form = 0; form < 2; ++form) {
+      void* fn = form ? t[i].fn4 : t[i].fn;
+      if (fn == nullptr) continue;
+      cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+      if (st != cudaSuccess) return st;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(form ? 4 * 256 : 2 * 512);
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = kPairSmemBytes;
+      int clusters = 0;
+      st = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
+      if (st != cudaSuccess) {
+        if (!form) return st;
+        (void)cudaGetLastError();
+        clusters = 0;
+      }
+      int& b = form ? best4 : best;
+      b = clusters < b ? clusters : b;
+    }
   }
   *max_clusters = best;
+  *max_quad_clusters = best4;
   return cudaSuccess;
 }
 
-domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStream_t stream, std::string* err) {
+domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, int max_quad_clusters, cudaStream_t stream,
+                                 std::string* err) {
   GemmParams p;
   memset(&p, 0, sizeof p);
   if (L.num_shards < 1 || L.num_shards > kMaxShards) {
     if (err) *err = "launch_gemm_pair: bad shard count";
     return DOMINO_ERR_INVALID_ARG;
   }
+  // quad form when there are at least two 256-row blocks to put side by side (and a quad kernel for this layout)
+  bool quad = max_quad_clusters > 0 && L.rows > 256;
+  if (quad) {
+    int n = 0;
+    const PairEntry* t = pair_table(&n);
+    bool have = false;
+    for (int i = 0; i < n; ++i)
+      if (t[i].epi == L.epi && t[i].a_mn == L.a_mn && t[i].b_mn == L.b_mn) have = t[i].fn4 != nullptr;
+    quad = have;
+  }
+  const int tile_rows = quad ? 512 : 256;
   const int a_box = L.a_mn ? kBK : 128;
-  const int b_box = L.b_mn ? kBK : 128;
+  const int b_box = L.b_mn ? kBK : (quad ? 64 : 128);
   for (int s = 0; s < L.num_shards; ++s) {
     if (!encode_bf16_sw128(&p.map_a[s], L.a[s], a_box, err)) return DOMINO_ERR_CUDA;
     if (!encode_bf16_sw128(&p.map_b0[s], L.b0[s], b_box, err)) return DOMINO_ERR_CUDA;
@@ -343,11 +407,11 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStre
   p.n_tile = L.n_tile;
   p.b1_off = L.b1_off;
   p.num_kb = static_cast<int32_t>((L.K + kBK - 1) / kBK);
-  p.tiles_m = (L.rows + 255) / 256;
+  p.tiles_m = (L.rows + tile_rows - 1) / tile_rows;
   p.tiles_n = (L.n_end - L.n_base + L.n_tile - 1) / L.n_tile;
   p.num_shards = L.num_shards;
   p.num_tiles = p.tiles_m * p.tiles_n * p.num_shards;
-  p.group_m = L.group_rows > 0 ? (L.group_rows + 255) / 256 : p.tiles_m;
+  p.group_m = L.group_rows > 0 ? (L.group_rows + tile_rows - 1) / tile_rows : p.tiles_m;
   if (p.group_m > p.tiles_m) p.group_m = p.tiles_m;
   if (p.group_m < 1) p.group_m = 1;
   p.status = L.status;
@@ -357,14 +421,16 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStre
   int n = 0;
   const PairEntry* t = pair_table(&n);
   for (int i = 0; i < n; ++i)
-    if (t[i].epi == L.epi && t[i].a_mn == L.a_mn && t[i].b_mn == L.b_mn) fn = t[i].fn;
+    if (t[i].epi == L.epi && t[i].a_mn == L.a_mn && t[i].b_mn == L.b_mn) fn = quad ? t[i].fn4 : t[i].fn;
   if (!fn) {
     if (err) *err = "launch_gemm_pair: no kernel for this epilogue and operand layout";
     return DOMINO_ERR_INVALID_ARG;
   }
-  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  const int cap = quad ? max_quad_clusters : max_clusters;
+  const int clusters = p.num_tiles < cap ? p.num_tiles : cap;
   void* args[] = {&p};
-  cudaError_t st = cudaLaunchKernel(fn, dim3(2 * clusters), dim3(kGemmThreads), args, kPairSmemBytes, stream);
+  cudaError_t st =
+      cudaLaunchKernel(fn, dim3((quad ? 4 : 2) * clusters), dim3(kGemmThreads), args, kPairSmemBytes, stream);
   if (st != cudaSuccess) {
     if (err) *err = std::string("pair gemm launch: ") + cudaGetErrorString(st);
     return DOMINO_ERR_CUDA;

@@ -96,6 +96,23 @@ def test_ragged_shapes(act, partial, schedule):
     _check_full(w, seed=3, schedule=schedule)
 
 
+@pytest.mark.parametrize("rows", [300, 700, 1000])
+@pytest.mark.parametrize("act,partial", [("gelu", "f32"), ("swiglu", "bf16")])
+def test_quad_row_tails(rows, act, partial):
+    # chunks of more than 256 rows run the separate-launch GEMMs as 512-row tiles of two CTA pairs
+    # sharing B: the second pair of the last tile lies partly (300, 1000) or wholly (700) below the
+    # chunk.  Rows past M (a sentinel band after the output) must stay untouched.
+    w = wl.Workload("quad_tail", M=2 * rows, d=512, F=768, P=2, mu=2, act=act, partial=partial)
+    t = wl.generate(w, 11)
+    Ybuf = torch.full((w.M + 64, w.d), 7.0, dtype=torch.bfloat16, device="cuda:0")
+    Y = _run(w, t, "streams", Y=Ybuf[:w.M])
+    f64 = wl.to_float64(t)
+    ref = oracle.mlp_fwd(f64["X"], _oracle_A(w, f64), f64["B"], w.act)
+    err = oracle.max_rel_err(Y.double().cpu().numpy(), ref)
+    assert err <= TOL, f"rows {rows}: {err:.3e}"
+    assert torch.all(Ybuf[w.M:] == 7.0), "wrote past the last row"
+
+
 @pytest.mark.parametrize("schedule", ["streams", "fused"])
 def test_llama_shard_width_tail(schedule):
     # F/P = 1376 as in the Llama-style workload (10.75 tiles of 128), small M and d
