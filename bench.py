@@ -160,7 +160,7 @@ class ClockSampler:
 
 # ------------------------------------------------------ tensor-core probe
 
-def tensor_probe(clk, repeats=3, mmas=1 << 19):
+def tensor_probe(clk, repeats=3, mmas=1 << 17):
     """Best of `repeats` runs of domino_tensor_peak (paired tcgen05 MMAs alone, every co-resident
     2-CTA cluster), with the per-SM rate per clock it measures and the theoretical rate
     SMs x that rate x SM clock, at the clock sampled under the timed region's load and at the

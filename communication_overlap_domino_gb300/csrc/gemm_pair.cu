@@ -299,6 +299,9 @@ struct PairEntry {
   void* fn4;  // 4-CTA clusters (two pairs sharing B)
 };
 
+// The quad form serves the forward GEMMs (both operands K-major), where it measured faster.  The backward
+// GEMMs (MN-major operands) keep 2-CTA clusters: their epilogues or operand layout, not the L2 load, bound
+// them, and the quad form runs on fewer SMs (4-CTA clusters do not tile every GPC).
 const PairEntry* pair_table(int* n) {
   static const PairEntry table[] = {
       {EPI_H_GELU, false, false, pair_ptr<EPI_H_GELU, false, false>(), quad_ptr<EPI_H_GELU, false, false>()},
@@ -307,13 +310,12 @@ const PairEntry* pair_table(int* n) {
       {EPI_H_SWIGLU, false, false, pair_ptr<EPI_H_SWIGLU, false, false>(), quad_ptr<EPI_H_SWIGLU, false, false>()},
       {EPI_Z_F32, false, false, pair_ptr<EPI_Z_F32, false, false>(), quad_ptr<EPI_Z_F32, false, false>()},
       {EPI_Z_BF16, false, false, pair_ptr<EPI_Z_BF16, false, false>(), quad_ptr<EPI_Z_BF16, false, false>()},
-      {EPI_DG_GELU, false, true, pair_ptr<EPI_DG_GELU, false, true>(), quad_ptr<EPI_DG_GELU, false, true>()},
-      {EPI_DG_GELU_TANH, false, true, pair_ptr<EPI_DG_GELU_TANH, false, true>(), quad_ptr<EPI_DG_GELU_TANH, false, true>()},
-      {EPI_DG_IDENTITY, false, true, pair_ptr<EPI_DG_IDENTITY, false, true>(), quad_ptr<EPI_DG_IDENTITY, false, true>()},
-      {EPI_DG_SWIGLU, false, true, pair_ptr<EPI_DG_SWIGLU, false, true>(), quad_ptr<EPI_DG_SWIGLU, false, true>()},
-      {EPI_Z_F32, false, true, pair_ptr<EPI_Z_F32, false, true>(), quad_ptr<EPI_Z_F32, false, true>()},
-      {EPI_Z_BF16, false, true, pair_ptr<EPI_Z_BF16, false, true>(), quad_ptr<EPI_Z_BF16, false, true>()},
-      // the weight gradient dA = dG^T X (both operands MN-major) measured slower in the quad form
+      {EPI_DG_GELU, false, true, pair_ptr<EPI_DG_GELU, false, true>(), nullptr},
+      {EPI_DG_GELU_TANH, false, true, pair_ptr<EPI_DG_GELU_TANH, false, true>(), nullptr},
+      {EPI_DG_IDENTITY, false, true, pair_ptr<EPI_DG_IDENTITY, false, true>(), nullptr},
+      {EPI_DG_SWIGLU, false, true, pair_ptr<EPI_DG_SWIGLU, false, true>(), nullptr},
+      {EPI_Z_F32, false, true, pair_ptr<EPI_Z_F32, false, true>(), nullptr},
+      {EPI_Z_BF16, false, true, pair_ptr<EPI_Z_BF16, false, true>(), nullptr},
       {EPI_Z_BF16, true, true, pair_ptr<EPI_Z_BF16, true, true>(), nullptr},
   };
   *n = static_cast<int>(sizeof(table) / sizeof(table[0]));

@@ -84,9 +84,8 @@ def test_backward_llama_tail_bf16_partials():
 
 
 def test_backward_partial_row_group():
-    # dH runs once over all M with its tiles in row groups of one chunk: chunk rows 640 -> groups of 2
-    # 512-row tiles (two pairs side by side) over 3, so the last group is partial and half of its last
-    # tile lies below M; F_p = 1376 leaves a 96-column tile
+    # dH runs once over all M with its tiles in row groups of one chunk: chunk rows 640 -> groups of 3
+    # 256-row blocks over 5 blocks, so the last group is partial; F_p = 1376 leaves a 96-column tile
     w = wl.Workload("group_tail_bwd", M=1280, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
     _check_full(w, seed=13)
     _check_full(w.with_(act="gelu", partial="f32"), seed=14)
@@ -94,8 +93,9 @@ def test_backward_partial_row_group():
 
 @pytest.mark.parametrize("rows", [300, 700])
 def test_backward_quad_row_tails(rows):
-    # chunks of more than 256 rows run dH and dX as 512-row tiles of two pairs; the second pair of the
-    # last tile lies partly (300) or wholly (700) below the chunk
+    # chunks of more than 256 rows: the forward GEMMs run as 512-row tiles of two pairs, the second
+    # pair of the last tile partly (300) or wholly (700) below the chunk; the backward's 256-row
+    # tiles then cover 600 and 1400 rows with ragged last blocks
     w = wl.Workload("quad_tail_bwd", M=2 * rows, d=512, F=768, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
     _check_full(w, seed=15)
 
