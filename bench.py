@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -189,6 +190,25 @@ def blas_threads():
     except Exception:
         pass
     return os.cpu_count() or 1
+
+
+def cpu_model():
+    """The host CPU's name (x86 'model name', or the Arm implementer/part ids) and its logical core count."""
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+        if m:
+            name = m.group(1).strip()
+        else:
+            imp = re.search(r"^CPU implementer\s*:\s*(\S+)", info, re.M)
+            part = re.search(r"^CPU part\s*:\s*(\S+)", info, re.M)
+            if imp and part:
+                name = f"{os.uname().machine} implementer {imp.group(1)} part {part.group(1)}"
+    except OSError:
+        pass
+    return {"model": name or os.uname().machine, "logical_cores": os.cpu_count()}
 
 
 def oracle_step(w, f64, X, dY):
@@ -559,6 +579,7 @@ def run_ours(args, w, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         rows, dt, fl = oracle_row_sample(w, t, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 5), "unit": "TFLOP/s", "cores": blas_threads(),
+                                "cpu": cpu_model(),
                                 "kind": "oracle",
                                 "sample": f"fp64 oracle {'forward+backward' if w.bwd else 'forward'} on {rows} "
                                           f"of {w.M} rows ({dt:.1f} s; rows are "
@@ -708,7 +729,7 @@ def run_attn(args, w, rank, world, local_rank):
             n += 1
         dt = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": round(w.flops() * n / w.B / dt / 1e12, 5), "unit": "TFLOP/s",
-                                "cores": blas_threads(), "kind": "oracle",
+                                "cores": blas_threads(), "cpu": cpu_model(), "kind": "oracle",
                                 "sample": f"fp64 attention oracle on {n} of {w.B} sequences ({dt:.1f} s)"}
     return line
 
@@ -739,7 +760,8 @@ def run_reference_attn(args, w):
         "dtype": "f64", "data": "synthetic: seeded bf16 values widened to fp64",
         "config": {"workload": w.name, "B": w.B, "S": w.S, "d": w.d, "H": w.H, "dh": w.dh, "P": w.P, "mu": w.mu,
                    "sequences_per_step": 1},
-        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": blas_threads(),
+                         "cpu": cpu_model(), "kind": "oracle",
                          "sample": f"fp64 attention oracle on 1 of {w.B} sequences per step"},
         "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -783,7 +805,8 @@ def run_reference(args, w):
         "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights, bf16 values widened to fp64",
         "config": {"workload": w.name, "M": w.M, "d": w.d, "F": w.F, "P": w.P, "mu": w.mu, "act": w.act,
                    "partials": w.partial, "out_slices": w.slices, "rows_per_step": rows},
-        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": blas_threads(),
+                         "cpu": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
