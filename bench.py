@@ -43,15 +43,23 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("attn.cu", "attn.h", "common.h", "epilogue.cuh", "fused.cu", "gemm.cu", "gemm.h", "gemm_pair.cu", "ptx.cuh",
-                  "shard_sum.cu")
+# The device-code sources each kernel kind is built from: a stored ncu capture of a kernel applies while the
+# hash of its own sources is unchanged.
+_GEMM_SOURCES = ("common.h", "epilogue.cuh", "gemm.cu", "gemm.h", "gemm_pair.cu", "ptx.cuh")
+KERNEL_SOURCES = {
+    "fused": ("common.h", "epilogue.cuh", "fused.cu", "gemm.h", "ptx.cuh"),
+    "gemm1": _GEMM_SOURCES, "gemm2": _GEMM_SOURCES,
+    "bwd_dh": _GEMM_SOURCES, "bwd_dx": _GEMM_SOURCES, "bwd_dw": _GEMM_SOURCES,
+    "shard_sum": ("common.h", "gemm.h", "ptx.cuh", "shard_sum.cu"),
+    "attn": ("attn.cu", "attn.h", "common.h", "ptx.cuh"),
+}
 
 
-def kernel_source_hash():
-    """Hash of the device-code sources, to tell whether a stored ncu capture still applies."""
+def kernel_source_hash(kernel_kind):
+    """Hash of the device-code sources of one kernel kind, to tell whether a stored ncu capture still applies."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "communication_overlap_domino_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel_kind]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -59,17 +67,19 @@ def kernel_source_hash():
 
 
 def ncu_traffic(kernel_kind, workload):
-    """DRAM bytes per launch from a committed ncu capture, if it matches the current sources."""
+    """DRAM bytes per launch from a committed ncu capture, if it matches the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_hash") != kernel_source_hash():
-        return None
     entry = rec.get("kernels", {}).get(f"{workload}/{kernel_kind}")
-    return None if entry is None else entry.get("dram_bytes_per_launch")
+    if entry is None or kernel_kind not in KERNEL_SOURCES:
+        return None
+    if entry.get("source_hash") != kernel_source_hash(kernel_kind):
+        return None
+    return entry.get("dram_bytes_per_launch")
 
 
 # ----------------------------------------------------------------- clocks

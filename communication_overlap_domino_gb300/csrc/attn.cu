@@ -108,6 +108,37 @@ __device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_
   return true;
 }
 
+// Blackwell's packed fp32 pair instructions (one instruction for two lanes' worth of FMA or add) and its
+// three-input maximum: the softmax warps are bound by instruction issue, so these cut their work.  Each
+// lane of the pair is an ordinary IEEE fp32 FMA or add.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -317,7 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fmaxf(__uint_as_float(v0[e]), __uint_as_float(v1[e])));
+            for (int e = 0; e < 32; ++e) mx = max3(mx, __uint_as_float(v0[e]), __uint_as_float(v1[e]));
           }
         }
         const float m_blk = mx * a.scale_log2;
@@ -329,30 +360,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         }
         // pass 2: this thread's 64 probabilities, packed as bf16 pairs
         uint32_t pk[32];
-        float sum = 0.0f;
+        float sum_even = 0.0f, sum_odd = 0.0f;  // the row sum of this thread's even and odd keys
         {
           uint32_t v0[32], v1[32];
           tmem_ld_32x32b_x32(ts + half * 64, v0);
           tmem_ld_32x32b_x32(ts + half * 64 + 32, v1);
           tmem_ld_wait();
+          const float c = a.scale_log2, nm = -m_run;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int k0 = half * 64 + 2 * e, k1 = k0 + 32;
-            float p0 = ex2_approx(fmaf(__uint_as_float(v0[2 * e]), a.scale_log2, -m_run));
-            float p1 = ex2_approx(fmaf(__uint_as_float(v0[2 * e + 1]), a.scale_log2, -m_run));
-            float p2 = ex2_approx(fmaf(__uint_as_float(v1[2 * e]), a.scale_log2, -m_run));
-            float p3 = ex2_approx(fmaf(__uint_as_float(v1[2 * e + 1]), a.scale_log2, -m_run));
+            float x0, x1, x2, x3;
+            fma2(x0, x1, __uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]), c, c, nm, nm);
+            fma2(x2, x3, __uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]), c, c, nm, nm);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
             if (diag) {
               p0 = k0 <= r ? p0 : 0.0f;
               p1 = k0 + 1 <= r ? p1 : 0.0f;
               p2 = k1 <= r ? p2 : 0.0f;
               p3 = k1 + 1 <= r ? p3 : 0.0f;
             }
-            sum += (p0 + p1) + (p2 + p3);
+            add2(sum_even, sum_odd, sum_even, sum_odd, p0, p1);
+            add2(sum_even, sum_odd, sum_even, sum_odd, p2, p3);
             pk[e] = pack_bf16(p0, p1);
             pk[16 + e] = pack_bf16(p2, p3);
           }
         }
+        const float sum = sum_even + sum_odd;
         // P_{j-1} V_{j-1} has landed: the P buffer is free and the output up to date
         if (j > 0) {
           if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
@@ -368,7 +402,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
               tmem_ld_32x32b_x32(to + cc * 32, v);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              for (int e = 0; e < 32; e += 2) {
+                float y0, y1;
+                mul2(y0, y1, __uint_as_float(v[e]), __uint_as_float(v[e + 1]), alpha, alpha);
+                v[e] = __float_as_uint(y0);
+                v[e + 1] = __float_as_uint(y1);
+              }
               tmem_st_32x32b_x32(to + cc * 32, v);
             }
             tmem_st_wait();
@@ -415,16 +454,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o[it.p]) + grow * a.ldo + it.h * kTile +
                                             half * 64);
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        dst[q8] = make_uint4(pack_bf16(__uint_as_float(o0[8 * q8 + 0]) * inv, __uint_as_float(o0[8 * q8 + 1]) * inv),
-                             pack_bf16(__uint_as_float(o0[8 * q8 + 2]) * inv, __uint_as_float(o0[8 * q8 + 3]) * inv),
-                             pack_bf16(__uint_as_float(o0[8 * q8 + 4]) * inv, __uint_as_float(o0[8 * q8 + 5]) * inv),
-                             pack_bf16(__uint_as_float(o0[8 * q8 + 6]) * inv, __uint_as_float(o0[8 * q8 + 7]) * inv));
-        dst[4 + q8] =
-            make_uint4(pack_bf16(__uint_as_float(o1[8 * q8 + 0]) * inv, __uint_as_float(o1[8 * q8 + 1]) * inv),
-                       pack_bf16(__uint_as_float(o1[8 * q8 + 2]) * inv, __uint_as_float(o1[8 * q8 + 3]) * inv),
-                       pack_bf16(__uint_as_float(o1[8 * q8 + 4]) * inv, __uint_as_float(o1[8 * q8 + 5]) * inv),
-                       pack_bf16(__uint_as_float(o1[8 * q8 + 6]) * inv, __uint_as_float(o1[8 * q8 + 7]) * inv));
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const uint32_t* oh = q8 < 4 ? o0 + 8 * q8 : o1 + 8 * (q8 - 4);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2)
+          mul2(y[e], y[e + 1], __uint_as_float(oh[e]), __uint_as_float(oh[e + 1]), inv, inv);
+        dst[q8] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                             pack_bf16(y[6], y[7]));
       }
     }
   }
