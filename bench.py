@@ -82,6 +82,29 @@ def ncu_traffic(kernel_kind, workload):
     return entry.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------------- NVTX
+
+# The timed region is an NVTX push/pop range of this name, so that a profiler's launch list can be limited
+# to it (ncu --nvtx --nvtx-include "timed_region/").
+TIMED_RANGE = "timed_region"
+
+
+def nvtx_push(name):
+    try:
+        import torch
+        torch.cuda.nvtx.range_push(name)
+    except Exception:  # NVTX is optional: the timing does not depend on it
+        pass
+
+
+def nvtx_pop():
+    try:
+        import torch
+        torch.cuda.nvtx.range_pop()
+    except Exception:
+        pass
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -356,12 +379,14 @@ def run_ours(args, w, rank, world, local_rank):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     wall0 = time.perf_counter()
+    nvtx_push(TIMED_RANGE)
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
         step(timed=True)
         ev[i][1].record(stream)
     barrier()
+    nvtx_pop()
     wall = time.perf_counter() - wall0
     clocks.top_up(load)
     clk = clocks.stop()
@@ -638,12 +663,14 @@ def run_attn(args, w, rank, world, local_rank):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    nvtx_push(TIMED_RANGE)
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
         step(timed=True)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    nvtx_pop()
     wall = time.perf_counter() - wall0
     clocks.top_up(load)
     clk = clocks.stop()
