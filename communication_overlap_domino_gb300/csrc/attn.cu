@@ -15,7 +15,8 @@
 //               needed for P_j V_j).
 //   warp 1      tensor-memory allocation; lane 0 issues the MMAs:
 //               S_j = Q K_j^T (M 128, N 128, K 128) into one of two TMEM score
-//               buffers, and O += P_j V_j into the TMEM output accumulator.
+//               buffers, and O += P_j V_j into the TMEM output accumulator,
+//               with P_j (the A operand) read from tensor memory too.
 //               S_{j+1} is issued before P_j V_j, so the next scores are
 //               computed while the softmax of block j runs.
 //   warps 2-9   two threads per query row (warps w and w + 4 read the same
@@ -26,10 +27,10 @@
 //               exp2 domain); then the thread rescales its half of the output
 //               row in tensor memory (after P_{j-1} V_{j-1} has landed) and its
 //               part of the row sum.  Each writes its 64 probabilities
-//               p = exp2(s * c - m) as bf16 into shared memory in the MMA's
-//               operand layout (once P_{j-1} V_{j-1} has finished reading the
-//               buffer).  After the last block the two parts of the row sum are
-//               added through shared memory and O / l is stored as bf16.
+//               p = exp2(s * c - m) as bf16 pairs into the P columns of tensor
+//               memory, its query row's lane (once P_{j-1} V_{j-1} has finished
+//               reading them).  After the last block the two parts of the row
+//               sum are added through shared memory and O / l is stored as bf16.
 //
 // Barriers (all waits bounded, as in the GEMMs): q_full / q_empty, k_full[s] /
 // k_empty[s], v_full[s] / v_empty[s], s_full[b] / s_empty[b], p_full, pv_full,
@@ -54,15 +55,15 @@ constexpr int kSoftmaxWarps = 8;  // consumer barriers count one arrival per sof
 constexpr int kTile = 128;                        // queries per item, keys per block, head width
 constexpr int kSub = kTile * 64 * 2;              // 16 KB: 128 rows x 64 bf16 (one 128-byte-swizzled box)
 constexpr int kQBytes = 2 * kSub;                 // Q tile: dh halves 0-63 and 64-127
-constexpr int kPBytes = 2 * kSub;                 // P tile: key halves 0-63 and 64-127
 constexpr int kKBytes = 2 * kSub;                 // K tile: dh halves
 constexpr int kVBytes = 2 * kSub;                 // V tile: 2 blocks of 64 keys x (2 boxes of 64 dh x 64 keys)
 constexpr int kSlots = 2;                         // slots of the K ring and of the V ring
 constexpr int kLsumBytes = 2 * 2 * kTile * 4;     // row-sum halves, double-buffered by item
-constexpr int kAttnSmemBytes = kQBytes + kPBytes + kSlots * (kKBytes + kVBytes) + kLsumBytes + 1024 + 256;
+constexpr int kAttnSmemBytes = kQBytes + kSlots * (kKBytes + kVBytes) + kLsumBytes + 1024 + 256;
 static_assert(kAttnSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kAttnTmemCols = 512;           // S buffers at 0 and 128, the output O at 256
+constexpr uint32_t kAttnTmemCols = 512;           // S buffers at 0 and 128, the output O at 256, P at 384
 constexpr uint32_t kOCol = 256;
+constexpr uint32_t kPCol = 384;                   // P as bf16 pairs: 64 columns, key 2c and 2c + 1 in column c
 constexpr float kRescaleLog2 = 8.0f;              // lazy rescaling threshold: the maximum may lag by 2^8
 
 struct AttnItem {
@@ -119,6 +120,18 @@ __device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_
   return true;
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulation: the A operand (M rows in lanes, K along
+// the columns, two bf16 per 32-bit column) is read from tensor memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Blackwell's packed fp32 pair instructions (one instruction for two lanes' worth of FMA or add) and its
 // three-input maximum: the softmax warps are bound by instruction issue, so these cut their work.  Each
 // lane of the pair is an ordinary IEEE fp32 FMA or add.
@@ -159,8 +172,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem;
-  uint8_t* sp = sq + kQBytes;
-  uint8_t* sk = sp + kPBytes;             // K ring: kSlots x 32 KB
+  uint8_t* sk = sq + kQBytes;             // K ring: kSlots x 32 KB
   uint8_t* sv = sk + kSlots * kKBytes;    // V ring: kSlots x 32 KB
   float* lsum = reinterpret_cast<float*>(sv + kSlots * kVBytes);  // [2 buffers][2 halves][128 rows]
   uint64_t* bars = reinterpret_cast<uint64_t*>(lsum + 2 * 2 * kTile);
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
     uint32_t q_phase = 0, kv_count = 0, s_count = 0, p_phase = 0, o_phase = 0;
-    const uint32_t qa = smem_u32(sq), pa = smem_u32(sp);
+    const uint32_t qa = smem_u32(sq);
     bool ok = true;
     for (int k = 0, t = attn_round_item(0); t < a.num_items && ok && !*abort_flag; t = attn_round_item(++k)) {
       const AttnItem it = attn_item(a, t);
@@ -307,10 +319,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         tc_fence_after_sync();
         const uint32_t va = smem_u32(sv + st * kVBytes);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = smem_desc_k128(pa + (k >> 2) * kSub) + 2 * (k & 3);
+        for (int k = 0; k < 8; ++k) {  // 16 keys per step: 8 columns of P in tensor memory
           const uint64_t bd = smem_desc_mn128(va + (k >> 2) * kSub) + (2048 >> 4) * (k & 3);
-          mma_bf16_ss(tmem_base + kOCol, ad, bd, idesc_pv, (j | k) != 0 ? 1u : 0u);
+          mma_bf16_ts(tmem_base + kOCol, tmem_base + kPCol + 8 * k, bd, idesc_pv, (j | k) != 0 ? 1u : 0u);
         }
         mma_commit(pv_full);
         mma_commit(&v_empty[st]);
@@ -438,14 +449,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
             tmem_st_wait();
           }
         }
-        uint8_t* row = sp + half * kSub + r * 128;
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {  // 16-byte chunk c16 holds keys half*64 + 8 c16 .. + 8
-          const int e0 = (c16 & 3) * 4 + (c16 >> 2) * 16;
-          const uint4 w = make_uint4(pk[e0], pk[e0 + 1], pk[e0 + 2], pk[e0 + 3]);
-          *reinterpret_cast<uint4*>(row + ((c16 ^ (r & 7)) << 4)) = w;
-        }
-        fence_proxy_async_shared();  // P is read by the tensor cores (async proxy)
+        // this thread's 64 keys as 32 bf16 pairs: pk[c] holds keys half * 64 + 2c, + 1 -> P column half * 32 + c
+        tmem_st_32x32b_x32(tmem_base + lane_off + kPCol + half * 32, pk);
+        tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();  // the warp's scores are read and its P stored: one arrival per warp
         if (lane == 0) {
