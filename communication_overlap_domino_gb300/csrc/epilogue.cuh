@@ -45,6 +45,25 @@ __device__ __forceinline__ float erf_as(float z) {
 }
 
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erf_as(x * 0.70710678118654752f)); }
+// gelu_erf of two values with the fp32 pair instructions: the same operations in the same order, so the
+// results equal gelu_erf's; the reciprocal and the exponential stay per value.
+__device__ __forceinline__ void gelu_erf2(float& h0, float& h1, float x0, float x1) {
+  float z0, z1, d0, d1, p0, p1, q0, q1, s0, s1, r0, r1;
+  mul2(z0, z1, x0, x1, 0.70710678118654752f, 0.70710678118654752f);
+  const float a0 = fabsf(z0), a1 = fabsf(z1);
+  fma2(d0, d1, 0.3275911f, 0.3275911f, a0, a1, 1.0f, 1.0f);
+  const float t0 = __fdividef(1.0f, d0), t1 = __fdividef(1.0f, d1);
+  fma2(p0, p1, t0, t1, 1.061405429f, 1.061405429f, -1.453152027f, -1.453152027f);
+  fma2(p0, p1, t0, t1, p0, p1, 1.421413741f, 1.421413741f);
+  fma2(p0, p1, t0, t1, p0, p1, -0.284496736f, -0.284496736f);
+  fma2(p0, p1, t0, t1, p0, p1, 0.254829592f, 0.254829592f);
+  mul2(p0, p1, p0, p1, t0, t1);
+  mul2(s0, s1, -a0, -a1, a0, a1);
+  fma2(r0, r1, -p0, -p1, __expf(s0), __expf(s1), 1.0f, 1.0f);
+  add2(q0, q1, 1.0f, 1.0f, copysignf(r0, z0), copysignf(r1, z1));
+  mul2(h0, h1, 0.5f, 0.5f, x0, x1);
+  mul2(h0, h1, h0, h1, q0, q1);
+}
 __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
 }
@@ -237,8 +256,13 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, uint32_t tacc, 
     if constexpr (EPI != EPI_Z_F32 && EPI != EPI_Z_BF16) {
       if (row_ok && e.aux != nullptr)
         store_row_bf16(static_cast<__nv_bfloat16*>(e.aux) + orow * e.ld_aux + col, h, n);
+      if constexpr (EPI == EPI_H_GELU) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(h[j]);
+        for (int j = 0; j < 32; j += 2) gelu_erf2(h[j], h[j + 1], h[j], h[j + 1]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[j] = activate<EPI>(h[j]);
+      }
     }
   }
 }
