@@ -124,6 +124,8 @@ SIGNATURES = [
     ("domino_mlp_workspace_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc), ctypes.c_int32]),
     ("domino_mlp_saved_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc)]),
     ("domino_mlp_fwd", ctypes.c_int, [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    ("domino_mlp_fwd_partials", ctypes.c_int,
+     [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VPP, _VPP, _VP, _VP, ctypes.c_size_t, _VP]),
     ("domino_mlp_bwd", ctypes.c_int,
      [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP, _VP, _VPP, _VPP, _VP, ctypes.c_size_t, _VP]),
     ("domino_shard_sum", ctypes.c_int,
@@ -134,6 +136,7 @@ SIGNATURES = [
     ("domino_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("domino_last_error", ctypes.c_char_p, []),
     ("domino_mlp_fwd_noalloc", ctypes.c_int, [ctypes.POINTER(MlpDesc), _VP, _VPP, _VPP, _VP, _VP]),
+    ("domino_mlp_fwd_noalloc_status", ctypes.c_int, [_VP, _VPP]),
     ("domino_kernel_times", ctypes.c_int32, [ctypes.POINTER(KernelTime), ctypes.c_int32]),
     ("domino_kernel_times_reset", None, []),
     ("domino_mlp_plan", ctypes.c_int, [ctypes.POINTER(MlpDesc), ctypes.POINTER(PlanHw), ctypes.POINTER(Plan)]),
@@ -151,10 +154,11 @@ def lib() -> ctypes.CDLL:
     """Loads the library (raises if it has not been built)."""
     global _LIB
     if _LIB is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+        path = os.environ.get("DOMINO_LIB_PATH") or LIB_PATH  # another build of the same library, if given
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
                                "(this package has no CPU or PyTorch fallback)")
-        handle = ctypes.CDLL(LIB_PATH)
+        handle = ctypes.CDLL(path)
         for name, res, args in SIGNATURES:
             fn = getattr(handle, name)
             fn.restype = res
@@ -273,6 +277,38 @@ def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, par
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "domino_mlp_fwd")
     return Y
+
+
+def mlp_fwd_partials(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str,
+                     out_slices: int = 1, schedule: str = "streams", Z_shards=None, piece_events=None, saved=None,
+                     workspace=None, stream=None, kernel_times: bool = False, timeout_ns: int = 0,
+                     pair_cta: bool = True):
+    """domino_mlp_fwd_partials on torch tensors: the row-parallel partials of every shard, not summed.
+    Returns Z_shards (P tensors [M, d], fp32 or bf16 as `partial`).  piece_events: None or mu * out_slices
+    torch.cuda.Event objects, each recorded when its (chunk, slice) piece of every partial is written."""
+    torch = _torch()
+    M, d = X.shape
+    P = len(A_shards)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
+    if Z_shards is None:
+        dt = torch.float32 if partial == "f32" else torch.bfloat16
+        Z_shards = [torch.empty((M, d), dtype=dt, device=X.device) for _ in range(P)]
+    need = workspace_size(desc)
+    if workspace is None:
+        workspace = _workspace(max(need, 256), X.device)
+    events = None
+    if piece_events is not None:
+        for e in piece_events:  # torch creates the CUDA event lazily, on first record
+            if e.cuda_event == 0:
+                e.record()
+        events = _ptr_array([e.cuda_event for e in piece_events])
+    st = lib().domino_mlp_fwd_partials(
+        ctypes.byref(desc), X.data_ptr(), _ptr_array([a.data_ptr() for a in A_shards]),
+        _ptr_array([b.data_ptr() for b in B_shards]), _ptr_array([z.data_ptr() for z in Z_shards]), events,
+        saved.data_ptr() if saved is not None else None, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "domino_mlp_fwd_partials")
+    return Z_shards
 
 
 def mlp_bwd(X, A_shards: List, B_shards: List, dY, saved, *, F: int, mu: int, act: str, partial: str,
@@ -418,6 +454,14 @@ def mlp_fwd_noalloc(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: 
         _ptr_array([b.data_ptr() for b in B_shards]), Y.data_ptr(), _stream_handle(stream))
     _check(st, "domino_mlp_fwd_noalloc")
     return Y
+
+
+def mlp_fwd_noalloc_status(stream=None):
+    """domino_mlp_fwd_noalloc_status: synchronises, returns and clears the device status of the last
+    no-alloc forward (0 = OK), and the device address of the fixed scratch array's header."""
+    header = ctypes.c_void_p()
+    st = int(lib().domino_mlp_fwd_noalloc_status(_stream_handle(stream), ctypes.byref(header)))
+    return st, int(header.value or 0)
 
 
 def shard_sum(partials: List, Y, *, stream=None):

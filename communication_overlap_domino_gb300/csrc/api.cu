@@ -53,7 +53,6 @@ struct DeviceState {
   int num_sms = 0;
   int fused_max_ctas = 0;     // co-resident CTAs of the fused kernel (cooperative launch limit)
   int pair_max_clusters = 0;  // co-resident 2-CTA clusters of the paired GEMM
-  int quad_max_clusters = 0;  // co-resident 4-CTA clusters of its quad form (0: not used)
   int fused_pair_clusters = 0;  // co-resident 2-CTA clusters of the paired fused kernel (0: not usable)
   cudaStream_t reduce_stream = nullptr;
   cudaEvent_t ev_fork = nullptr;
@@ -92,7 +91,7 @@ domino_status_t device_state(DeviceState** out) {
     }
     e = cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = prepare_gemm_kernels();
-    if (e == cudaSuccess) e = prepare_pair_kernels(&ds.pair_max_clusters, &ds.quad_max_clusters);
+    if (e == cudaSuccess) e = prepare_pair_kernels(&ds.pair_max_clusters);
     if (e == cudaSuccess) e = prepare_attn_kernel();
     int per_sm = 0;
     if (e == cudaSuccess) e = prepare_fused_kernels(&per_sm, &ds.fused_pair_clusters);
@@ -146,6 +145,8 @@ domino_status_t check_desc(const domino_mlp_desc_t* desc, Shape* s) {
     return fail(DOMINO_ERR_ALIGNMENT, "d, F/P and d/out_slices must be multiples of 8 (16-byte rows)");
   const int64_t lim = int64_t(1) << 30;
   if (d.M >= lim || d.d >= lim || Fp >= lim) return fail(DOMINO_ERR_UNSUPPORTED, "dimension too large");
+  // the shard-sum counts 16-byte vectors of Y (8 elements) with 32-bit indices
+  if (d.M * (d.d / 8) >= (int64_t(1) << 32)) return fail(DOMINO_ERR_UNSUPPORTED, "M * d / 8 must be below 2^32");
   s->M = d.M;
   s->d = d.d;
   s->F = d.F;
@@ -247,7 +248,7 @@ domino_status_t timed(Timer& T, cudaStream_t st, int32_t stream_id, int32_t kind
 
 // One grouped GEMM launch, as one-CTA tiles or as paired-CTA clusters.
 domino_status_t run_gemm(const GemmLaunch& L, const DeviceState* ds, bool pair, cudaStream_t st, std::string* err) {
-  return pair ? launch_gemm_pair(L, ds->pair_max_clusters, ds->quad_max_clusters, st, err)
+  return pair ? launch_gemm_pair(L, ds->pair_max_clusters, st, err)
               : launch_gemm(L, ds->num_sms, st, err);
 }
 
@@ -274,6 +275,8 @@ struct FwdSeq {
   void* pre[kMaxShards] = {};
   void* Z[kMaxShards] = {};
   cudaEvent_t* ev_piece = nullptr;  // mu * S events, one per piece
+  bool reduce = true;               // false: the partials are the result (no shard-sum)
+  void* const* user_events = nullptr;  // partials only: the caller's piece events (nullable)
 
   // H and the pre-activations go to `saved` when it is given, else H to the workspace.
   void bind(uint8_t* ws, const WsLayout& W, void* saved) {
@@ -353,6 +356,16 @@ struct FwdSeq {
       L.timeout_ns = tmo;
       st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return run_gemm(L, ds, pair, s0, err); });
       if (st != DOMINO_OK) return st;
+      if (!reduce) {
+        if (user_events) {
+          cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(user_events[k * s.S + sl]), s0);
+          if (e != cudaSuccess) {
+            if (err) *err = std::string("piece event record: ") + cudaGetErrorString(e);
+            return DOMINO_ERR_CUDA;
+          }
+        }
+        continue;
+      }
       st = shard_sum_piece(k, sl, err);
       if (st != DOMINO_OK) return st;
     }
@@ -797,21 +810,32 @@ size_t domino_mlp_saved_size(const domino_mlp_desc_t* desc) {
   return saved_shard_bytes(s) * s.P;
 }
 
-domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
-                               const void* const* B_shards, void* Y, void* saved, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// The forward pass of domino_mlp_fwd (Z_out == NULL: partials in the workspace, summed into Y) and of
+// domino_mlp_fwd_partials (Z_out != NULL: the partials, written to the caller's buffers, are the result).
+domino_status_t mlp_fwd_impl(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                             const void* const* B_shards, void* Y, void* const* Z_out, void* const* piece_events,
+                             void* saved, void* workspace, size_t workspace_bytes, void* stream) {
   Shape s;
   domino_status_t st = check_desc(desc, &s);
   if (st != DOMINO_OK) return st;
+  const bool reduce = Z_out == nullptr;
   if (s.M == 0) return DOMINO_OK;  // an empty batch reads and writes nothing; X and Y may be NULL
-  if (!X || !A_shards || !B_shards || !Y || !workspace)
-    return fail(DOMINO_ERR_INVALID_ARG, "X, A_shards, B_shards, Y and workspace must be non-NULL");
+  if (!X || !A_shards || !B_shards || (reduce && !Y) || !workspace)
+    return fail(DOMINO_ERR_INVALID_ARG, reduce ? "X, A_shards, B_shards, Y and workspace must be non-NULL"
+                                               : "X, A_shards, B_shards, Z_shards and workspace must be non-NULL");
   for (int p = 0; p < s.P; ++p) {
-    if (!A_shards[p] || !B_shards[p]) return fail(DOMINO_ERR_INVALID_ARG, "NULL shard pointer");
-    if (!aligned16(A_shards[p]) || !aligned16(B_shards[p]))
+    if (!A_shards[p] || !B_shards[p] || (!reduce && !Z_out[p]))
+      return fail(DOMINO_ERR_INVALID_ARG, "NULL shard pointer");
+    if (!aligned16(A_shards[p]) || !aligned16(B_shards[p]) || (!reduce && !aligned16(Z_out[p])))
       return fail(DOMINO_ERR_ALIGNMENT, "shard pointers must be 16-byte aligned");
   }
-  if (!aligned16(X) || !aligned16(Y) || (saved && !aligned16(saved)) ||
+  if (!reduce && piece_events)
+    for (int i = 0; i < s.mu * s.S; ++i)
+      if (!piece_events[i]) return fail(DOMINO_ERR_INVALID_ARG, "NULL piece event");
+  if (!aligned16(X) || (reduce && !aligned16(Y)) || (saved && !aligned16(saved)) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(DOMINO_ERR_ALIGNMENT, "X, Y, saved must be 16-byte and workspace 256-byte aligned");
   const WsLayout W = ws_layout(s, false);
@@ -848,6 +872,10 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
   f.Y = Y;
   f.ev_piece = ds->ev_piece;
   f.bind(ws, W, saved);
+  f.reduce = reduce;
+  f.user_events = piece_events;
+  if (!reduce)
+    for (int p = 0; p < s.P; ++p) f.Z[p] = Z_out[p];
   static const int kEpiOfAct[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_SWIGLU, EPI_H_IDENTITY};
   std::string err;
 
@@ -862,7 +890,8 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
       F.aux[p] = f.pre[p];
       F.Z[p] = f.Z[p];
     }
-    F.Y = Y;
+    F.Y = reduce ? Y : nullptr;
+    F.reduce = reduce;
     F.sync = reinterpret_cast<uint32_t*>(ws + W.sync_off);
     F.timeline = reinterpret_cast<uint64_t*>(ws + kTimelineOff);
     F.M = s.M;
@@ -889,6 +918,11 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
       return r;
     });
     if (st != DOMINO_OK) return fail(st, err);
+    if (!reduce && piece_events)  // one launch: every piece is complete when it ends
+      for (int i = 0; i < s.mu * s.S; ++i) {
+        cudaError_t e2 = cudaEventRecord(static_cast<cudaEvent_t>(piece_events[i]), s0);
+        if (e2 != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("piece event record: ") + cudaGetErrorString(e2));
+      }
     return DOMINO_OK;
   }
 
@@ -899,6 +933,23 @@ domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, con
   }
   join_streams(ds, s0, sr);
   return DOMINO_OK;
+}
+}  // namespace
+
+extern "C" {
+
+domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                               const void* const* B_shards, void* Y, void* saved, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return mlp_fwd_impl(desc, X, A_shards, B_shards, Y, nullptr, nullptr, saved, workspace, workspace_bytes, stream);
+}
+
+domino_status_t domino_mlp_fwd_partials(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
+                                        const void* const* B_shards, void* const* Z_shards, void* const* piece_events,
+                                        void* saved, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!Z_shards) return fail(DOMINO_ERR_INVALID_ARG, "Z_shards must be non-NULL");
+  return mlp_fwd_impl(desc, X, A_shards, B_shards, nullptr, Z_shards, piece_events, saved, workspace,
+                      workspace_bytes, stream);
 }
 
 domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,

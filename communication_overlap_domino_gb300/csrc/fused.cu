@@ -860,7 +860,7 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pai
   f.tiles_a = L.P * f.tiles_m * f.tiles_n1;
   f.tiles_b = L.P * f.tiles_m * f.tiles_n2;
   f.num_gemm_tiles = L.mu * (f.tiles_a + f.tiles_b);
-  f.num_red_items = L.mu * f.tiles_m * f.tiles_n2;
+  f.num_red_items = L.reduce ? L.mu * f.tiles_m * f.tiles_n2 : 0;
   f.kb1 = static_cast<int32_t>((L.d + kBK - 1) / kBK);
   f.kb2 = static_cast<int32_t>((Fp + kBK - 1) / kBK);
   f.tiles_m2 = (f.tiles_m + 1) / 2;

@@ -46,11 +46,9 @@ struct GemmLaunch {
 };
 
 cudaError_t prepare_gemm_kernels();
-cudaError_t prepare_pair_kernels(int* max_clusters, int* max_quad_clusters);
-// Paired-CTA GEMM (gemm_pair.cu): same launch description, 2-CTA clusters, or
-// 4-CTA clusters (two pairs sharing B by multicast) when max_quad_clusters > 0
-// and the launch has more than 256 rows.
-domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, int max_quad_clusters, cudaStream_t stream,
+cudaError_t prepare_pair_kernels(int* max_clusters);
+// Paired-CTA GEMM (gemm_pair.cu): same launch description, 2-CTA clusters.
+domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStream_t stream,
                                  std::string* err);
 bool encode_bf16_sw128(CUtensorMap* map, const Operand2D& op, int box_rows, std::string* err);
 // TMA store map of a row-major output: box 32 rows x box_cols, 128-byte rows
@@ -80,7 +78,8 @@ struct FusedLaunch {
   int mu = 1, P = 1;
   int epi_a = EPI_H_GELU;
   bool partial_f32 = true;
-  bool pair = false;  // paired-CTA tiles (2-CTA clusters)
+  bool pair = false;    // paired-CTA tiles (2-CTA clusters)
+  bool reduce = true;   // false: the partials are the result (no shard-sum pieces; Y unused)
   DeviceStatus* status = nullptr;
   uint64_t timeout_ns = 0;
 };

@@ -18,15 +18,7 @@
 //   tempty[a] in the even CTA, count 256: its own 128 epilogue threads plus the
 //            odd CTA's 128, which arrive remotely once they have read their rows.
 // Tensor memory is allocated collectively by warp 1 of both CTAs.
-//
-// Quad form (4-CTA clusters, two pairs on one 512 x 256 tile): the two pairs
-// share the tile's B column block, so each CTA loads only half of its 128 B
-// rows (a 64-row box) and multicasts it to the CTA in the same position of the
-// other pair.  Per SM this cuts the operand bytes loaded from L2 per MMA by a
-// quarter (A 16 KB + B 8 KB per stage instead of 16 + 16).  Each pair leader's
-// full[s] still receives 64 KB per stage (its pair's A halves, and its B halves
-// from both pairs' loads); empty[s] in every CTA counts one MMA completion from
-// each pair leader, since a stage slot is written by both pairs' producers.
+
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -52,7 +44,7 @@ static_assert(kPairSmemBytes <= 232448, "shared memory budget");
 constexpr int kPairAccBufs = 2;
 constexpr uint32_t kPairTmemCols = 256 * kPairAccBufs;
 
-// Tile t -> (shard, cluster row block (256 rows per pair, 512 per quad), column block).  Rows go in groups of
+// Tile t -> (shard, pair row block (256 rows), column block).  Rows go in groups of
 // group_m blocks; within a group: for each shard, for each column block, the
 // group's row blocks.  Consecutive tiles (run at the same time by the clusters)
 // share a column block of B; a group's rows of A stay in L2 while every shard
@@ -72,9 +64,9 @@ __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int
   mb2 = g * G + (r2 - nb * gm);
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool QUAD>
+template <int EPI, bool A_MN, bool B_MN>
 __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
-  constexpr int kCluster = QUAD ? 4 : 2;
+  constexpr int kCluster = 2;
   constexpr int kTileRows = 128 * kCluster;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -99,7 +91,7 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], QUAD ? 2 : 1);
+      mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -129,9 +121,6 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), leader_rank);  // the pair leader's full[0]
-    // quad: this CTA's 64-row share of the B rows it and its counterpart in the other pair use
-    const uint16_t b_mask = static_cast<uint16_t>(0x5u << (rank & 1u));
-    const int b_part = static_cast<int>(rank >> 1);
     for (int t = cluster_id; t < num_tiles && !*abort_flag; t += num_clusters) {
       int shard, mbx, nb;
       pair_tile_coords(p, t, shard, mbx, nb);
@@ -155,13 +144,7 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
         } else {
           tma_load_2d_pair(sa, &p.map_a[shard], bar, k0, ya);
         }
-        if constexpr (QUAD) {
-          // 64 B rows (8 KB; a K-major map has 64-row boxes here) to both CTAs of this position
-          if constexpr (B_MN)
-            tma_load_2d_pair_multicast(sb + 8192 * b_part, mapb, bar, yb + 64 * b_part, k0, b_mask);
-          else
-            tma_load_2d_pair_multicast(sb + 8192 * b_part, mapb, bar, k0, yb + 64 * b_part, b_mask);
-        } else if constexpr (B_MN) {
+        if constexpr (B_MN) {
           tma_load_2d_pair(sb, mapb, bar, yb, k0);
           tma_load_2d_pair(sb + 8192, mapb, bar, yb + 64, k0);
         } else {
@@ -177,9 +160,9 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
       if (!ok) break;
     }
     // Drain: the even CTA waits until every load counted on its barriers (its
-    // own, the odd CTA's and, in the quad form, the other pair's multicasts into
-    // this pair) has landed; loads into the odd CTA complete no later than the
-    // cluster barrier below, which the even CTA reaches only after this.
+    // own and the odd CTA's) has landed; loads into the odd CTA complete no
+    // later than the cluster barrier below, which the even CTA reaches only
+    // after this.
     if (leader) {
       for (int s = 0; s < kPairStages; ++s) {
         if (issued_mask & (1u << s)) {
@@ -215,8 +198,8 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
           mma_bf16_ss_pair(d_tmem, adesc + kAdvA * k, bdesc + kAdvB * k, idesc, (kb | k) != 0 ? 1u : 0u);
-        // frees the stage in every CTA that wrote it: the pair, and in the quad form the other pair too
-        mma_commit_pair_multicast(&empty_bar[stage], QUAD ? 0xF : pair_mask);
+        // frees the stage in both CTAs of the pair
+        mma_commit_pair_multicast(&empty_bar[stage], pair_mask);
         if (++stage == kPairStages) {
           stage = 0;
           phase ^= 1;
@@ -274,49 +257,35 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmParams p) {
-  gemm_pair_body<EPI, A_MN, B_MN, false>(p);
-}
-
-template <int EPI, bool A_MN, bool B_MN>
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kGemmThreads, 1)
-    gemm_quad_kernel(const __grid_constant__ GemmParams p) {
-  gemm_pair_body<EPI, A_MN, B_MN, true>(p);
+  gemm_pair_body<EPI, A_MN, B_MN>(p);
 }
 
 template <int EPI, bool A_MN, bool B_MN>
 void* pair_ptr() {
   return reinterpret_cast<void*>(&gemm_pair_kernel<EPI, A_MN, B_MN>);
 }
-template <int EPI, bool A_MN, bool B_MN>
-void* quad_ptr() {
-  return reinterpret_cast<void*>(&gemm_quad_kernel<EPI, A_MN, B_MN>);
-}
 
 struct PairEntry {
   int epi;
   bool a_mn, b_mn;
-  void* fn;   // 2-CTA clusters
-  void* fn4;  // 4-CTA clusters (two pairs sharing B)
+  void* fn;  // 2-CTA clusters
 };
 
-// The quad form serves the forward GEMMs (both operands K-major), where it measured faster.  The backward
-// GEMMs (MN-major operands) keep 2-CTA clusters: their epilogues or operand layout, not the L2 load, bound
-// them, and the quad form runs on fewer SMs (4-CTA clusters do not tile every GPC).
 const PairEntry* pair_table(int* n) {
   static const PairEntry table[] = {
-      {EPI_H_GELU, false, false, pair_ptr<EPI_H_GELU, false, false>(), quad_ptr<EPI_H_GELU, false, false>()},
-      {EPI_H_GELU_TANH, false, false, pair_ptr<EPI_H_GELU_TANH, false, false>(), quad_ptr<EPI_H_GELU_TANH, false, false>()},
-      {EPI_H_IDENTITY, false, false, pair_ptr<EPI_H_IDENTITY, false, false>(), quad_ptr<EPI_H_IDENTITY, false, false>()},
-      {EPI_H_SWIGLU, false, false, pair_ptr<EPI_H_SWIGLU, false, false>(), quad_ptr<EPI_H_SWIGLU, false, false>()},
-      {EPI_Z_F32, false, false, pair_ptr<EPI_Z_F32, false, false>(), quad_ptr<EPI_Z_F32, false, false>()},
-      {EPI_Z_BF16, false, false, pair_ptr<EPI_Z_BF16, false, false>(), quad_ptr<EPI_Z_BF16, false, false>()},
-      {EPI_DG_GELU, false, true, pair_ptr<EPI_DG_GELU, false, true>(), nullptr},
-      {EPI_DG_GELU_TANH, false, true, pair_ptr<EPI_DG_GELU_TANH, false, true>(), nullptr},
-      {EPI_DG_IDENTITY, false, true, pair_ptr<EPI_DG_IDENTITY, false, true>(), nullptr},
-      {EPI_DG_SWIGLU, false, true, pair_ptr<EPI_DG_SWIGLU, false, true>(), nullptr},
-      {EPI_Z_F32, false, true, pair_ptr<EPI_Z_F32, false, true>(), nullptr},
-      {EPI_Z_BF16, false, true, pair_ptr<EPI_Z_BF16, false, true>(), nullptr},
-      {EPI_Z_BF16, true, true, pair_ptr<EPI_Z_BF16, true, true>(), nullptr},
+      {EPI_H_GELU, false, false, pair_ptr<EPI_H_GELU, false, false>()},
+      {EPI_H_GELU_TANH, false, false, pair_ptr<EPI_H_GELU_TANH, false, false>()},
+      {EPI_H_IDENTITY, false, false, pair_ptr<EPI_H_IDENTITY, false, false>()},
+      {EPI_H_SWIGLU, false, false, pair_ptr<EPI_H_SWIGLU, false, false>()},
+      {EPI_Z_F32, false, false, pair_ptr<EPI_Z_F32, false, false>()},
+      {EPI_Z_BF16, false, false, pair_ptr<EPI_Z_BF16, false, false>()},
+      {EPI_DG_GELU, false, true, pair_ptr<EPI_DG_GELU, false, true>()},
+      {EPI_DG_GELU_TANH, false, true, pair_ptr<EPI_DG_GELU_TANH, false, true>()},
+      {EPI_DG_IDENTITY, false, true, pair_ptr<EPI_DG_IDENTITY, false, true>()},
+      {EPI_DG_SWIGLU, false, true, pair_ptr<EPI_DG_SWIGLU, false, true>()},
+      {EPI_Z_F32, false, true, pair_ptr<EPI_Z_F32, false, true>()},
+      {EPI_Z_BF16, false, true, pair_ptr<EPI_Z_BF16, false, true>()},
+      {EPI_Z_BF16, true, true, pair_ptr<EPI_Z_BF16, true, true>()},
   };
   *n = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;
@@ -325,40 +294,29 @@ const PairEntry* pair_table(int* n) {
 }  // namespace
 
 // Sets the shared-memory attribute of every paired kernel and returns how many
-// 2-CTA clusters, and 4-CTA clusters of the quad form, can be resident at once
-// (the persistent grid sizes): the GPU's SMs need not group evenly.  A device
-// that cannot hold a 4-CTA cluster of these kernels gets 0 and the 2-CTA form.
-cudaError_t prepare_pair_kernels(int* max_clusters, int* max_quad_clusters) {
+// 2-CTA clusters can be resident at once (the persistent grid size): the GPU's
+// SMs need not group evenly.
+cudaError_t prepare_pair_kernels(int* max_clusters) {
   int n = 0;
   const PairEntry* t = pair_table(&n);
-  int best = 1 << 30, best4 = 1 << 30;
+  int best = 1 << 30;
   for (int i = 0; i < n; ++i) {
-    for (int form = 0; form < 2; ++form) {
-      void* fn = form ? t[i].fn4 : t[i].fn;
-      if (fn == nullptr) continue;
-      cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
-      if (st != cudaSuccess) return st;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(form ? 4 * 256 : 2 * 512);
-      cfg.blockDim = dim3(kGemmThreads);
-      cfg.dynamicSmemBytes = kPairSmemBytes;
-      int clusters = 0;
-      st = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
-      if (st != cudaSuccess) {
-        if (!form) return st;
-        (void)cudaGetLastError();
-        clusters = 0;
-      }
-      int& b = form ? best4 : best;
-      b = clusters < b ? clusters : b;
-    }
+    cudaError_t st = cudaFuncSetAttribute(t[i].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+    if (st != cudaSuccess) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 512);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    int clusters = 0;
+    st = cudaOccupancyMaxActiveClusters(&clusters, t[i].fn, &cfg);
+    if (st != cudaSuccess) return st;
+    best = clusters < best ? clusters : best;
   }
   *max_clusters = best;
-  *max_quad_clusters = best4;
   return cudaSuccess;
 }
 
-domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, int max_quad_clusters, cudaStream_t stream,
+domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStream_t stream,
                                  std::string* err) {
   GemmParams p;
   memset(&p, 0, sizeof p);
@@ -366,19 +324,9 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, int max_
     if (err) *err = "launch_gemm_pair: bad shard count";
     return DOMINO_ERR_INVALID_ARG;
   }
-  // quad form when there are at least two 256-row blocks to put side by side (and a quad kernel for this layout)
-  bool quad = max_quad_clusters > 0 && L.rows > 256;
-  if (quad) {
-    int n = 0;
-    const PairEntry* t = pair_table(&n);
-    bool have = false;
-    for (int i = 0; i < n; ++i)
-      if (t[i].epi == L.epi && t[i].a_mn == L.a_mn && t[i].b_mn == L.b_mn) have = t[i].fn4 != nullptr;
-    quad = have;
-  }
-  const int tile_rows = quad ? 512 : 256;
+  const int tile_rows = 256;
   const int a_box = L.a_mn ? kBK : 128;
-  const int b_box = L.b_mn ? kBK : (quad ? 64 : 128);
+  const int b_box = L.b_mn ? kBK : 128;
   for (int s = 0; s < L.num_shards; ++s) {
     if (!encode_bf16_sw128(&p.map_a[s], L.a[s], a_box, err)) return DOMINO_ERR_CUDA;
     if (!encode_bf16_sw128(&p.map_b0[s], L.b0[s], b_box, err)) return DOMINO_ERR_CUDA;
@@ -423,16 +371,15 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, int max_
   int n = 0;
   const PairEntry* t = pair_table(&n);
   for (int i = 0; i < n; ++i)
-    if (t[i].epi == L.epi && t[i].a_mn == L.a_mn && t[i].b_mn == L.b_mn) fn = quad ? t[i].fn4 : t[i].fn;
+    if (t[i].epi == L.epi && t[i].a_mn == L.a_mn && t[i].b_mn == L.b_mn) fn = t[i].fn;
   if (!fn) {
     if (err) *err = "launch_gemm_pair: no kernel for this epilogue and operand layout";
     return DOMINO_ERR_INVALID_ARG;
   }
-  const int cap = quad ? max_quad_clusters : max_clusters;
-  const int clusters = p.num_tiles < cap ? p.num_tiles : cap;
+  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
   void* args[] = {&p};
   cudaError_t st =
-      cudaLaunchKernel(fn, dim3((quad ? 4 : 2) * clusters), dim3(kGemmThreads), args, kPairSmemBytes, stream);
+      cudaLaunchKernel(fn, dim3(2 * clusters), dim3(kGemmThreads), args, kPairSmemBytes, stream);
   if (st != cudaSuccess) {
     if (err) *err = std::string("pair gemm launch: ") + cudaGetErrorString(st);
     return DOMINO_ERR_CUDA;

@@ -13,7 +13,13 @@
 // address is looked up once per device with cudaGetSymbolAddress, with that
 // device current, during the first call on the device; that first call should
 // therefore come before any stream capture.  The computation is the forward
-// pass's serial schedule (the same kernels, in the same order, on `stream`).
+// pass's serial schedule with one-CTA GEMM tiles (the kernels domino_mlp_fwd
+// runs with DOMINO_SCHEDULE_SERIAL and DOMINO_FLAG_ONE_CTA, in the same order,
+// on `stream`).
+//
+// The first 256 bytes of the array are a header that every call clears: its
+// first 16 bytes are the device status words the GEMMs' bounded waits record a
+// timeout into, read back by domino_mlp_fwd_noalloc_status.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -114,8 +120,9 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
   const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : 2000000000ull;
   cudaStream_t s0 = static_cast<cudaStream_t>(stream);
 
-  // Scratch layout: 256-byte header | H [P][M][Fp] bf16 | Z [P][M][d].  H and Z are
-  // fully written before they are read, so only the header is cleared.
+  // Scratch layout: 256-byte header (device status words at bytes 0-15) |
+  // H [P][M][Fp] bf16 | Z [P][M][d].  H and Z are fully written before they are
+  // read, so only the header is cleared.
   uint8_t* base = nd->scratch;
   const size_t h_shard = static_cast<size_t>(M) * Fp * 2;
   const size_t z_off = (256 + h_shard * P + 255) / 256 * 256;
@@ -124,6 +131,7 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
   if (e != cudaSuccess) return noalloc_fail(DOMINO_ERR_CUDA, std::string("header clear: ") + cudaGetErrorString(e));
 
   static const int kEpiOfAct[4] = {EPI_H_GELU, EPI_H_GELU_TANH, EPI_H_SWIGLU, EPI_H_IDENTITY};
+  DeviceStatus* status = reinterpret_cast<DeviceStatus*>(base);
   std::string err;
   for (int k = 0; k < mu; ++k) {
     const int32_t row0 = static_cast<int32_t>(k * Mc);
@@ -146,6 +154,7 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
     L1.n_base = 0;
     L1.n_end = static_cast<int32_t>(Fp);
     L1.K = d;
+    L1.status = status;
     L1.timeout_ns = tmo;
     st = launch_gemm(L1, nd->num_sms, s0, &err);
     if (st != DOMINO_OK) return noalloc_fail(st, err);
@@ -167,6 +176,7 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
       L2.n_base = col0;
       L2.n_end = static_cast<int32_t>(col0 + ds);
       L2.K = Fp;
+      L2.status = status;
       L2.timeout_ns = tmo;
       st = launch_gemm(L2, nd->num_sms, s0, &err);
       if (st != DOMINO_OK) return noalloc_fail(st, err);
@@ -186,4 +196,23 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
     }
   }
   return DOMINO_OK;
+}
+
+extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc_status(void* stream, void** header) {
+  NoallocDevice* nd = nullptr;
+  domino_status_t st = noalloc_setup(&nd);
+  if (st != DOMINO_OK) return st;
+  if (header) *header = nd->scratch;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return noalloc_fail(DOMINO_ERR_CUDA, std::string("stream sync: ") + cudaGetErrorString(e));
+  DeviceStatus h;
+  e = cudaMemcpy(&h, nd->scratch, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return noalloc_fail(DOMINO_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(e));
+  if (h.code == 0) return DOMINO_OK;
+  e = cudaMemset(nd->scratch, 0, sizeof h);
+  if (e != cudaSuccess) return noalloc_fail(DOMINO_ERR_CUDA, std::string("status clear: ") + cudaGetErrorString(e));
+  char buf[160];
+  snprintf(buf, sizeof buf, "no-alloc forward: device wait gave up: site %u, block %u, detail %u", h.where, h.block,
+           h.aux);
+  return noalloc_fail(static_cast<domino_status_t>(h.code), buf);
 }

@@ -206,21 +206,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
-// Paired-CTA tensor load with cluster multicast: the box lands at the same
-// shared-memory offset in every CTA of `cta_mask`, and each destination's bytes
-// are counted on the barrier at `bar_cluster`'s offset in the CTA that stands to
-// that destination as `bar_cluster`'s CTA stands to this one (itself, or the
-// even CTA of its pair).
-__device__ __forceinline__ void tma_load_2d_pair_multicast(void* smem_dst, const CUtensorMap* map,
-                                                           uint32_t bar_cluster, int32_t x, int32_t y,
-                                                           uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
-      : "memory");
-}
-
 // L2 eviction-priority policies for cache hints (createpolicy).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;

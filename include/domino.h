@@ -155,6 +155,29 @@ DOMINO_API domino_status_t domino_mlp_fwd(const domino_mlp_desc_t* desc, const v
                                const void* const* B_shards, void* Y, void* saved, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* Forward pass up to the exchange: the row-parallel partials of every shard,
+ * without the sum over shards.  The Domino page ("Domino: Eliminating
+ * Communication in LLM Training via Generic Tensor Slicing and Overlapping",
+ * Abstract) overlaps each piece's communication with the next piece's
+ * computation; on tensor-parallel ranks that communication is the all-reduce of
+ * these partials, so this is the computation one rank holds (P = 1: its own
+ * shard A_p, B_p) when the all-reduce runs outside this library.
+ *  - Z_shards[p]: [M,d] row-major in desc->partial_dtype, 16-byte aligned,
+ *    caller-owned; receives Z_p = act(X A_p) B_p (each (k, s) piece exactly as
+ *    domino_mlp_fwd computes it before its shard-sum, bit for bit).
+ *  - piece_events: NULL, or mu * out_slices cudaEvent_t handles created by the
+ *    caller.  Event k * out_slices + s is recorded on `stream` as soon as piece
+ *    (k, s) of every Z_p is written (SERIAL / STREAMS: right after that piece's
+ *    row-parallel GEMM, so a collective on another stream can start on it while
+ *    the next chunk computes; FUSED: after the one launch, which writes all).
+ *  - X, A_shards, B_shards, saved, workspace, stream, errors: as domino_mlp_fwd
+ *    (the workspace is sized by domino_mlp_workspace_size; its partial buffers
+ *    are not used).  Y is not touched. */
+DOMINO_API domino_status_t domino_mlp_fwd_partials(const domino_mlp_desc_t* desc, const void* X,
+                                                   const void* const* A_shards, const void* const* B_shards,
+                                                   void* const* Z_shards, void* const* piece_events, void* saved,
+                                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Backward pass of the same block (chain rule), sliced the same way.
  * dY [M,d] in; dX [M,d] out; dA_shards[p] / dB_shards[p] out (bf16, the same
  * layouts as A_shards[p] / B_shards[p]).  `saved` must hold what domino_mlp_fwd
@@ -234,12 +257,24 @@ DOMINO_API const char* domino_last_error(void);
  *  - Every call on a device shares the one array and leaves its contents behind:
  *    calls that overlap on the GPU (other streams, other host threads) race, so
  *    serialise them.
- *  - Device-side waits are bounded as in domino_mlp_fwd, but a timeout of this
- *    variant is not reported through domino_query_device_status. */
+ *  - Device-side waits are bounded as in domino_mlp_fwd.  A wait that runs out
+ *    records DOMINO_ERR_TIMEOUT in status words at the start of the array (Y is
+ *    then incomplete); read them with domino_mlp_fwd_noalloc_status before the
+ *    next call on the device, which clears them. */
 #define DOMINO_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
 DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_desc_t* desc, const void* X,
                                                   const void* const* A_shards, const void* const* B_shards, void* Y,
                                                   void* stream);
+
+/* Device status of the most recent domino_mlp_fwd_noalloc call on the current
+ * device: synchronises `stream`, returns DOMINO_OK or the error a device-side
+ * wait recorded (DOMINO_ERR_TIMEOUT; detail in domino_last_error) and clears it.
+ * If `header` is non-NULL it receives the device address of the array's
+ * 256-byte header (status words at bytes 0-15), which can be handed to
+ * domino_selftest_wait_timeout as its workspace to exercise this report.  Does
+ * the per-device set-up of domino_mlp_fwd_noalloc if no call has done it yet;
+ * allocates nothing. */
+DOMINO_API domino_status_t domino_mlp_fwd_noalloc_status(void* stream, void** header);
 
 /* Kernel launch timing.  Every call made with DOMINO_FLAG_KERNEL_TIMES records a
  * CUDA event before and after each of its kernel launches, on the stream the

@@ -191,3 +191,32 @@ def test_tensor_peak_validates_before_cuda(lib):
     assert lib.domino_tensor_peak(1, 0, 0x40000, ws - 1, 0, None, ref) == 4
     assert lib.domino_tensor_peak(1, 0, 0x40010, ws, 0, None, ref) == 3
     assert b"mmas_per_cluster" in lib.domino_last_error() or b"256-byte" in lib.domino_last_error()
+
+
+def test_partials_validates(lib):
+    d = desc()
+    arr = b._ptr_array([0x20000] * 2)
+    z = b._ptr_array([0x50000, 0x58000])
+    ws = 1 << 40
+    fn = lib.domino_mlp_fwd_partials
+    assert fn(None, 0x30000, arr, arr, z, None, None, 0x10000, ws, None) == 1
+    assert fn(ctypes.byref(d), 0x30000, arr, arr, None, None, None, 0x10000, ws, None) == 1
+    assert fn(ctypes.byref(d), 0x30000, arr, arr, b._ptr_array([0x50000, 0]), None, None, 0x10000, ws, None) == 1
+    assert fn(ctypes.byref(d), 0x30000, arr, arr, b._ptr_array([0x50000, 0x58004]), None, None, 0x10000, ws,
+              None) == 3
+    assert fn(ctypes.byref(d), 0x30000, arr, arr, z, b._ptr_array([0x1] + [0] * 7), None, 0x10000, ws, None) == 1
+    assert "event" in lib.domino_last_error().decode()
+    small = b.workspace_size(d) - 1
+    assert fn(ctypes.byref(d), 0x30000, arr, arr, z, None, None, 0x10000, small, None) == 4
+    # an empty batch touches nothing
+    e = desc(M=0)
+    assert fn(ctypes.byref(e), 0, arr, arr, z, None, None, 0x10000, ws, None) == 0
+
+
+def test_descriptor_rejects_outputs_beyond_32bit_vector_count(lib):
+    # the shard-sum counts 16-byte vectors of Y with 32-bit indices: M * d / 8 must stay below 2^32
+    d = desc(M=(1 << 28) - 1024, d=1 << 7, F=1024, mu=1)
+    assert b.workspace_size(d) > 0
+    d2 = desc(M=(1 << 28) + 1024, d=1 << 7, F=1024, mu=1)
+    assert b.workspace_size(d2) == 0
+    assert "2^32" in lib.domino_last_error().decode()

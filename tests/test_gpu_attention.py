@@ -90,3 +90,18 @@ def test_gpt_attention_full_size_sampled():
         err = max_rel_err(Y[rows], ref)
         assert err <= TOL, f"sequence {seq}: {err:.3e}"
     assert np.isfinite(Y).all()
+
+
+def test_llama_attention_full_size_sampled():
+    # 4 sequences of 2048 tokens, d 4096, 32 heads on 8 shards, 4 chunks of one sequence each, bf16 partials:
+    # the first and the last chunk's sequence against the oracle
+    w = wl.ATTN_WORKLOADS["llama_attn_fwd"]
+    t = wl.generate_attn(w, seed=0)
+    Y = _run(w, t).double().cpu().numpy()
+    f = _f64(t)
+    for seq in (0, w.B - 1):
+        rows = slice(seq * w.S, (seq + 1) * w.S)
+        ref = att.attn_fwd(f["X"][rows], f["Wqkv"], f["Wo"], w.S, w.H)
+        err = max_rel_err(Y[rows], ref)
+        assert err <= TOL, f"sequence {seq}: {err:.3e}"
+    assert np.isfinite(Y).all()

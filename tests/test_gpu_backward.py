@@ -91,12 +91,12 @@ def test_backward_partial_row_group():
     _check_full(w.with_(act="gelu", partial="f32"), seed=14)
 
 
-@pytest.mark.parametrize("rows", [300, 700])
-def test_backward_quad_row_tails(rows):
-    # chunks of more than 256 rows: the forward GEMMs run as 512-row tiles of two pairs, the second
-    # pair of the last tile partly (300) or wholly (700) below the chunk; the backward's 256-row
-    # tiles then cover 600 and 1400 rows with ragged last blocks
-    w = wl.Workload("quad_tail_bwd", M=2 * rows, d=512, F=768, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
+@pytest.mark.parametrize("rows", [129, 300, 700])
+def test_backward_pair_row_tails(rows):
+    # 256-row tiles on 2-CTA clusters: the last tile's odd CTA holds 1 row (129), lies wholly below the
+    # chunk (300) or holds part of its block (700); the dH and weight-gradient launches over all M then
+    # end on a ragged block too
+    w = wl.Workload("pair_tail_bwd", M=2 * rows, d=512, F=768, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
     _check_full(w, seed=15)
 
 
@@ -117,17 +117,32 @@ def test_llama_fwdbwd_full_size_sampled():
     t = wl.generate(w, 0, with_dy=True)
     Y, dX, dA, dB = _run_fwd_bwd(w, t)
     rng = np.random.default_rng(0)
-    rows = sorted(set(int(r) for k in range(w.mu) for r in
-                      [k * w.Mc, k * w.Mc + w.Mc - 1, *(k * w.Mc + rng.integers(0, w.Mc, 4))]))
+    # 64 rows of every chunk: the tile edges (128-row CTA blocks, 256-row pair tiles), the chunk's last
+    # row and random rows
+    rows = set()
+    for k in range(w.mu):
+        lo = k * w.Mc
+        chunk = {lo + o for o in (0, 1, 127, 128, 255, 256, 511, 512) if o < w.Mc} | {lo + w.Mc - 1}
+        while len(chunk) < 64:
+            chunk.add(lo + int(rng.integers(0, w.Mc)))
+        rows |= chunk
+    rows = sorted(rows)
     Xr = t["X"][rows].double().numpy()
     dYr = t["dY"][rows].double().numpy()
     Wg, Wu, Wd = (t[k].double().numpy() for k in ("Wg", "Wu", "B"))
     ref_rows = oracle.mlp_bwd(Xr, (Wg, Wu), Wd, dYr, "swiglu")
     assert oracle.max_rel_err(_f64(dX[rows]), ref_rows["dX"]) <= TOL
     assert oracle.max_rel_err(_f64(Y[rows]), oracle.mlp_fwd(Xr, (Wg, Wu), Wd, "swiglu")) <= TOL
-    # hidden units from every shard, including each shard's last unit (the N and K tails)
-    units = sorted(set([p * w.Fp + j for p in range(w.P) for j in (0, w.Fp - 1)] +
-                       [int(u) for u in rng.integers(0, w.F, 8)]))
+    # 10 hidden units of every shard: the column-tile edges (256-wide N tiles of dH, 64-deep K blocks of
+    # dX), the shard's last unit (the N and K tails) and random units
+    units = set()
+    for p in range(w.P):
+        lo = p * w.Fp
+        shard = {lo + j for j in (0, 63, 64, 255, 256, 1279, 1280, w.Fp - 1) if j < w.Fp}
+        while len(shard) < 10:
+            shard.add(lo + int(rng.integers(0, w.Fp)))
+        units |= shard
+    units = sorted(units)
     ref_cols = oracle.mlp_bwd(t["X"].double().numpy(), (Wg[:, units], Wu[:, units]), Wd[units],
                               t["dY"].double().numpy(), "swiglu")
     assert oracle.max_rel_err(_f64(dA[0][:, units]), ref_cols["dWg"]) <= TOL

@@ -1,9 +1,11 @@
 """Strand interleaving (domino_mlp_fwd_bwd_interleaved) on the GB300: the forward
 of strand a and the backward of strand b in one call give bit-for-bit the
-results of a separate domino_mlp_fwd(a) and domino_mlp_bwd(b)."""
+results of a separate domino_mlp_fwd(a) and domino_mlp_bwd(b), and each output
+matches the fp64 oracle (max|g - g_ref| / max|g_ref| <= 1e-2 per tensor)."""
 import pytest
 import torch
 
+import oracle
 from communication_overlap_domino_gb300 import binding as b
 from communication_overlap_domino_gb300 import workloads as wl
 
@@ -23,7 +25,7 @@ def _strands(w):
     ta, tb = wl.generate(w, 31, with_dy=True), wl.generate(w, 32, with_dy=True)
     A = (ta["Wg"].to(dev), ta["Wu"].to(dev)) if w.act == "swiglu" else ta["A"].to(dev)
     A_sh, B_sh = b.shard_weights(A, ta["B"].to(dev), w.P)
-    return A_sh, B_sh, ta["X"].to(dev), tb["X"].to(dev), tb["dY"].to(dev)
+    return A_sh, B_sh, ta["X"].to(dev), tb["X"].to(dev), tb["dY"].to(dev), ta, tb
 
 
 @pytest.mark.parametrize("schedule", ["streams", "serial"])
@@ -32,7 +34,7 @@ def _strands(w):
     wl.Workload("interleave_glu", M=1024, d=512, F=2752, P=2, mu=4, act="swiglu", partial="bf16", bwd=True),
 ], ids=lambda w: w.name if isinstance(w, wl.Workload) else w)
 def test_interleaved_equals_separate_calls(w, schedule):
-    A_sh, B_sh, Xa, Xb, dYb = _strands(w)
+    A_sh, B_sh, Xa, Xb, dYb, ta, tb = _strands(w)
     kw = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices)
     desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, schedule)
     saved_b = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device=Xa.device)
@@ -50,3 +52,18 @@ def test_interleaved_equals_separate_calls(w, schedule):
     assert b.query_device_status(ws) == 0
     assert torch.equal(Ya, Ya_ref) and torch.equal(saved_a, saved_a_ref) and torch.equal(dXb, dXb_ref)
     assert all(torch.equal(x, y) for x, y in zip(dA, dA_ref)) and all(torch.equal(x, y) for x, y in zip(dB, dB_ref))
+    # against the oracle: strand a's forward, strand b's backward (weights are strand a's)
+    fa, fb = wl.to_float64(ta), wl.to_float64(tb)
+    A = (fa["Wg"], fa["Wu"]) if w.act == "swiglu" else fa["A"]
+    f64 = lambda x: x.double().cpu().numpy()  # noqa: E731
+    errs = {"Ya": oracle.max_rel_err(f64(Ya), oracle.mlp_fwd(fa["X"], A, fa["B"], w.act))}
+    ref = oracle.mlp_bwd(fb["X"], A, fa["B"], fb["dY"], w.act)
+    dA_full, dB_full = b.unshard_grads(dA, dB, w.act)
+    errs["dXb"] = oracle.max_rel_err(f64(dXb), ref["dX"])
+    errs["dB"] = oracle.max_rel_err(f64(dB_full), ref["dB"])
+    if w.act == "swiglu":
+        errs["dWg"] = oracle.max_rel_err(f64(dA_full[0]), ref["dWg"])
+        errs["dWu"] = oracle.max_rel_err(f64(dA_full[1]), ref["dWu"])
+    else:
+        errs["dA"] = oracle.max_rel_err(f64(dA_full), ref["dA"])
+    assert all(v <= 1e-2 for v in errs.values()), errs

@@ -96,16 +96,17 @@ def test_ragged_shapes(act, partial, schedule):
     _check_full(w, seed=3, schedule=schedule)
 
 
-@pytest.mark.parametrize("rows", [300, 700, 1000])
+@pytest.mark.parametrize("rows", [129, 200, 300, 700])
 @pytest.mark.parametrize("act,partial", [("gelu", "f32"), ("swiglu", "bf16")])
-def test_quad_row_tails(rows, act, partial):
-    # chunks of more than 256 rows run the separate-launch GEMMs as 512-row tiles of two CTA pairs
-    # sharing B: the second pair of the last tile lies partly (300, 1000) or wholly (700) below the
-    # chunk.  Rows past M (a sentinel band after the output) must stay untouched.
-    w = wl.Workload("quad_tail", M=2 * rows, d=512, F=768, P=2, mu=2, act=act, partial=partial)
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_pair_row_tails(rows, act, partial, schedule):
+    # the GEMMs run 256-row tiles on 2-CTA clusters, 128 rows per CTA: in the last tile of a chunk the
+    # odd CTA holds 1 row (129), part of its block (200, 700) or lies wholly below the chunk (300).
+    # Rows past M (a sentinel band after the output) must stay untouched.
+    w = wl.Workload("pair_tail", M=2 * rows, d=512, F=768, P=2, mu=2, act=act, partial=partial)
     t = wl.generate(w, 11)
     Ybuf = torch.full((w.M + 64, w.d), 7.0, dtype=torch.bfloat16, device="cuda:0")
-    Y = _run(w, t, "streams", Y=Ybuf[:w.M])
+    Y = _run(w, t, schedule, Y=Ybuf[:w.M])
     f64 = wl.to_float64(t)
     ref = oracle.mlp_fwd(f64["X"], _oracle_A(w, f64), f64["B"], w.act)
     err = oracle.max_rel_err(Y.double().cpu().numpy(), ref)
@@ -199,14 +200,22 @@ def test_saved_preactivations():
 
 # ------------------------------------------------------- full-size workloads
 
-def _sample_rows(w, per_chunk=6, seed=0):
+# offsets within a chunk where one tile (128 rows per CTA, 256 per CTA pair, 512 per group of pairs) ends and
+# the next begins
+_TILE_EDGES = (0, 1, 127, 128, 255, 256, 511, 512)
+
+
+def _sample_rows(w, per_chunk=64, seed=0):
+    """Rows of every chunk for a sampled comparison: the tile edges, the chunk's last row and random rows."""
     rng = np.random.default_rng(seed)
     rows = []
     for k in range(w.mu):
         lo = k * w.Mc
-        rows += [lo, lo + w.Mc - 1]
-        rows += list(lo + rng.integers(0, w.Mc, per_chunk - 2))
-    return sorted(set(int(r) for r in rows))
+        picked = {lo + o for o in _TILE_EDGES if o < w.Mc} | {lo + w.Mc - 1}
+        while len(picked) < min(per_chunk, w.Mc):
+            picked.add(lo + int(rng.integers(0, w.Mc)))
+        rows += picked
+    return sorted(int(r) for r in rows)
 
 
 def _check_sampled(w, schedule="streams"):  # noqa: C901
