@@ -82,6 +82,15 @@ def ncu_traffic(kernel_kind, workload):
     return entry.get("dram_bytes_per_launch")
 
 
+def tensor_peak_for(peaks, launch_s):
+    """The bf16 denominator for a kernel whose launches last launch_s seconds: the burst figure (a GEMM
+    timed alone, best of 10) for launches under a second, the sustained one (seconds back to back under
+    the power cap) for longer ones.  Returns (peak, which)."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    return (burst, "bf16_tflops") if launch_s < 1.0 else (sustained, "bf16_tflops_sustained")
+
+
 # ------------------------------------------------------------------- NVTX
 
 # The timed region is an NVTX push/pop range of this name, so that a profiler's launch list can be limited
@@ -411,6 +420,38 @@ def run_ours(args, w, rank, world, local_rank):
             ex.append(max(0, tl["reduce_end_ns"] - tl["gemm_end_ns"]) * 1e-6)
         fused_exposed = statistics.mean(ex)
 
+    # ---- A/B measure of the reduction's cost: the same call without the shard-sum, alternating with the full
+    # call (L2 flushed before each).  domino_mlp_fwd_partials runs the same GEMM tiles in the same order and
+    # writes the same partials, which are its result; the difference in mean duration is what the shard-sum
+    # adds to the layer, including its slowing of the GEMM tiles it runs beside.
+    ab = None
+    if not w.bwd and args.ab_pairs > 0:
+        zdt = torch.float32 if w.partial == "f32" else torch.bfloat16
+        Zab = [torch.empty((w.M, w.d), dtype=zdt, device=dev) for _ in range(w.P)]
+        kw_ab = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices, schedule=args.schedule,
+                     workspace=ws)
+        ev_ab = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.ab_pairs)] for _ in range(2)]
+        for i in range(args.ab_pairs):
+            for which in (0, 1):
+                flush.zero_()
+                ev_ab[which][i][0].record(stream)
+                if which == 0:
+                    b.mlp_fwd(X, A_sh, B_sh, Y=Y, **kw_ab)
+                else:
+                    b.mlp_fwd_partials(X, A_sh, B_sh, Z_shards=Zab, **kw_ab)
+                ev_ab[which][i][1].record(stream)
+        torch.cuda.synchronize()
+        full_ms = statistics.mean(a.elapsed_time(e) for a, e in ev_ab[0])
+        part_ms = statistics.mean(a.elapsed_time(e) for a, e in ev_ab[1])
+        ab = {"full_ms": round(full_ms, 4), "partials_ms": round(part_ms, 4), "pairs": args.ab_pairs,
+              "exposed_us": round(1e3 * (full_ms - part_ms), 2),
+              "method": "mean duration of domino_mlp_fwd minus that of domino_mlp_fwd_partials (same schedule, "
+                        "same GEMM tiles, no shard-sum), calls alternating, L2 flushed before each"}
+        del Zab
+        if b.query_device_status(ws) != 0:
+            raise RuntimeError("device status after the A/B calls")
+
     # ---- the L2 flush alone, for reading the end-to-end numbers (which contain it)
     fl_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
     for s_, e_ in fl_ev:
@@ -536,7 +577,8 @@ def run_ours(args, w, rank, world, local_rank):
     dominant = max((k for k in kinds if k != "shard_sum"), key=lambda k: kinds[k]["total_ms"])
     dom_tflops = kinds[dominant]["flops"] / (kinds[dominant]["total_ms"] * 1e-3) / 1e12
     dom_flops_per_launch = kinds[dominant]["flops"] / kinds[dominant]["launches"]
-    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_tf, peak_key = tensor_peak_for(peaks, kinds[dominant]["avg_us"] * 1e-6)
+    sustained_tf = float(peaks.get("bf16_tflops_sustained", peak_tf))
     ss_gbs = ss_bytes / (kinds["shard_sum"]["avg_us"] * 1e-6) / 1e9 if "shard_sum" in kinds else None
     span_ms, exposed_ms = timeline_stats(records)
     calls_per_step = 2 if w.bwd else 1
@@ -565,19 +607,27 @@ def run_ours(args, w, rank, world, local_rank):
                    "l2": "flushed between steps (256 MiB write outside the step events)",
                    **({"plan": args.plan_result} if getattr(args, "plan_result", None) else {})},
         "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
+        "pct_of_bf16_sustained": round(100.0 * value / world / sustained_tf, 2),
         "exposed_reduce_us_per_layer": round(1e3 * exposed_ms, 2),
         "exposed_reduce_frac": round(exposed_ms / span_ms, 4) if span_ms > 0 else None,
+        "exposed_reduce_method": "fused: the kernel's own %globaltimer stamps, last GEMM tile end to last "
+                                 "shard-sum piece end; streams/serial: call span minus the union of GEMM launch "
+                                 "intervals (CUDA events)",
+        "exposed_reduce_ab_us_per_layer": None if ab is None else ab["exposed_us"],
+        "exposed_reduce_ab": ab,
         "roofline": {
-            "kernel": f"gemm_bf16_tcgen05 ({dominant})",
-            "note": "achieved = algorithmic flops of the kernel's launches / their summed event durations",
+            "kernel": {"fused": "fused_fwd_pair_kernel (both projections and the shard-sum, one launch)"}.get(
+                dominant, f"gemm_pair_kernel ({dominant})"),
+            "note": "achieved = algorithmic flops of the kernel's launches / their summed event durations; peak = "
+                    "the burst bf16 figure for launches under a second, else the sustained one",
             "bound": "tensor",
             "achieved": round(dom_tflops, 2),
             "peak": peak_tf,
             "unit": "TFLOP/s",
             "frac": round(dom_tflops / peak_tf, 4),
-            "peak_source": f"{peak_src} bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
-            else f"{peak_src} bf16_tflops",
-            "frac_of_burst": round(dom_tflops / float(peaks.get("bf16_tflops", peak_tf)), 4),
+            "peak_source": f"{peak_src} {peak_key}",
+            "avg_launch_us": round(kinds[dominant]["avg_us"], 2),
+            "frac_of_sustained": round(dom_tflops / sustained_tf, 4),
             "flops_per_launch": dom_flops_per_launch,
             "traffic": ncu_traffic(dominant, w.name),
             "frac_of_mma_probe": round(dom_tflops / probe["tflops"], 4),
@@ -699,7 +749,6 @@ def run_attn(args, w, rank, world, local_rank):
         return None
 
     peaks, peak_src = load_peaks()
-    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     Mc = w.M // w.mu
     core_flops_chunk = 2 * 2 * (w.B // w.mu) * w.H * w.dh * (w.S * (w.S + 1) // 2)
     launch_flops = {"gemm1": 2.0 * Mc * w.d * 3 * w.H * w.dh, "attn": float(core_flops_chunk),
@@ -713,6 +762,8 @@ def run_attn(args, w, rank, world, local_rank):
     for k in kinds.values():
         k["avg_us"] = 1e3 * k["total_ms"] / k["launches"]
     a_tf = kinds["attn"]["flops"] / (kinds["attn"]["total_ms"] * 1e-3) / 1e12
+    peak_tf, peak_key = tensor_peak_for(peaks, kinds["attn"]["avg_us"] * 1e-6)
+    sustained_tf = float(peaks.get("bf16_tflops_sustained", peak_tf))
     span_ms, exposed_ms = timeline_stats(records)
     value = whole_job_tflops(w.flops(), world, mean_ms)
     line = {
@@ -739,7 +790,8 @@ def run_attn(args, w, rank, world, local_rank):
             "note": "achieved = causal attention flops (Q K^T and P V over the visible query-key pairs) of the "
                     "kernel's launches / their summed event durations",
             "bound": "tensor", "achieved": round(a_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
-            "frac": round(a_tf / peak_tf, 4), "peak_source": f"{peak_src} bf16_tflops_sustained",
+            "frac": round(a_tf / peak_tf, 4), "peak_source": f"{peak_src} {peak_key}",
+            "avg_launch_us": round(kinds["attn"]["avg_us"], 2), "frac_of_sustained": round(a_tf / sustained_tf, 4),
             "flops_per_launch": float(core_flops_chunk), "traffic": ncu_traffic("attn", w.name),
             "frac_of_mma_probe": round(a_tf / probe["tflops"], 4),
         },
@@ -862,6 +914,8 @@ def main():
                     help="take mu and the schedule from domino_mlp_plan (overrides --mu and --schedule)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ab-pairs", type=int, default=30,
+                    help="alternating full / partials-only calls for the A/B measure of the reduction (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -88,8 +88,9 @@ WORKLOADS: Dict[str, Workload] = {
     )
 }
 
-# The workload the throughput benchmark times at one GPU.
-BENCH_WORKLOAD = "gpt_gelu_fwd"
+# The workload the throughput benchmark times at one GPU: the largest configuration, at the mu (4) and the
+# fused schedule that domino_mlp_plan picks for it on a GB300.
+BENCH_WORKLOAD = "large_swiglu_fwd"
 
 
 def _randn(shape: Tuple[int, ...], seed: int, std: float) -> torch.Tensor:
