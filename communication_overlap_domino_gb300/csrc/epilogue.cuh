@@ -67,11 +67,41 @@ __device__ __forceinline__ void gelu_erf2(float& h0, float& h1, float x0, float 
 __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.79788456080286536f * (x + 0.044715f * x * x * x)));
 }
-// silu(x) = x * sigmoid(x) with the fast reciprocal: far inside the bf16
-// rounding of its result; for x -> -inf the denominator overflows to inf and
-// the quotient goes to 0 as it should.
-__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float silu(float x) { return x * sigmoid_fast(x); }
+// The logistic function of two values with the fp32 pair instructions, from exp(-x) = 2^(-x log2 e): the
+// scaling and the 1 + e go two at a time, the exponential (ex2.approx) and the fast reciprocal stay per
+// value (far inside the bf16 rounding of the results).  As x -> -inf, 2^(-x log2 e) overflows to inf and the
+// quotient goes to 0.
+__device__ __forceinline__ void sigmoid2(float& s0, float& s1, float x0, float x1) {
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  float a0, a1, d0, d1;
+  mul2(a0, a1, x0, x1, kNegLog2e, kNegLog2e);
+  add2(d0, d1, ex2_approx(a0), ex2_approx(a1), 1.0f, 1.0f);
+  s0 = __fdividef(1.0f, d0);
+  s1 = __fdividef(1.0f, d1);
+}
+
+// SwiGLU of two (gate, up) pairs: h = silu(g) u = (g sigmoid(g)) u.
+__device__ __forceinline__ void swiglu2(float& h0, float& h1, float g0, float g1, float u0, float u1) {
+  float s0, s1;
+  sigmoid2(s0, s1, g0, g1);
+  mul2(s0, s1, s0, s1, g0, g1);
+  mul2(h0, h1, s0, s1, u0, u1);
+}
+
+// The SwiGLU backward of two (gate, up) pairs, with s = sigmoid(g):
+// du = dH silu(g) = (dH g) s and dg = dH u silu'(g) = ((dH u) s)(1 + g (1 - s)).
+__device__ __forceinline__ void swiglu_grad2(float& dg0, float& dg1, float& du0, float& du1, float dh0, float dh1,
+                                             float g0, float g1, float u0, float u1) {
+  float s0, s1, t0, t1, v0, v1, w0, w1;
+  sigmoid2(s0, s1, g0, g1);
+  mul2(t0, t1, dh0, dh1, g0, g1);
+  mul2(du0, du1, t0, t1, s0, s1);
+  mul2(v0, v1, dh0, dh1, u0, u1);
+  mul2(v0, v1, v0, v1, s0, s1);
+  add2(w0, w1, 1.0f, 1.0f, -s0, -s1);
+  fma2(w0, w1, g0, g1, w0, w1, 1.0f, 1.0f);
+  mul2(dg0, dg1, v0, v1, w0, w1);
+}
 
 // Derivatives for the backward epilogue (product and chain rules).
 __device__ __forceinline__ float gelu_erf_grad(float x) {
@@ -237,7 +267,9 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& e, uint32_t tacc, 
     tmem_ld_32x32b_x32(tacc + kBN / 2 + c * 32, r1);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) h[j] = silu(__uint_as_float(r0[j])) * __uint_as_float(r1[j]);
+    for (int j = 0; j < 32; j += 2)
+      swiglu2(h[j], h[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), __uint_as_float(r1[j]),
+              __uint_as_float(r1[j + 1]));
     if (row_ok && e.aux != nullptr) {
       float g[32], u[32];
 #pragma unroll
@@ -392,12 +424,9 @@ __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc
     if constexpr (kSwiglu) {
       float dg[32], du[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float dh = __uint_as_float(r0[j]);
-        const float sg = sigmoid_fast(g[j]);
-        du[j] = dh * g[j] * sg;                               // dH * silu(g)
-        dg[j] = dh * u[j] * sg * (1.0f + g[j] * (1.0f - sg));  // dH * u * silu'(g)
-      }
+      for (int j = 0; j < 32; j += 2)
+        swiglu_grad2(dg[j], dg[j + 1], du[j], du[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), g[j],
+                     g[j + 1], u[j], u[j + 1]);
       if (tma) {
         stage_and_store<false>(e, dg, lane, sbuf, col, y);
         stage_and_store<false>(e, du, lane, sbuf, static_cast<int32_t>(e.out_u_off + col), y);

@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
     prefetch_tmap(&f.map_x);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
+    const uint64_t keep_a = l2_policy_evict_last();  // X and H: re-read by every column block
     for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
       const FusedTile T = fused_tile(f, t);
       const CUtensorMap *ma, *mb0, *mb1;
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
         uint8_t* sb = smem_b + stage * kBStageBytes;
         mbar_arrive_expect_tx(&full_bar[stage], kAStageBytes + kBStageBytes);
         const int k0 = kb * kBK;
-        tma_load_2d(sa, ma, &full_bar[stage], k0, ya);
+        tma_load_2d(sa, ma, &full_bar[stage], k0, ya, keep_a);
         tma_load_2d(sb, mb0, &full_bar[stage], k0, yb0);
         tma_load_2d(sb + kBStageBytes / 2, mb1, &full_bar[stage], k0, yb1);
         issued_mask |= 1u << stage;
@@ -577,6 +578,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
+    // X (GEMM1) and H (GEMM2) are the operands every column block re-reads while the weights stream past:
+    // their lines are the last the L2 gives up
+    const uint64_t keep_a = l2_policy_evict_last();
     for (int t = cluster_id; t < num_tiles && !*abort_flag; t += num_clusters) {
       const FusedTile T = fused_pair_tile(f, t);
       const int m = 2 * T.m + static_cast<int>(rank);  // this CTA's 128-row block
@@ -612,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * (kPA + kPB));
         const uint32_t bar = full0 + stage * 8;
         const int k0 = kb * kBK;
-        tma_load_2d_pair(sa, ma, bar, k0, ya);
+        tma_load_2d_pair(sa, ma, bar, k0, ya, keep_a);
         tma_load_2d_pair(sb, mb, bar, k0, yb);
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);

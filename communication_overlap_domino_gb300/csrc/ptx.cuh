@@ -206,6 +206,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// The paired-CTA tensor load with an L2 eviction-priority policy (createpolicy)
+// for the lines it brings in.
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t x, int32_t y, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(cache_hint)
+      : "memory");
+}
+
 // L2 eviction-priority policies for cache hints (createpolicy).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;
