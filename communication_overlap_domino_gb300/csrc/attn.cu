@@ -8,34 +8,38 @@
 // the output rescaled by exp2(m_old - m_new) when the maximum grows), so no
 // score matrix ever reaches global memory.
 //
-// Persistent kernel, one CTA per SM, 10 warps:
-//   warp 0      TMA producer: the Q tile once per item, then the key blocks K_j
-//               and value blocks V_j into two 2-slot rings, K one block ahead
-//               of V (K_{j+1} is needed for the next scores before V_j is
-//               needed for P_j V_j).
-//   warp 1      tensor-memory allocation; lane 0 issues the MMAs:
-//               S_j = Q K_j^T (M 128, N 128, K 128) into one of two TMEM score
-//               buffers, and O += P_j V_j into the TMEM output accumulator,
-//               with P_j (the A operand) read from tensor memory too.
-//               S_{j+1} is issued before P_j V_j, so the next scores are
-//               computed while the softmax of block j runs.
-//   warps 2-9   two threads per query row (warps w and w + 4 read the same
-//               tensor-memory lanes), each owning 64 of the row's 128 key and
-//               output columns.  Both take the row maximum over all 128 scores,
-//               so they agree on it.  Lazy rescaling: the running maximum m only
-//               moves when a block's maximum exceeds it by more than 2^8 (in the
-//               exp2 domain); then the thread rescales its half of the output
-//               row in tensor memory (after P_{j-1} V_{j-1} has landed) and its
-//               part of the row sum.  Each writes its 64 probabilities
-//               p = exp2(s * c - m) as bf16 pairs into the P columns of tensor
-//               memory, its query row's lane (once P_{j-1} V_{j-1} has finished
-//               reading them).  After the last block the two parts of the row
-//               sum are added through shared memory and O / l is stored as bf16.
+// Persistent kernel, one CTA per SM, running two independent streams of items
+// ("lanes" 0 and 1) that share only the tensor cores: while the softmax warps
+// of one lane turn a block of scores into probabilities, the tensor cores
+// multiply the other lane's probabilities by V and compute its next scores.
+// Each lane has its own producer, MMA issuer and softmax warps, so one lane
+// waiting on a load never holds up the other.  12 warps:
+//   warps 0, 10 TMA producer of lane 0, lane 1: the lane's Q tile (one slot)
+//               and its key and value blocks through a 2-slot ring of 32 KB
+//               slots, in the order its MMAs consume them.
+//   warps 1, 11 lane 0 of each issues its lane's MMAs (warp 1 also allocates
+//               the 512 tensor-memory columns): per step, O += P_b V_b for the
+//               block b whose probabilities are ready (A operand from tensor
+//               memory), then S_{b+1} = Q K_{b+1}^T (M 128, N 128, K 128) into
+//               the same tensor-memory columns, which P_b occupied.  The tensor
+//               cores execute one thread's MMAs in issue order, so the P V
+//               product has read P_b before S_{b+1} overwrites it.
+//   warps 2-5   softmax of lane 0, warps 6-9 of lane 1: one thread per query
+//               row (warp w reads tensor-memory lanes 32 (w % 4) ..).  Per key
+//               block: the row maximum over the 128 scores, lazy rescaling (the
+//               running maximum m only moves when a block's maximum exceeds it
+//               by more than 2^8 in the exp2 domain; then the warp rescales its
+//               output rows in tensor memory, which the previous P V product
+//               has finished updating), and the 128 probabilities
+//               p = exp2(s c - m) written as bf16 pairs over score columns
+//               64-127.  After an item's last block: O / l as bf16 to global
+//               memory.
+// Tensor memory per lane L: scores / probabilities at columns 128 L, the
+// output accumulator at 256 + 128 L.
 //
-// Barriers (all waits bounded, as in the GEMMs): q_full / q_empty, k_full[s] /
-// k_empty[s], v_full[s] / v_empty[s], s_full[b] / s_empty[b], p_full, pv_full,
-// o_empty, l_ready[2], final; the softmax warps arrive once per warp, after
-// __syncwarp, on s_empty, p_full, o_empty and l_ready.
+// Barriers (all waits bounded), per lane: q_full / q_empty, ring full / empty
+// per slot, s_full, p_full, o_full / o_empty, final.  The softmax warps arrive
+// once per warp, after __syncwarp.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -50,20 +54,18 @@ namespace domino {
 
 namespace {
 
-constexpr int kAttnThreads = 320;
-constexpr int kSoftmaxWarps = 8;  // consumer barriers count one arrival per softmax warp
+constexpr int kAttnThreads = 384;
+constexpr int kLaneWarps = 4;                     // softmax warps per lane; consumer barriers count one per warp
 constexpr int kTile = 128;                        // queries per item, keys per block, head width
 constexpr int kSub = kTile * 64 * 2;              // 16 KB: 128 rows x 64 bf16 (one 128-byte-swizzled box)
 constexpr int kQBytes = 2 * kSub;                 // Q tile: dh halves 0-63 and 64-127
-constexpr int kKBytes = 2 * kSub;                 // K tile: dh halves
-constexpr int kVBytes = 2 * kSub;                 // V tile: 2 blocks of 64 keys x (2 boxes of 64 dh x 64 keys)
-constexpr int kSlots = 2;                         // slots of the K ring and of the V ring
-constexpr int kLsumBytes = 2 * 2 * kTile * 4;     // row-sum halves, double-buffered by item
-constexpr int kAttnSmemBytes = kQBytes + kSlots * (kKBytes + kVBytes) + kLsumBytes + 1024 + 256;
+constexpr int kSlotBytes = 2 * kSub;              // one K block (dh halves) or one V block (MN-major boxes)
+constexpr int kRing = 2;                          // K / V ring slots per lane
+constexpr int kAttnSmemBytes = 2 * (kQBytes + kRing * kSlotBytes) + 1024 + 512;
 static_assert(kAttnSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kAttnTmemCols = 512;           // S buffers at 0 and 128, the output O at 256, P at 384
-constexpr uint32_t kOCol = 256;
-constexpr uint32_t kPCol = 384;                   // P as bf16 pairs: 64 columns, key 2c and 2c + 1 in column c
+constexpr uint32_t kAttnTmemCols = 512;
+constexpr uint32_t kOCol = 256;                   // output accumulator of lane L at kOCol + 128 L
+constexpr uint32_t kPCol = 64;                    // probabilities at score columns 64-127 (keys 2q, 2q + 1 in 64 + q)
 constexpr float kRescaleLog2 = 8.0f;              // lazy rescaling threshold: the maximum may lag by 2^8
 
 struct AttnItem {
@@ -71,7 +73,7 @@ struct AttnItem {
 };
 
 // Items in order of decreasing query tile: the diagonal makes tile i cost i + 1
-// key blocks, so the longest items start first on the persistent CTAs.
+// key blocks, so the longest items start first.
 __device__ __forceinline__ AttnItem attn_item(const AttnParams& a, int t) {
   const int per_tile = a.P * a.seqs * a.Hp;
   AttnItem it;
@@ -84,41 +86,55 @@ __device__ __forceinline__ AttnItem attn_item(const AttnParams& a, int t) {
   return it;
 }
 
-// The item a CTA runs in its k-th round: the rounds deal the items (longest first) across the persistent
-// CTAs in alternating directions, so a CTA that took one of a round's longest items takes one of the next
-// round's shortest.  With causal items of 1 .. nq key blocks this evens the CTAs' loads (GPT-style chunk:
-// at most 10 key blocks per CTA against 14 when every round deals in the same direction; the mean is 9.5).
-// Every item is dealt exactly once; a CTA's first index past num_items ends its rounds (only the last round
+// The item lane `lane` of this CTA runs in its k-th round.  Each round deals 2 x gridDim items (longest
+// first) to the lanes in a fixed order in which a CTA's two lanes stand at opposite ends (lane 0 of CTA c at
+// position c, lane 1 at 2 gridDim - 1 - c), and the rounds alternate direction: in every round one lane of a
+// CTA takes one of the longer items and the other one of the shorter, and each lane alternates between the
+// two from round to round (with causal items of 1 .. nq key blocks this evens the lanes' and the CTAs' loads).
+// Every item is dealt exactly once; a lane's first index past num_items ends its rounds (only the last round
 // can be partial).
-__device__ __forceinline__ int attn_round_item(int k) {
-  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-  return k * g + ((k & 1) ? g - 1 - b : b);
+__device__ __forceinline__ int attn_round_item(int k, int lane) {
+  const int g = 2 * static_cast<int>(gridDim.x);
+  const int v = lane == 0 ? static_cast<int>(blockIdx.x) : g - 1 - static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? g - 1 - v : v);
 }
 
-// Issues S = Q K^T for the key block in K-ring slot k_idx % 2 into score
-// buffer s_idx % 2, once the block has landed and the buffer is free; the slot
-// is released when the MMAs have read it.
-__device__ __forceinline__ bool attn_issue_s(const AttnParams& a, uint32_t tmem_base, uint32_t qa, uint8_t* sk,
-                                             uint64_t* k_full, uint64_t* k_empty, uint64_t* s_empty,
-                                             uint64_t* s_full, uint32_t k_idx, uint32_t s_idx,
-                                             volatile int* abort_flag, int t) {
-  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-  const uint32_t st = k_idx & 1, sb = s_idx & 1;
-  if (!mbar_wait(&k_full[st], (k_idx >> 1) & 1, abort_flag, a.timeout_ns, a.status, kSiteMmaFull, t)) return false;
-  if (!mbar_wait(&s_empty[sb], ((s_idx >> 1) & 1) ^ 1, abort_flag, a.timeout_ns, a.status, kSiteMmaTmemEmpty, t))
-    return false;
-  tc_fence_after_sync();
-  const uint32_t ka = smem_u32(sk + st * kKBytes);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint64_t ad = smem_desc_k128(qa + (k >> 2) * kSub) + 2 * (k & 3);
-    const uint64_t bd = smem_desc_k128(ka + (k >> 2) * kSub) + 2 * (k & 3);
-    mma_bf16_ss(tmem_base + sb * kTile, ad, bd, idesc_s, k != 0 ? 1u : 0u);
+// One lane's sequence of key blocks, flattened over its items: block (item t, j) for j = 0 .. i.  `cur` is
+// the next block whose scores are to be computed, `prev` the block whose probabilities feed the next P V.
+// The producer and the MMA issuer step identical copies of it, so they agree on every load and MMA.
+struct LaneWalk {
+  int round = 0;
+  int t = 0;      // current item (>= num_items: none left)
+  AttnItem it{};
+  int j = 0;      // next block of the current item whose scores are computed
+  bool has_prev = false;
+  AttnItem prev_it{};
+  int prev_j = 0;
+  int items = 0;  // items started (their first block's scores issued)
+
+  __device__ __forceinline__ void start(const AttnParams& a, int lane) {
+    t = attn_round_item(0, lane);
+    if (t < a.num_items) it = attn_item(a, t);
   }
-  mma_commit(&s_full[sb]);
-  mma_commit(&k_empty[st]);
-  return true;
-}
+  __device__ __forceinline__ bool has_cur(const AttnParams& a) const { return t < a.num_items; }
+  __device__ __forceinline__ bool done(const AttnParams& a) const { return !has_prev && !has_cur(a); }
+  // after one step: the current block becomes `prev`, the walk moves to the next block or item
+  __device__ __forceinline__ void advance(const AttnParams& a, int lane) {
+    if (!has_cur(a)) {
+      has_prev = false;
+      return;
+    }
+    has_prev = true;
+    prev_it = it;
+    prev_j = j;
+    if (j == 0) ++items;
+    if (++j > it.i) {
+      j = 0;
+      t = attn_round_item(++round, lane);
+      if (t < a.num_items) it = attn_item(a, t);
+    }
+  }
+};
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulation: the A operand (M rows in lanes, K along
 // the columns, two bf16 per 32-bit column) is read from tensor memory.
@@ -140,45 +156,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = smem;
-  uint8_t* sk = sq + kQBytes;             // K ring: kSlots x 32 KB
-  uint8_t* sv = sk + kSlots * kKBytes;    // V ring: kSlots x 32 KB
-  float* lsum = reinterpret_cast<float*>(sv + kSlots * kVBytes);  // [2 buffers][2 halves][128 rows]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(lsum + 2 * 2 * kTile);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;    // [2]
-  uint64_t* k_empty = bars + 4;   // [2]
-  uint64_t* v_full = bars + 6;    // [2]
-  uint64_t* v_empty = bars + 8;   // [2]
-  uint64_t* s_full = bars + 10;   // [2]
-  uint64_t* s_empty = bars + 12;  // [2]
-  uint64_t* p_full = bars + 14;
-  uint64_t* pv_full = bars + 15;
-  uint64_t* o_empty = bars + 16;
-  uint64_t* final_bar = bars + 17;
-  uint64_t* l_ready = bars + 18;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  // per lane: Q tile | kRing K / V slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * (kQBytes + kRing * kSlotBytes));
+  // per lane L, at bars + 16 L: ring full [kRing], ring empty [kRing], q_full, q_empty, s_full, p_full, o_full,
+  // o_empty, final
+  constexpr int kBarsPerLane = 16;
+  static_assert(2 * kRing + 7 <= kBarsPerLane, "barrier block");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kBarsPerLane);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], kSoftmaxWarps);
-      mbar_init(&l_ready[s], kSoftmaxWarps);
+    for (int l = 0; l < 2; ++l) {
+      uint64_t* b = bars + kBarsPerLane * l;
+      for (int s = 0; s < kRing; ++s) {
+        mbar_init(&b[s], 1);
+        mbar_init(&b[kRing + s], 1);
+      }
+      mbar_init(&b[2 * kRing + 0], 1);           // q_full
+      mbar_init(&b[2 * kRing + 1], 1);           // q_empty
+      mbar_init(&b[2 * kRing + 2], 1);           // s_full
+      mbar_init(&b[2 * kRing + 3], kLaneWarps);  // p_full
+      mbar_init(&b[2 * kRing + 4], 1);           // o_full
+      mbar_init(&b[2 * kRing + 5], kLaneWarps);  // o_empty
+      mbar_init(&b[2 * kRing + 6], 1);           // final
     }
-    mbar_init(p_full, kSoftmaxWarps);
-    mbar_init(pv_full, 1);
-    mbar_init(o_empty, kSoftmaxWarps);
-    mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -192,193 +195,234 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t tmo = a.timeout_ns;
 
-  if (warp == 0 && lane == 0) {
+  // the lane a control warp serves: warps 0 and 1 lane 0, warps 10 and 11 lane 1
+  const int ctl_lane = warp >= 10 ? 1 : 0;
+  uint8_t* sq = smem + ctl_lane * (kQBytes + kRing * kSlotBytes);
+  uint8_t* ring = sq + kQBytes;
+  uint64_t* lb = bars + kBarsPerLane * ctl_lane;
+  uint64_t* ring_full = lb;
+  uint64_t* ring_empty = lb + kRing;
+  uint64_t* q_full = lb + 2 * kRing;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* s_full = q_full + 2;
+  uint64_t* p_full = q_full + 3;
+  uint64_t* o_full = q_full + 4;
+  uint64_t* o_empty = q_full + 5;
+  uint64_t* final_bar = q_full + 6;
+
+  if ((warp == 0 || warp == 10) && lane == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t q_phase = 0, k_count = 0, v_count = 0;
-    uint32_t issued_q = 0, issued_k = 0, issued_v = 0, k_parity = 0, v_parity = 0;
+    const int L = ctl_lane;
+    uint32_t g = 0, q_count = 0;  // ring loads and Q loads issued
+    uint32_t ring_issued = 0, ring_parity = 0;
     bool ok = true;
-    // one K or V block into its ring slot (waits until the slot's previous block has been read)
-    auto load_block = [&](bool is_k, uint32_t idx, const CUtensorMap* mqk, const CUtensorMap* mv, int col, int y,
-                          int t) -> bool {
-      const uint32_t st = idx & 1, ph = (idx >> 1) & 1;
-      uint64_t* full = is_k ? &k_full[st] : &v_full[st];
-      if (!mbar_wait(is_k ? &k_empty[st] : &v_empty[st], ph ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t))
-        return false;
+    // one K block (two boxes of 64 dh x 128 keys) or one V block (the MN-major B operand: per 64-key block,
+    // two boxes of 64 dh x 64 keys) into the next ring slot
+    auto load_block = [&](bool is_k, const AttnItem& it, int j, int t) -> bool {
+      const uint32_t st = g % kRing, ph = (g / kRing) & 1;
+      if (!mbar_wait(&ring_empty[st], ph ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t)) return false;
+      uint8_t* dst = ring + st * kSlotBytes;
+      const int y = a.row0 + it.b * a.S + j * kTile;
+      mbar_arrive_expect_tx(&ring_full[st], kSlotBytes);
       if (is_k) {
-        uint8_t* dst = sk + st * kKBytes;
-        mbar_arrive_expect_tx(full, kKBytes);
-        tma_load_2d(dst, mqk, full, col, y);
-        tma_load_2d(dst + kSub, mqk, full, col + 64, y);
-        issued_k |= 1u << st;
-        k_parity = (k_parity & ~(1u << st)) | (ph << st);
+        const int kx = (a.Hp + it.h) * kTile;
+        tma_load_2d(dst, &a.map_qk[it.p], &ring_full[st], kx, y);
+        tma_load_2d(dst + kSub, &a.map_qk[it.p], &ring_full[st], kx + 64, y);
       } else {
-        // V as the MN-major B operand: per 64-key block, two boxes of 64 dh x 64 keys
-        uint8_t* dst = sv + st * kVBytes;
-        mbar_arrive_expect_tx(full, kVBytes);
+        const int vx = (2 * a.Hp + it.h) * kTile;
         for (int kb = 0; kb < 2; ++kb) {
-          tma_load_2d(dst + kb * kSub, mv, full, col, y + kb * 64);
-          tma_load_2d(dst + kb * kSub + 8192, mv, full, col + 64, y + kb * 64);
+          tma_load_2d(dst + kb * kSub, &a.map_v[it.p], &ring_full[st], vx, y + kb * 64);
+          tma_load_2d(dst + kb * kSub + 8192, &a.map_v[it.p], &ring_full[st], vx + 64, y + kb * 64);
         }
-        issued_v |= 1u << st;
-        v_parity = (v_parity & ~(1u << st)) | (ph << st);
       }
+      ring_issued |= 1u << st;
+      ring_parity = (ring_parity & ~(1u << st)) | (ph << st);
+      ++g;
       return true;
     };
-    for (int k = 0, t = attn_round_item(0); t < a.num_items && ok && !*abort_flag; t = attn_round_item(++k)) {
-      const AttnItem it = attn_item(a, t);
-      const CUtensorMap* mqk = &a.map_qk[it.p];
-      const CUtensorMap* mv = &a.map_v[it.p];
-      const int seq_row0 = a.row0 + it.b * a.S;
-      if (!mbar_wait(q_empty, q_phase ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, t)) break;
-      q_phase ^= 1;
-      mbar_arrive_expect_tx(q_full, kQBytes);
-      const int qx = it.h * kTile;
-      const int qy = seq_row0 + it.i * kTile;
-      tma_load_2d(sq, mqk, q_full, qx, qy);
-      tma_load_2d(sq + kSub, mqk, q_full, qx + 64, qy);
-      issued_q = 1;
-      const int kx = (a.Hp + it.h) * kTile;
-      const int vx = (2 * a.Hp + it.h) * kTile;
-      // K runs one block ahead of V: K_0, K_1, V_0, K_2, V_1, ..., V_i
-      for (int j = 0; j <= it.i + 1 && ok; ++j) {
-        if (j <= it.i) ok = load_block(true, k_count++, mqk, mv, kx, seq_row0 + j * kTile, t);
-        if (ok && j >= 1) ok = load_block(false, v_count++, mqk, mv, vx, seq_row0 + (j - 1) * kTile, t);
+    LaneWalk lw;
+    lw.start(a, L);
+    while (ok && !*abort_flag && !lw.done(a)) {
+      // one step: the previous block's V, then the current block's Q (first block) and K
+      if (lw.has_prev) ok = load_block(false, lw.prev_it, lw.prev_j, lw.t);
+      if (ok && lw.has_cur(a)) {
+        if (lw.j == 0) {  // the item's Q tile, once the lane's previous item has issued its last scores
+          if (!mbar_wait(q_empty, (q_count & 1) ^ 1, abort_flag, tmo, a.status, kSiteProducerEmpty, lw.t)) break;
+          ++q_count;
+          const int qx = lw.it.h * kTile;
+          const int qy = a.row0 + lw.it.b * a.S + lw.it.i * kTile;
+          mbar_arrive_expect_tx(q_full, kQBytes);
+          tma_load_2d(sq, &a.map_qk[lw.it.p], q_full, qx, qy);
+          tma_load_2d(sq + kSub, &a.map_qk[lw.it.p], q_full, qx + 64, qy);
+        }
+        ok = load_block(true, lw.it, lw.j, lw.t);
       }
+      lw.advance(a, L);
     }
     // drain: every load issued has landed before the CTA can exit
     volatile int no_abort = 0;
-    if (issued_q) mbar_wait(q_full, (q_phase ^ 1) & 1, &no_abort, tmo, a.status, kSiteDrain, 0);
-    for (int s = 0; s < 2; ++s) {
-      if (issued_k & (1u << s)) mbar_wait(&k_full[s], (k_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 1 + s);
-      if (issued_v & (1u << s)) mbar_wait(&v_full[s], (v_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 3 + s);
-    }
-  } else if (warp == 1 && lane == 0) {
+    if (q_count > 0) mbar_wait(q_full, (q_count - 1) & 1, &no_abort, tmo, a.status, kSiteDrain, 0);
+    for (int s = 0; s < kRing; ++s)
+      if (ring_issued & (1u << s))
+        mbar_wait(&ring_full[s], (ring_parity >> s) & 1, &no_abort, tmo, a.status, kSiteDrain, 1 + s);
+  } else if ((warp == 1 || warp == 11) && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    const int L = ctl_lane;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
-    uint32_t q_phase = 0, kv_count = 0, s_count = 0, p_phase = 0, o_phase = 0;
+    const uint32_t t_s = tmem_base + L * kTile;          // scores, then probabilities
+    const uint32_t t_o = tmem_base + kOCol + L * kTile;  // output accumulator
     const uint32_t qa = smem_u32(sq);
-    bool ok = true;
-    for (int k = 0, t = attn_round_item(0); t < a.num_items && ok && !*abort_flag; t = attn_round_item(++k)) {
-      const AttnItem it = attn_item(a, t);
-      if (!mbar_wait(q_full, q_phase, abort_flag, tmo, a.status, kSiteMmaFull, t)) break;
-      q_phase ^= 1;
-      const uint32_t kv0 = kv_count;  // K and V blocks are counted alike
-      if (!attn_issue_s(a, tmem_base, qa, sk, k_full, k_empty, s_empty, s_full, kv_count, s_count, abort_flag, t))
-        break;
-      if (it.i == 0) mma_commit(q_empty);  // Q is read by the score MMAs only: free after the item's last one
-      // the output accumulator is free once the previous item's output has been read
-      if (!mbar_wait(o_empty, o_phase ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, t)) break;
-      o_phase ^= 1;
-      for (int j = 0; j <= it.i; ++j) {
-        if (j + 1 <= it.i) {
-          if (!attn_issue_s(a, tmem_base, qa, sk, k_full, k_empty, s_empty, s_full, kv0 + j + 1, s_count + j + 1,
-                            abort_flag, t)) {
-            ok = false;
-            break;
-          }
-          if (j + 1 == it.i) mma_commit(q_empty);
+    uint32_t g = 0, q_count = 0, p_count = 0, o_items = 0;
+    LaneWalk lw;
+    lw.start(a, L);
+    while (!*abort_flag && !lw.done(a)) {
+      if (lw.has_prev) {
+        // ---- O += P V for the previous block, once its probabilities are written
+        const uint32_t st = g % kRing, ph = (g / kRing) & 1;
+        if (lw.prev_j == 0) {  // the accumulator is free once the lane's previous item's output was read
+          if (!mbar_wait(o_empty, (o_items & 1) ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, lw.t)) break;
+          ++o_items;
         }
-        const uint32_t vi = kv0 + j, st = vi & 1;
-        if (!mbar_wait(p_full, p_phase, abort_flag, tmo, a.status, kSiteAttnP, t) ||
-            !mbar_wait(&v_full[st], (vi >> 1) & 1, abort_flag, tmo, a.status, kSiteMmaFull, t)) {
-          ok = false;
+        if (!mbar_wait(p_full, p_count & 1, abort_flag, tmo, a.status, kSiteAttnP, lw.t) ||
+            !mbar_wait(&ring_full[st], ph, abort_flag, tmo, a.status, kSiteMmaFull, lw.t))
           break;
-        }
-        p_phase ^= 1;
+        ++p_count;
         tc_fence_after_sync();
-        const uint32_t va = smem_u32(sv + st * kVBytes);
+        const uint32_t va = smem_u32(ring + st * kSlotBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // 16 keys per step: 8 columns of P in tensor memory
           const uint64_t bd = smem_desc_mn128(va + (k >> 2) * kSub) + (2048 >> 4) * (k & 3);
-          mma_bf16_ts(tmem_base + kOCol, tmem_base + kPCol + 8 * k, bd, idesc_pv, (j | k) != 0 ? 1u : 0u);
+          mma_bf16_ts(t_o, t_s + kPCol + 8 * k, bd, idesc_pv, (lw.prev_j | k) != 0 ? 1u : 0u);
         }
-        mma_commit(pv_full);
-        mma_commit(&v_empty[st]);
+        mma_commit(&ring_empty[st]);
+        if (lw.prev_j == lw.prev_it.i) mma_commit(o_full);
+        ++g;
       }
-      kv_count = kv0 + it.i + 1;
-      s_count += it.i + 1;
-      if (!ok) break;
+      if (lw.has_cur(a)) {
+        // ---- S = Q K^T for the current block, into the columns P just left
+        const uint32_t st = g % kRing, ph = (g / kRing) & 1;
+        if (lw.j == 0) {
+          if (!mbar_wait(q_full, q_count & 1, abort_flag, tmo, a.status, kSiteMmaFull, lw.t)) break;
+          ++q_count;
+        }
+        if (!mbar_wait(&ring_full[st], ph, abort_flag, tmo, a.status, kSiteMmaFull, lw.t)) break;
+        tc_fence_after_sync();
+        const uint32_t ka = smem_u32(ring + st * kSlotBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ad = smem_desc_k128(qa + (k >> 2) * kSub) + 2 * (k & 3);
+          const uint64_t bd = smem_desc_k128(ka + (k >> 2) * kSub) + 2 * (k & 3);
+          mma_bf16_ss(t_s, ad, bd, idesc_s, k != 0 ? 1u : 0u);
+        }
+        mma_commit(&ring_empty[st]);
+        mma_commit(s_full);
+        if (lw.j == lw.it.i) mma_commit(q_empty);  // the item's last scores: its Q tile is free
+        ++g;
+      }
+      lw.advance(a, L);
     }
     mma_commit(final_bar);
     volatile int no_abort = 0;
     mbar_wait(final_bar, 0, &no_abort, tmo, a.status, kSiteDrain, 99);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 10) {
     // --------------------------------------------------- softmax / output
+    const int L = (warp - 2) / kLaneWarps;
+    uint64_t* sb = bars + kBarsPerLane * L + 2 * kRing;  // this lane's q_full .. final
+    uint64_t* s_full = sb + 2;
+    uint64_t* p_full = sb + 3;
+    uint64_t* o_full = sb + 4;
+    uint64_t* o_empty = sb + 5;
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;   // key / output columns half * 64 .. + 64
     const int r = quarter * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t to = tmem_base + lane_off + kOCol + half * 64;  // this thread's half of the output row
-    uint32_t s_count = 0, pv_phase = 0, item_count = 0;
-    for (int k = 0, t = attn_round_item(0); t < a.num_items && !*abort_flag; t = attn_round_item(++k), ++item_count) {
+    const uint32_t ts = tmem_base + lane_off + L * kTile;          // this row's scores / probabilities
+    const uint32_t to = tmem_base + lane_off + kOCol + L * kTile;  // this row's output accumulator
+    const float c = a.scale_log2;
+    uint32_t s_count = 0, item_count = 0;
+    for (int k = 0, t = attn_round_item(0, L); t < a.num_items && !*abort_flag;
+         t = attn_round_item(++k, L), ++item_count) {
       const AttnItem it = attn_item(a, t);
       float m_run = -INFINITY, l_run = 0.0f;
       bool ok = true;
       for (int j = 0; j <= it.i; ++j, ++s_count) {
-        const uint32_t sb = s_count & 1;
-        if (!mbar_wait(&s_full[sb], (s_count >> 1) & 1, abort_flag, tmo, a.status, kSiteEpilogueTmemFull, t)) {
+        if (!mbar_wait(s_full, s_count & 1, abort_flag, tmo, a.status, kSiteEpilogueTmemFull, t)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t ts = tmem_base + lane_off + sb * kTile;
-        const bool diag = j == it.i;
-        // the row's 128 scores in two batches of tensor-memory loads: this thread's own 64 keys (half * 64 ..)
-        // stay in registers for the probabilities, the other 64 serve only the maximum (two batches, as all
-        // 128 at once would not fit the 168 registers a thread of this 10-warp block can have)
-        uint32_t vo0[32], vo1[32];
+        const bool diag = j == it.i;  // keys 0 .. r of this block are visible to row r
+        // pass 1: the row maximum of the visible scores, in two batches of 64 columns; the second batch stays
+        // in registers for pass 2
         float mx = -INFINITY;
+        uint32_t w0[32], w1[32];
         {
-          const int ko = half * 64, kx = (half ^ 1) * 64;
-          uint32_t vx[32];
-          tmem_ld_32x32b_x32(ts + ko, vo0);
-          tmem_ld_32x32b_x32(ts + ko + 32, vo1);
-          tmem_ld_32x32b_x32(ts + kx, vx);
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(ts, v0);
+          tmem_ld_32x32b_x32(ts + 32, v1);
           tmem_ld_wait();
-          // pass 1: row maximum of the visible scores
+          tmem_ld_32x32b_x32(ts + 64, w0);
+          tmem_ld_32x32b_x32(ts + 96, w1);
           if (diag) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              if (ko + e <= r) mx = fmaxf(mx, __uint_as_float(vo0[e]));
-              if (ko + 32 + e <= r) mx = fmaxf(mx, __uint_as_float(vo1[e]));
-              if (kx + e <= r) mx = fmaxf(mx, __uint_as_float(vx[e]));
+              if (e <= r) mx = fmaxf(mx, __uint_as_float(v0[e]));
+              if (32 + e <= r) mx = fmaxf(mx, __uint_as_float(v1[e]));
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = max3(mx, __uint_as_float(vo0[e]), __uint_as_float(vo1[e]));
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) mx = max3(mx, __uint_as_float(vx[e]), __uint_as_float(vx[e + 1]));
+            for (int e = 0; e < 32; ++e) mx = max3(mx, __uint_as_float(v0[e]), __uint_as_float(v1[e]));
           }
-          tmem_ld_32x32b_x32(ts + kx + 32, vx);
           tmem_ld_wait();
           if (diag) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (kx + 32 + e <= r) mx = fmaxf(mx, __uint_as_float(vx[e]));
+            for (int e = 0; e < 32; ++e) {
+              if (64 + e <= r) mx = fmaxf(mx, __uint_as_float(w0[e]));
+              if (96 + e <= r) mx = fmaxf(mx, __uint_as_float(w1[e]));
+            }
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) mx = max3(mx, __uint_as_float(vx[e]), __uint_as_float(vx[e + 1]));
+            for (int e = 0; e < 32; ++e) mx = max3(mx, __uint_as_float(w0[e]), __uint_as_float(w1[e]));
           }
         }
-        const float m_blk = mx * a.scale_log2;
-        const bool rescale = m_blk > m_run + kRescaleLog2;
+        const float m_blk = mx * c;
+        const bool grow_m = m_blk > m_run + kRescaleLog2;
         float alpha = 1.0f;
-        if (rescale) {
-          alpha = ex2_approx(m_run - m_blk);
+        if (grow_m) {
+          alpha = ex2_approx(m_run - m_blk);  // 0 for the first block
           m_run = m_blk;
         }
-        // pass 2: this thread's 64 probabilities, packed as bf16 pairs
-        uint32_t pk[32];
-        float sum_even = 0.0f, sum_odd = 0.0f;  // the row sum of this thread's even and odd keys
-        {
-          const float c = a.scale_log2, nm = -m_run;
+        // tensor-memory loads and stores are warp-wide: the whole warp rescales its rows (alpha = 1 where the
+        // maximum stayed) once the previous P V has finished (its completion preceded these scores')
+        if (j > 0 && __any_sync(0xffffffffu, grow_m)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(to + cc * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float y0, y1;
+              mul2(y0, y1, __uint_as_float(v[e]), __uint_as_float(v[e + 1]), alpha, alpha);
+              v[e] = __float_as_uint(y0);
+              v[e + 1] = __float_as_uint(y1);
+            }
+            tmem_st_32x32b_x32(to + cc * 32, v);
+          }
+        }
+        // pass 2: the 128 probabilities as bf16 pairs over score columns 64-127 (keys 2q, 2q + 1 -> column
+        // 64 + q).  Keys 64-127 first, from the registers of pass 1 (their probabilities overwrite the scores
+        // of those keys), then keys 0-63, reloaded (their probabilities overwrite scores 64-95, already read).
+        float sum_even = 0.0f, sum_odd = 0.0f;
+        const float nm = -m_run;
+        auto probs = [&](const uint32_t (&x0)[32], const uint32_t (&x1)[32], int kbase, uint32_t (&pk)[32]) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int k0 = half * 64 + 2 * e, k1 = k0 + 32;
-            float x0, x1, x2, x3;
-            fma2(x0, x1, __uint_as_float(vo0[2 * e]), __uint_as_float(vo0[2 * e + 1]), c, c, nm, nm);
-            fma2(x2, x3, __uint_as_float(vo1[2 * e]), __uint_as_float(vo1[2 * e + 1]), c, c, nm, nm);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            const int k0 = kbase + 2 * e, k1 = k0 + 32;
+            float y0, y1, y2, y3;
+            fma2(y0, y1, __uint_as_float(x0[2 * e]), __uint_as_float(x0[2 * e + 1]), c, c, nm, nm);
+            fma2(y2, y3, __uint_as_float(x1[2 * e]), __uint_as_float(x1[2 * e + 1]), c, c, nm, nm);
+            float p0 = ex2_approx(y0), p1 = ex2_approx(y1), p2 = ex2_approx(y2), p3 = ex2_approx(y3);
             if (diag) {
               p0 = k0 <= r ? p0 : 0.0f;
               p1 = k0 + 1 <= r ? p1 : 0.0f;
@@ -390,78 +434,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
             pk[e] = pack_bf16(p0, p1);
             pk[16 + e] = pack_bf16(p2, p3);
           }
+        };
+        {
+          uint32_t pk[32];
+          probs(w0, w1, 64, pk);
+          tmem_st_32x32b_x32(ts + kPCol + 32, pk);
         }
-        const float sum = sum_even + sum_odd;
-        // P_{j-1} V_{j-1} has landed: the P buffer is free and the output up to date
-        if (j > 0) {
-          if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
-            ok = false;
-            break;
-          }
-          pv_phase ^= 1;
-          tc_fence_after_sync();
-          if (rescale) {
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              uint32_t v[32];
-              tmem_ld_32x32b_x32(to + cc * 32, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                float y0, y1;
-                mul2(y0, y1, __uint_as_float(v[e]), __uint_as_float(v[e + 1]), alpha, alpha);
-                v[e] = __float_as_uint(y0);
-                v[e + 1] = __float_as_uint(y1);
-              }
-              tmem_st_32x32b_x32(to + cc * 32, v);
-            }
-            tmem_st_wait();
-          }
+        {
+          uint32_t v0[32], v1[32], pk[32];
+          tmem_ld_32x32b_x32(ts, v0);
+          tmem_ld_32x32b_x32(ts + 32, v1);
+          tmem_ld_wait();
+          probs(v0, v1, 0, pk);
+          tmem_st_32x32b_x32(ts + kPCol, pk);
         }
-        // this thread's 64 keys as 32 bf16 pairs: pk[c] holds keys half * 64 + 2c, + 1 -> P column half * 32 + c
-        tmem_st_32x32b_x32(tmem_base + lane_off + kPCol + half * 32, pk);
         tmem_st_wait();
         tc_fence_before_sync();
-        __syncwarp();  // the warp's scores are read and its P stored: one arrival per warp
-        if (lane == 0) {
-          mbar_arrive(&s_empty[sb]);
-          mbar_arrive(p_full);
-        }
-        l_run = l_run * alpha + sum;
+        __syncwarp();  // the warp's probabilities (and any rescaled output) are written: one arrival per warp
+        if (lane == 0) mbar_arrive(p_full);
+        l_run = l_run * alpha + (sum_even + sum_odd);
       }
       if (!ok) break;
-      // the last P V has landed: read this thread's half of the output row
-      if (!mbar_wait(pv_full, pv_phase, abort_flag, tmo, a.status, kSiteAttnPV, t)) break;
-      pv_phase ^= 1;
+      // the item's last P V has landed: read the output row, free the accumulator, store O / l as bf16
+      if (!mbar_wait(o_full, item_count & 1, abort_flag, tmo, a.status, kSiteAttnPV, t)) break;
       tc_fence_after_sync();
-      uint32_t o0[32], o1[32];
-      tmem_ld_32x32b_x32(to, o0);
-      tmem_ld_32x32b_x32(to + 32, o1);
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_empty);
-      // the row sum: this thread's part plus its partner's, through shared memory
-      const uint32_t lb = item_count & 1;
-      float* lbuf = lsum + lb * 2 * kTile;
-      lbuf[half * kTile + r] = l_run;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&l_ready[lb]);
-      if (!mbar_wait(&l_ready[lb], (item_count >> 1) & 1, abort_flag, tmo, a.status, kSiteAttnPV, t)) break;
-      const float inv = 1.0f / (lbuf[r] + lbuf[kTile + r]);
-      // O / l as bf16: this thread's 128 contiguous bytes of the row
       const int64_t grow = a.row0 + static_cast<int64_t>(it.b) * a.S + it.i * kTile + r;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o[it.p]) + grow * a.ldo + it.h * kTile +
-                                            half * 64);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o[it.p]) + grow * a.ldo + it.h * kTile);
+      const float inv = 1.0f / l_run;
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const uint32_t* oh = q8 < 4 ? o0 + 8 * q8 : o1 + 8 * (q8 - 4);
-        float y[8];
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t o0[32], o1[32];
+        tmem_ld_32x32b_x32(to + hb * 64, o0);
+        tmem_ld_32x32b_x32(to + hb * 64 + 32, o1);
+        tmem_ld_wait();
+        if (hb == 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_empty);
+        }
 #pragma unroll
-        for (int e = 0; e < 8; e += 2)
-          mul2(y[e], y[e + 1], __uint_as_float(oh[e]), __uint_as_float(oh[e + 1]), inv, inv);
-        dst[q8] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                             pack_bf16(y[6], y[7]));
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const uint32_t* oh = q8 < 4 ? o0 + 8 * q8 : o1 + 8 * (q8 - 4);
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            mul2(y[e], y[e + 1], __uint_as_float(oh[e]), __uint_as_float(oh[e + 1]), inv, inv);
+          dst[hb * 8 + q8] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                                        pack_bf16(y[6], y[7]));
+        }
       }
     }
   }
@@ -508,7 +528,8 @@ domino_status_t launch_attn_fwd(const AttnLaunch& L, int num_sms, cudaStream_t s
   a.status = L.status;
   a.timeout_ns = L.timeout_ns;
   if (a.num_items == 0) return DOMINO_OK;
-  const int grid = a.num_items < num_sms ? a.num_items : num_sms;
+  const int lanes_needed = (a.num_items + 1) / 2;  // two lanes of items per CTA
+  const int grid = lanes_needed < num_sms ? lanes_needed : num_sms;
   void* args[] = {&a};
   const cudaError_t st = cudaLaunchKernel(reinterpret_cast<const void*>(&attn_fwd_kernel), dim3(grid),
                                           dim3(kAttnThreads), args, kAttnSmemBytes, stream);
