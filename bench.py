@@ -48,6 +48,7 @@ def load_peaks():
 _GEMM_SOURCES = ("common.h", "epilogue.cuh", "gemm.cu", "gemm.h", "gemm_pair.cu", "ptx.cuh")
 KERNEL_SOURCES = {
     "fused": ("common.h", "epilogue.cuh", "fused.cu", "gemm.h", "ptx.cuh"),
+    "bwd_dx_fused": ("common.h", "epilogue.cuh", "fused.cu", "gemm.h", "ptx.cuh"),
     "gemm1": _GEMM_SOURCES, "gemm2": _GEMM_SOURCES,
     "bwd_dh": _GEMM_SOURCES, "bwd_dx": _GEMM_SOURCES, "bwd_dw": _GEMM_SOURCES,
     "shard_sum": ("common.h", "gemm.h", "ptx.cuh", "shard_sum.cu"),
@@ -411,14 +412,24 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- fused schedule: reduction time left after the last GEMM tile, from the
     # kernel's own %globaltimer stamps (read back after each of a few extra calls)
     fused_exposed = None
+    fused_exposed_parts = None
     if args.schedule == "fused":
-        ex = []
+        ex_f, ex_b = [], []
         for _ in range(20):
             b.mlp_fwd(X, A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, schedule="fused", Y=Y,
                       workspace=ws, saved=saved if w.bwd else None)
             tl = b.read_timeline(ws)
-            ex.append(max(0, tl["reduce_end_ns"] - tl["gemm_end_ns"]) * 1e-6)
-        fused_exposed = statistics.mean(ex)
+            ex_f.append(max(0, tl["reduce_end_ns"] - tl["gemm_end_ns"]) * 1e-6)
+            if w.bwd:  # the backward's partial input gradients and their shard-sum: one cooperative launch
+                b.mlp_bwd(X, A_sh, B_sh, dY, saved, F=w.F, mu=w.mu, act=w.act, partial=w.partial,
+                          out_slices=w.slices, schedule="fused", dX=dX, dA_shards=dA_sh, dB_shards=dB_sh,
+                          workspace=ws)
+                tl = b.read_timeline(ws)
+                ex_b.append(max(0, tl["reduce_end_ns"] - tl["gemm_end_ns"]) * 1e-6)
+        fused_exposed = statistics.mean(ex_f) + (statistics.mean(ex_b) if ex_b else 0.0)
+        fused_exposed_parts = {"fwd_us": round(1e3 * statistics.mean(ex_f), 2)}
+        if ex_b:
+            fused_exposed_parts["bwd_us"] = round(1e3 * statistics.mean(ex_b), 2)
 
     # ---- A/B measure of the reduction's cost: the same call without the shard-sum, alternating with the full
     # call (L2 flushed before each).  domino_mlp_fwd_partials runs the same GEMM tiles in the same order and
@@ -562,6 +573,7 @@ def run_ours(args, w, rank, world, local_rank):
         return {"fused": float(w.fwd_flops()),
                 "gemm1": 2.0 * w.Mc * w.d * w.F * nact, "gemm2": 2.0 * w.Mc * w.F * ds_,
                 "bwd_dh": 2.0 * w.M * w.d * w.F, "bwd_dx": 2.0 * w.Mc * nact * w.F * ds_,
+                "bwd_dx_fused": 2.0 * w.M * nact * w.F * w.d,
                 "bwd_dw": 2.0 * w.M * w.d * w.F * (nact if r["slice"] == 0 else 1)}.get(r["kind"], 0.0)
 
     psize = 4 if w.partial == "f32" else 2
@@ -584,8 +596,8 @@ def run_ours(args, w, rank, world, local_rank):
     calls_per_step = 2 if w.bwd else 1
     span_ms *= calls_per_step
     exposed_ms *= calls_per_step
-    if fused_exposed is not None:  # the fused forward reduces inside the kernel: use its device timeline
-        exposed_ms = fused_exposed + (exposed_ms * (calls_per_step - 1) / calls_per_step if w.bwd else 0.0)
+    if fused_exposed is not None:  # the fused kernels reduce inside the launch: use their device timelines
+        exposed_ms = fused_exposed
 
     flops = w.fwd_flops() + (w.bwd_flops() if w.bwd else 0)
     value = whole_job_tflops(flops, world, mean_ms)
@@ -613,10 +625,13 @@ def run_ours(args, w, rank, world, local_rank):
         "exposed_reduce_method": "fused: the kernel's own %globaltimer stamps, last GEMM tile end to last "
                                  "shard-sum piece end; streams/serial: call span minus the union of GEMM launch "
                                  "intervals (CUDA events)",
+        "exposed_reduce_us_per_call": fused_exposed_parts,
         "exposed_reduce_ab_us_per_layer": None if ab is None else ab["exposed_us"],
         "exposed_reduce_ab": ab,
         "roofline": {
-            "kernel": {"fused": "fused_fwd_pair_kernel (both projections and the shard-sum, one launch)"}.get(
+            "kernel": {"fused": "fused_fwd_pair_kernel (both projections and the shard-sum, one launch)",
+                       "bwd_dx_fused": "fused_fwd_pair_kernel, backward mode (partial input gradients of every "
+                                       "chunk and their shard-sum, one launch)"}.get(
                 dominant, f"gemm_pair_kernel ({dominant})"),
             "note": "achieved = algorithmic flops of the kernel's launches / their summed event durations; peak = "
                     "the burst bf16 figure for launches under a second, else the sustained one",

@@ -20,7 +20,8 @@ STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTE
 ACT = {"gelu": 0, "gelu_tanh": 1, "swiglu": 2, "identity": 3}
 PARTIAL = {"f32": 0, "bf16": 1}
 SCHEDULE = {"serial": 0, "streams": 1, "fused": 2}
-KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused", 7: "attn"}
+KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused", 7: "attn",
+               8: "bwd_dx_fused"}
 FLAG_KERNEL_TIMES = 1
 FLAG_ONE_CTA = 2
 MAX_SHARDS = 16

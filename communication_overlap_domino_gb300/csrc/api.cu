@@ -520,6 +520,37 @@ struct BwdSeq {
     return DOMINO_OK;
   }
 
+  // FUSED schedule: the partial input gradients of every chunk and their shard-sum in one cooperative launch
+  // (tile-granular overlap, as in the fused forward).  Returns DOMINO_ERR_UNSUPPORTED with nothing launched
+  // when the device cannot run it; the caller then issues dx_chunk() per chunk.
+  domino_status_t dx_fused(uint8_t* ws, const WsLayout& W, std::string* err) const {
+    FusedDxLaunch F;
+    for (int p = 0; p < s.P; ++p) {
+      F.dG[p] = dG[p];
+      F.W[p] = A_shards[p];
+      F.Z[p] = Z[p];
+    }
+    F.dX = dX;
+    F.sync = reinterpret_cast<uint32_t*>(ws + W.sync_off);
+    F.timeline = reinterpret_cast<uint64_t*>(ws + kTimelineOff);
+    F.M = s.M;
+    F.d = s.d;
+    F.K2 = nF();
+    F.mu = s.mu;
+    F.P = s.P;
+    F.partial_f32 = s.partial == DOMINO_PARTIAL_F32;
+    F.status = status;
+    F.timeout_ns = tmo;
+    if (ds->fused_pair_clusters < 1) return DOMINO_ERR_UNSUPPORTED;
+    cudaError_t e = cudaMemsetAsync(ws + kTimelineOff, 0, kSyncOff - kTimelineOff + W.sync_bytes, s0);
+    if (e != cudaSuccess) {
+      if (err) *err = std::string("counter reset: ") + cudaGetErrorString(e);
+      return DOMINO_ERR_CUDA;
+    }
+    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DX_FUSED, 0, 0,
+                 [&] { return launch_fused_dx(F, ds->fused_pair_clusters, s0, err); });
+  }
+
   // Weight gradients over all M (they run while the last shard-sum drains).
   domino_status_t dw(std::string* err) const {
     {
@@ -989,7 +1020,9 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != DOMINO_OK) return st;
-  cudaStream_t sr = s.schedule != DOMINO_SCHEDULE_SERIAL ? ds->reduce_stream : s0;  // FUSED: streams for the backward
+  // FUSED: dH, one cooperative launch for the partial input gradients of every chunk and their shard-sum, then
+  // the weight gradients (STREAMS if the device cannot run the cooperative launch)
+  cudaStream_t sr = s.schedule != DOMINO_SCHEDULE_SERIAL ? ds->reduce_stream : s0;
   const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DeviceStatus* dstat = reinterpret_cast<DeviceStatus*>(ws);
@@ -1020,7 +1053,13 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   std::string err;
   fork_streams(ds, s0, sr);
   st = g.dh(&err);
-  for (int k = 0; k < s.mu && st == DOMINO_OK; ++k) st = g.dx_chunk(k, &err);
+  bool fused_dx = false;
+  if (st == DOMINO_OK && s.schedule == DOMINO_SCHEDULE_FUSED && pair) {
+    const domino_status_t fs = g.dx_fused(ws, W, &err);
+    if (fs == DOMINO_OK) fused_dx = true;
+    else if (fs != DOMINO_ERR_UNSUPPORTED) st = fs;
+  }
+  for (int k = 0; k < s.mu && st == DOMINO_OK && !fused_dx; ++k) st = g.dx_chunk(k, &err);
   if (st == DOMINO_OK) st = g.dw(&err);
   if (st != DOMINO_OK) return fail(st, err);
   join_streams(ds, s0, sr);

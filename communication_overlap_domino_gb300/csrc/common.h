@@ -123,7 +123,9 @@ struct FusedParams {
   int32_t num_gemm_tiles, num_red_items;
   int32_t tiles_m2, tiles_a2, tiles_b2;  // paired kernel: 256-row blocks, tiles per chunk and phase
   int32_t num_pair_tiles;
-  int32_t kb1, kb2;                  // K blocks of GEMM1 (d) and GEMM2 (Fp)
+  int32_t kb1, kb2;                  // K blocks of GEMM1 (d) and GEMM2 (Fp, or the backward's nact Fp)
+  int32_t a2_input;                  // 1: GEMM2's A operand is an input complete before the launch (no GEMM1
+                                     // tiles, no H counters): the backward's partial input gradients
   DeviceStatus* status;
   uint64_t timeout_ns;
 };

@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_fwd_kernel(const __gri
 // epilogue drains, stores and publishes its own 128-row block, so the counters
 // and the shard-sum pieces are the same as in the one-CTA kernel.  The odd
 // CTA's warp 1, which issues no MMAs, works on the shard-sum from the start.
-template <int EPI_A, int EPI_B>
+template <int EPI_A, int EPI_B, bool B2_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     fused_fwd_pair_kernel(const __grid_constant__ FusedParams f) {
   constexpr int kPStages = 6;
@@ -574,7 +574,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- TMA producer
-    prefetch_tmap(&f.map_x);
+    if (!f.a2_input) prefetch_tmap(&f.map_x);
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);
@@ -593,7 +593,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
         yb = T.n * f.n_tile1 + (leader ? 0 : f.b1_off1);
         nkb = f.kb1;
       } else {
-        if (m < f.tiles_m) {
+        if (m < f.tiles_m && !f.a2_input) {
           const uint32_t* ctr = f.hcnt + (T.k * f.P + T.p) * f.tiles_m + m;
           if (!wait_counter(ctr, static_cast<uint32_t>(f.tiles_n1) * 4, abort_flag, tmo, f.status, kSiteFusedH, t))
             break;
@@ -617,7 +617,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
         const uint32_t bar = full0 + stage * 8;
         const int k0 = kb * kBK;
         tma_load_2d_pair(sa, ma, bar, k0, ya, keep_a);
-        tma_load_2d_pair(sb, mb, bar, k0, yb);
+        if (B2_MN && T.phase == 1) {
+          // the CTA's 128 output columns of B, stored [K][N]: two boxes of 64 columns x 64 K rows
+          tma_load_2d_pair(sb, mb, bar, yb, k0);
+          tma_load_2d_pair(sb + 8192, mb, bar, yb + 64, k0);
+        } else {
+          tma_load_2d_pair(sb, mb, bar, k0, yb);
+        }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kPStages) {
@@ -637,12 +643,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     }
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------- MMA issuer (even CTA)
-    constexpr uint32_t idesc = idesc_bf16_f32(256, kBN);
+    constexpr uint32_t idesc_a = idesc_bf16_f32(256, kBN);
+    constexpr uint32_t idesc_b = idesc_bf16_f32(256, kBN, false, B2_MN);
     uint32_t stage = 0, phase = 0;
     int i = 0;
     for (int t = cluster_id; t < num_tiles && !*abort_flag; t += num_clusters, ++i) {
       const FusedTile T = fused_pair_tile(f, t);
       const int nkb = T.phase == 0 ? f.kb1 : f.kb2;
+      const bool b_mn = B2_MN && T.phase == 1;
       const uint32_t acc = i & 1;
       const uint32_t acc_phase = (i >> 1) & 1;
       if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1, abort_flag, tmo, f.status, kSiteMmaTmemEmpty, t)) break;
@@ -656,10 +664,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
         }
         tc_fence_after_sync();
         const uint64_t adesc = smem_desc_k128(smem_u32(smem_a + stage * kPA));
-        const uint64_t bdesc = smem_desc_k128(smem_u32(smem_b + stage * kPB));
+        if (b_mn) {  // MN-major B: a K step of 16 rows advances 2 KB
+          const uint64_t bdesc = smem_desc_mn128(smem_u32(smem_b + stage * kPB));
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          mma_bf16_ss_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss_pair(d_tmem, adesc + 2 * k, bdesc + (2048 >> 4) * k, idesc_b, (kb | k) != 0 ? 1u : 0u);
+        } else {
+          const uint64_t bdesc = smem_desc_k128(smem_u32(smem_b + stage * kPB));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_a, (kb | k) != 0 ? 1u : 0u);
+        }
         mma_commit_pair_multicast(&empty_bar[stage], 0x3);
         if (++stage == kPStages) {
           stage = 0;
@@ -750,7 +765,13 @@ void* fused_ptr() {
 
 template <int A, int B>
 void* fused_pair_ptr() {
-  return reinterpret_cast<void*>(&fused_fwd_pair_kernel<A, B>);
+  return reinterpret_cast<void*>(&fused_fwd_pair_kernel<A, B, false>);
+}
+
+// The backward's dX kernel: no GEMM1 phase, GEMM2 with the MN-major weight shard as B.
+void* fused_dx_kernel_for(bool f32) {
+  return f32 ? reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_F32, true>)
+             : reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_BF16, true>);
 }
 
 void* fused_pair_kernel_for(int epi_a, bool f32) {
@@ -803,6 +824,19 @@ cudaError_t prepare_fused_kernels(int* max_ctas_per_sm, int* max_pair_clusters) 
       if (st != cudaSuccess) return st;
       clusters = n < clusters ? n : clusters;
     }
+  }
+  for (int f32 = 0; f32 < 2; ++f32) {
+    void* fn = fused_dx_kernel_for(f32 != 0);
+    cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    if (st != cudaSuccess) return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 512);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    int n = 0;
+    st = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (st != cudaSuccess) return st;
+    clusters = n < clusters ? n : clusters;
   }
   *max_pair_clusters = clusters;
   int occ = 1 << 30;
@@ -907,6 +941,66 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pai
     return DOMINO_ERR_CUDA;
   }
   return DOMINO_OK;
+}
+
+}  // namespace domino
+
+namespace domino {
+
+domino_status_t launch_fused_dx(const FusedDxLaunch& L, int max_pair_clusters, cudaStream_t stream, std::string* err) {
+  if (max_pair_clusters < 1) {
+    if (err) *err = "fused dX kernel: no paired cooperative launch on this device";
+    return DOMINO_ERR_UNSUPPORTED;
+  }
+  FusedParams f;
+  memset(&f, 0, sizeof f);
+  for (int p = 0; p < L.P; ++p) {
+    // A: dG_p [M, K2] K-major, 128-row boxes; B: A_shards[p] [K2, d] MN-major, 64 x 64 boxes
+    if (!encode_bf16_sw128(&f.map_h[p], Operand2D{L.dG[p], L.M, L.K2, L.K2}, kBM, err)) return DOMINO_ERR_CUDA;
+    if (!encode_bf16_sw128(&f.map_w2[p], Operand2D{L.W[p], L.K2, L.d, L.d}, kBK, err)) return DOMINO_ERR_CUDA;
+    if (!encode_store_map(&f.map_zout[p], L.Z[p], L.M, L.d, L.d, L.partial_f32, L.partial_f32 ? 32 : 64, err))
+      return DOMINO_ERR_CUDA;
+    f.z[p] = L.Z[p];
+  }
+  f.y = L.dX;
+  f.Mc = static_cast<int32_t>(L.M / L.mu);
+  f.tiles_m = (f.Mc + kBM - 1) / kBM;
+  f.tiles_n2 = static_cast<int32_t>((L.d + kBN - 1) / kBN);
+  f.hcnt = L.sync;
+  f.zcnt = L.sync + static_cast<int64_t>(L.mu) * L.P * f.tiles_m;
+  f.red_next = f.zcnt + static_cast<int64_t>(L.mu) * f.tiles_m * f.tiles_n2 * 4;
+  f.timeline = L.timeline;
+  f.d = L.d;
+  f.mu = L.mu;
+  f.P = L.P;
+  f.tiles_b = L.P * f.tiles_m * f.tiles_n2;
+  f.num_red_items = L.mu * f.tiles_m * f.tiles_n2;
+  f.kb2 = static_cast<int32_t>((L.K2 + kBK - 1) / kBK);
+  f.tiles_m2 = (f.tiles_m + 1) / 2;
+  f.tiles_a2 = 0;  // no GEMM1 phase
+  f.tiles_b2 = L.P * f.tiles_m2 * f.tiles_n2;
+  f.num_pair_tiles = L.mu * f.tiles_b2;
+  f.a2_input = 1;
+  f.status = L.status;
+  f.timeout_ns = L.timeout_ns;
+  if (f.num_pair_tiles == 0) return DOMINO_OK;
+  void* fn = fused_dx_kernel_for(L.partial_f32);
+  const int clusters = f.num_pair_tiles < max_pair_clusters ? f.num_pair_tiles : max_pair_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&f};
+  const cudaError_t st = cudaLaunchKernelExC(&cfg, fn, args);
+  if (st == cudaSuccess) return DOMINO_OK;
+  if (err) *err = std::string("fused dX launch: ") + cudaGetErrorString(st);
+  return DOMINO_ERR_UNSUPPORTED;
 }
 
 }  // namespace domino

@@ -94,13 +94,16 @@ typedef enum domino_schedule {
   DOMINO_SCHEDULE_SERIAL = 0, /* GEMMs and shard-sums in order on one stream: no overlap  */
   DOMINO_SCHEDULE_STREAMS = 1, /* shard-sum of piece (k,s) on a second stream, released by
                                   an event after its GEMM, overlapping the next piece      */
-  DOMINO_SCHEDULE_FUSED = 2    /* forward only: GEMM1, GEMM2 and the shard-sum of every chunk
-                                  in one persistent cooperative launch; the shard-sum of each
+  DOMINO_SCHEDULE_FUSED = 2    /* forward: GEMM1, GEMM2 and the shard-sum of every chunk in
+                                  one persistent cooperative launch; the shard-sum of each
                                   128x256 output tile starts as soon as its P partials are
-                                  stored, on the same SMs that keep running GEMM tiles.  The
-                                  result is bit-identical to the other schedules; out_slices
-                                  does not change the work (the pieces are already tiles).
-                                  domino_mlp_bwd runs the STREAMS schedule for it.          */
+                                  stored, on the same SMs that keep running GEMM tiles.
+                                  backward: dH, then the partial input gradients of every
+                                  chunk and their shard-sum in one such launch, then the
+                                  weight gradients (STREAMS if the device cannot run the
+                                  paired cooperative launch).  Results are bit-identical to
+                                  the other schedules; out_slices does not change the work
+                                  (the pieces are already tiles).                          */
 } domino_schedule_t;
 
 /* desc->flags */
@@ -178,7 +181,11 @@ DOMINO_API domino_status_t domino_mlp_fwd_partials(const domino_mlp_desc_t* desc
                                                    void* const* Z_shards, void* const* piece_events, void* saved,
                                                    void* workspace, size_t workspace_bytes, void* stream);
 
-/* Backward pass of the same block (chain rule), sliced the same way.
+/* Backward pass of the same block (chain rule), sliced the same way: the Domino
+ * page ("Domino: Eliminating Communication in LLM Training via Generic Tensor
+ * Slicing and Overlapping", Abstract) slices the data dependency of a whole
+ * training step, and the backward's exchange is the all-reduce of the input
+ * gradient's row-parallel partials, which the shard-sum stands in for here.
  * dY [M,d] in; dX [M,d] out; dA_shards[p] / dB_shards[p] out (bf16, the same
  * layouts as A_shards[p] / B_shards[p]).  `saved` must hold what domino_mlp_fwd
  * wrote for the same X and weights.  workspace: domino_mlp_workspace_size(desc, 1)
@@ -191,14 +198,19 @@ DOMINO_API domino_status_t domino_mlp_fwd_partials(const domino_mlp_desc_t* desc
  *     buffer, then dX_k[:, s] = sum over p of the partials (the shard-sum, in fp32,
  *     shard order; it overlaps the next chunk's GEMMs);
  * then, over all M: dA_p = dG_p^T X and dB_p = dY^T H_p (they overlap the last
- * chunk's shard-sum).  M == 0 writes zero weight gradients and touches nothing
+ * chunk's shard-sum).  With DOMINO_SCHEDULE_FUSED the partial input gradients
+ * of every chunk and their shard-sum run as one cooperative launch in which each
+ * 128x256 tile of dX is summed as soon as its P partials are stored (the weight
+ * gradients follow it).  M == 0 writes zero weight gradients and touches nothing
  * else (X, dY, saved, dX and workspace may then be NULL). */
 DOMINO_API domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, const void* const* A_shards,
                                const void* const* B_shards, const void* dY, const void* saved, void* dX,
                                void* const* dA_shards, void* const* dB_shards, void* workspace,
                                size_t workspace_bytes, void* stream);
 
-/* The shard-sum alone: Y[r, c] = bf16( sum_{p=0}^{P-1} partials[p][r, c] ),
+/* The shard-sum alone, the stand-in on one GPU for the tensor-parallel all-reduce
+ * whose cost the Domino page (Abstract) hides behind computation:
+ * Y[r, c] = bf16( sum_{p=0}^{P-1} partials[p][r, c] ),
  * fp32 accumulation in shard order, one round-to-nearest-even at the end.
  * partials: HOST array of P device pointers to [rows, cols] matrices with leading
  * dimension ld_partial (elements) in `partial_dtype`; Y [rows, cols] bf16 with
@@ -206,8 +218,9 @@ DOMINO_API domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const v
 DOMINO_API domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t partial_dtype, int64_t rows,
                                  int64_t cols, int64_t ld_partial, void* Y, int64_t ld_y, void* stream);
 
-/* Device-side timeline of the last DOMINO_SCHEDULE_FUSED forward call made with
- * this workspace (%globaltimer nanoseconds): when its first CTA started, when the
+/* Device-side timeline of the last DOMINO_SCHEDULE_FUSED cooperative launch made
+ * with this workspace (the forward, or the backward's partial input gradients;
+ * %globaltimer nanoseconds): when its first CTA started, when the
  * last GEMM tile's epilogue finished, and when the last shard-sum finished.
  * reduce_end_ns - gemm_end_ns (if positive) is the reduction time left exposed.
  * Synchronises `stream`; `out` is host memory. */
@@ -219,7 +232,10 @@ typedef struct domino_timeline {
 DOMINO_API domino_status_t domino_read_timeline(const void* workspace, void* stream, domino_timeline_t* out);
 
 /* Synchronises `stream`, returns the first device-side error recorded in the
- * workspace's status word since the last query (DOMINO_OK if none) and clears it. */
+ * workspace's status word since the last query (DOMINO_OK if none) and clears it.
+ * The pages have no counterpart: every device-side wait of the library is bounded
+ * (desc->timeout_ns), and a wait that runs out records DOMINO_ERR_TIMEOUT here
+ * instead of hanging the GPU. */
 DOMINO_API domino_status_t domino_query_device_status(void* workspace, void* stream);
 
 /* Self-test of the bounded device-side waits: launches one block that waits, with
@@ -291,7 +307,9 @@ typedef enum domino_kernel_kind {
   DOMINO_KERNEL_BWD_DX = 4,    /* backward: partial input gradients                    */
   DOMINO_KERNEL_BWD_DW = 5,    /* backward: weight gradients                           */
   DOMINO_KERNEL_FUSED = 6,     /* the fused forward kernel (whole call)                */
-  DOMINO_KERNEL_ATTN = 7       /* attention core of the attention block                */
+  DOMINO_KERNEL_ATTN = 7,      /* attention core of the attention block                */
+  DOMINO_KERNEL_BWD_DX_FUSED = 8 /* backward, FUSED schedule: the partial input gradients of
+                                    every chunk and their shard-sum in one launch          */
 } domino_kernel_kind_t;
 
 typedef struct domino_kernel_time {

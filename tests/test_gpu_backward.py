@@ -73,14 +73,32 @@ def test_tiny_backward():
 
 
 @pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "identity"])
-def test_backward_ragged(act):
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_backward_ragged(act, schedule):
     w = wl.Workload("ragged_bwd", M=600, d=336, F=984, P=3, mu=3, act=act, partial="f32", slices=2, bwd=True)
-    _check_full(w, seed=8)
+    _check_full(w, seed=8, schedule=schedule)
 
 
-def test_backward_llama_tail_bf16_partials():
+@pytest.mark.parametrize("act,partial", [("swiglu", "bf16"), ("gelu", "f32")])
+def test_fused_backward_equals_streams(act, partial):
+    # the FUSED backward computes the partial input gradients of every chunk and their shard-sum in one
+    # cooperative launch: the same tiles, K order and shard order as the per-chunk launches, so bit-equal
+    w = wl.Workload("fused_bwd", M=1000, d=336, F=1968, P=3, mu=2, act=act, partial=partial, bwd=True)
+    t = wl.generate(w, 17, with_dy=True)
+    ref = _run_fwd_bwd(w, t, "streams")
+    got = _run_fwd_bwd(w, t, "fused")
+    names = ("Y", "dX")
+    for n, a, b2 in zip(names, got[:2], ref[:2]):
+        assert torch.equal(a, b2), f"{n} differs between the fused and the stream schedules"
+    ga = got[2] if isinstance(got[2], tuple) else (got[2],)
+    ra = ref[2] if isinstance(ref[2], tuple) else (ref[2],)
+    assert all(torch.equal(a, b2) for a, b2 in zip(ga, ra)) and torch.equal(got[3], ref[3])
+
+
+@pytest.mark.parametrize("schedule", ["serial", "fused"])
+def test_backward_llama_tail_bf16_partials(schedule):
     w = wl.Workload("llama_tail_bwd", M=512, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
-    _check_full(w, seed=9, schedule="serial")
+    _check_full(w, seed=9, schedule=schedule)
 
 
 def test_backward_partial_row_group():
@@ -92,12 +110,13 @@ def test_backward_partial_row_group():
 
 
 @pytest.mark.parametrize("rows", [129, 300, 700])
-def test_backward_pair_row_tails(rows):
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_backward_pair_row_tails(rows, schedule):
     # 256-row tiles on 2-CTA clusters: the last tile's odd CTA holds 1 row (129), lies wholly below the
     # chunk (300) or holds part of its block (700); the dH and weight-gradient launches over all M then
     # end on a ragged block too
     w = wl.Workload("pair_tail_bwd", M=2 * rows, d=512, F=768, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)
-    _check_full(w, seed=15)
+    _check_full(w, seed=15, schedule=schedule)
 
 
 def test_backward_empty_batch_zeroes_weight_grads():
@@ -112,10 +131,11 @@ def test_backward_empty_batch_zeroes_weight_grads():
     assert all(torch.all(a == 0) for a in dA) and all(torch.all(x == 0) for x in dB)
 
 
-def test_llama_fwdbwd_full_size_sampled():
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_llama_fwdbwd_full_size_sampled(schedule):
     w = wl.WORKLOADS["llama_swiglu_fwdbwd"]
     t = wl.generate(w, 0, with_dy=True)
-    Y, dX, dA, dB = _run_fwd_bwd(w, t)
+    Y, dX, dA, dB = _run_fwd_bwd(w, t, schedule)
     rng = np.random.default_rng(0)
     # 64 rows of every chunk: the tile edges (128-row CTA blocks, 256-row pair tiles), the chunk's last
     # row and random rows
