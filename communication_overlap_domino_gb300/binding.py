@@ -21,7 +21,7 @@ ACT = {"gelu": 0, "gelu_tanh": 1, "swiglu": 2, "identity": 3}
 PARTIAL = {"f32": 0, "bf16": 1}
 SCHEDULE = {"serial": 0, "streams": 1, "fused": 2}
 KERNEL_KIND = {0: "gemm1", 1: "gemm2", 2: "shard_sum", 3: "bwd_dh", 4: "bwd_dx", 5: "bwd_dw", 6: "fused", 7: "attn",
-               8: "bwd_dx_fused"}
+               8: "bwd_dx_fused", 9: "attn_out_fused"}
 FLAG_KERNEL_TIMES = 1
 FLAG_ONE_CTA = 2
 MAX_SHARDS = 16
@@ -45,7 +45,7 @@ class MlpDesc(ctypes.Structure):
         ("partial_dtype", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("reserve_sms", ctypes.c_int32),
         ("timeout_ns", ctypes.c_uint64),
     ]
 
@@ -183,12 +183,12 @@ def _ptr_array(ptrs: Sequence[int]):
 
 def make_desc(M: int, d: int, F: int, P: int, mu: int, act: str, partial: str, out_slices: int = 1,
               schedule: str = "streams", kernel_times: bool = False, timeout_ns: int = 0,
-              pair_cta: bool = True) -> MlpDesc:
+              pair_cta: bool = True, reserve_sms: int = 0) -> MlpDesc:
     """pair_cta: run the separate-launch GEMMs as paired-CTA 256x256 tiles (default) or,
-    if False, as one-CTA 128x256 tiles."""
+    if False, as one-CTA 128x256 tiles.  reserve_sms: SMs the library's kernels leave free."""
     flags = (FLAG_KERNEL_TIMES if kernel_times else 0) | (0 if pair_cta else FLAG_ONE_CTA)
     return MlpDesc(M=M, d=d, F=F, P=P, mu=mu, out_slices=out_slices, act=ACT[act], partial_dtype=PARTIAL[partial],
-                   schedule=SCHEDULE[schedule], flags=flags, reserved=0, timeout_ns=timeout_ns)
+                   schedule=SCHEDULE[schedule], flags=flags, reserve_sms=reserve_sms, timeout_ns=timeout_ns)
 
 
 def workspace_size(desc: MlpDesc, with_bwd: bool = False) -> int:
@@ -259,12 +259,13 @@ def shard_weights(A, B, P: int):
 
 def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str, out_slices: int = 1,
             schedule: str = "streams", Y=None, saved=None, workspace=None, stream=None, kernel_times: bool = False,
-            timeout_ns: int = 0, pair_cta: bool = True):
+            timeout_ns: int = 0, pair_cta: bool = True, reserve_sms: int = 0):
     """domino_mlp_fwd on torch tensors; returns Y [M, d] bf16."""
     torch = _torch()
     M, d = X.shape
     P = len(A_shards)
-    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta,
+                     reserve_sms=reserve_sms)
     if Y is None:
         Y = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
     need = workspace_size(desc)
@@ -283,14 +284,15 @@ def mlp_fwd(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, par
 def mlp_fwd_partials(X, A_shards: List, B_shards: List, *, F: int, mu: int, act: str, partial: str,
                      out_slices: int = 1, schedule: str = "streams", Z_shards=None, piece_events=None, saved=None,
                      workspace=None, stream=None, kernel_times: bool = False, timeout_ns: int = 0,
-                     pair_cta: bool = True):
+                     pair_cta: bool = True, reserve_sms: int = 0):
     """domino_mlp_fwd_partials on torch tensors: the row-parallel partials of every shard, not summed.
     Returns Z_shards (P tensors [M, d], fp32 or bf16 as `partial`).  piece_events: None or mu * out_slices
     torch.cuda.Event objects, each recorded when its (chunk, slice) piece of every partial is written."""
     torch = _torch()
     M, d = X.shape
     P = len(A_shards)
-    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta,
+                     reserve_sms=reserve_sms)
     if Z_shards is None:
         dt = torch.float32 if partial == "f32" else torch.bfloat16
         Z_shards = [torch.empty((M, d), dtype=dt, device=X.device) for _ in range(P)]
@@ -314,14 +316,15 @@ def mlp_fwd_partials(X, A_shards: List, B_shards: List, *, F: int, mu: int, act:
 
 def mlp_bwd(X, A_shards: List, B_shards: List, dY, saved, *, F: int, mu: int, act: str, partial: str,
             out_slices: int = 1, schedule: str = "streams", dX=None, dA_shards=None, dB_shards=None, workspace=None,
-            stream=None, kernel_times: bool = False, timeout_ns: int = 0, pair_cta: bool = True):
+            stream=None, kernel_times: bool = False, timeout_ns: int = 0, pair_cta: bool = True, reserve_sms: int = 0):
     """domino_mlp_bwd on torch tensors; returns (dX, dA_shards, dB_shards).
 
     `saved` must be the buffer a domino_mlp_fwd call with the same inputs filled."""
     torch = _torch()
     M, d = X.shape
     P = len(A_shards)
-    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta)
+    desc = make_desc(M, d, F, P, mu, act, partial, out_slices, schedule, kernel_times, timeout_ns, pair_cta,
+                     reserve_sms=reserve_sms)
     if dX is None:
         dX = torch.empty((M, d), dtype=torch.bfloat16, device=X.device)
     if dA_shards is None:

@@ -36,6 +36,10 @@ domino_status_t fail(domino_status_t st, const std::string& msg) {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr size_t kHeaderBytes = 256;
+// The FUSED attention block: chunk k's output-projection launch keeps its timeline (3 words) at header byte
+// 64 + 24 k, so up to 8 chunks fit in the header.
+constexpr int kAttnFusedMaxChunks = 8;
+constexpr size_t kAttnTimelineOff = 64;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -132,7 +136,7 @@ domino_status_t check_desc(const domino_mlp_desc_t* desc, Shape* s) {
   if (d.schedule != DOMINO_SCHEDULE_SERIAL && d.schedule != DOMINO_SCHEDULE_STREAMS &&
       d.schedule != DOMINO_SCHEDULE_FUSED)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown schedule");
-  if (d.reserved != 0) return fail(DOMINO_ERR_INVALID_ARG, "reserved must be 0");
+  if (d.reserve_sms < 0) return fail(DOMINO_ERR_INVALID_ARG, "reserve_sms must be >= 0");
   if ((d.flags & ~(DOMINO_FLAG_KERNEL_TIMES | DOMINO_FLAG_ONE_CTA)) != 0)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
   if (static_cast<int64_t>(d.mu) * d.out_slices > DOMINO_MAX_PIECES)
@@ -246,10 +250,35 @@ domino_status_t timed(Timer& T, cudaStream_t st, int32_t stream_id, int32_t kind
   return r;
 }
 
+// The persistent grids of one call: the device's co-residency limits, less the SMs the caller reserves
+// (desc->reserve_sms) for work of its own that runs beside the library (a collective, another stream).
+struct Grid {
+  int num_sms = 0;              // SMs the one-CTA kernels and the shard-sum spread over
+  int pair_clusters = 0;        // 2-CTA clusters of the paired GEMM
+  int fused_ctas = 0;           // CTAs of the one-CTA fused kernel
+  int fused_pair_clusters = 0;  // 2-CTA clusters of the paired fused kernels (0: not usable)
+};
+
+Grid grid_for(const DeviceState* ds, int reserve_sms) {
+  Grid g;
+  const int avail = ds->num_sms - reserve_sms;
+  const int per_sm = ds->num_sms > 0 ? ds->fused_max_ctas / ds->num_sms : 0;
+  g.num_sms = avail;
+  g.pair_clusters = ds->pair_max_clusters < avail / 2 ? ds->pair_max_clusters : avail / 2;
+  g.fused_ctas = per_sm * avail;
+  g.fused_pair_clusters = ds->fused_pair_clusters < avail / 2 ? ds->fused_pair_clusters : avail / 2;
+  return g;
+}
+
+domino_status_t check_reserve(const DeviceState* ds, int reserve_sms) {
+  if (reserve_sms > ds->num_sms - 2)
+    return fail(DOMINO_ERR_INVALID_ARG, "reserve_sms must leave at least 2 SMs to the library");
+  return DOMINO_OK;
+}
+
 // One grouped GEMM launch, as one-CTA tiles or as paired-CTA clusters.
-domino_status_t run_gemm(const GemmLaunch& L, const DeviceState* ds, bool pair, cudaStream_t st, std::string* err) {
-  return pair ? launch_gemm_pair(L, ds->pair_max_clusters, st, err)
-              : launch_gemm(L, ds->num_sms, st, err);
+domino_status_t run_gemm(const GemmLaunch& L, const Grid& g, bool pair, cudaStream_t st, std::string* err) {
+  return pair ? launch_gemm_pair(L, g.pair_clusters, st, err) : launch_gemm(L, g.num_sms, st, err);
 }
 
 // ------------------------------------------------------- launch sequences
@@ -262,6 +291,7 @@ domino_status_t run_gemm(const GemmLaunch& L, const DeviceState* ds, bool pair, 
 struct FwdSeq {
   Shape s{};
   DeviceState* ds = nullptr;
+  Grid grid{};
   Timer* T = nullptr;
   cudaStream_t s0 = nullptr, sr = nullptr;
   bool pair = true;
@@ -326,7 +356,7 @@ struct FwdSeq {
       L.K = s.d;
       L.status = status;
       L.timeout_ns = tmo;
-      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, grid, pair, s0, err); });
       if (st != DOMINO_OK) return st;
     }
     for (int sl = 0; sl < s.S; ++sl) {
@@ -354,7 +384,7 @@ struct FwdSeq {
       L.K = s.Fp;
       L.status = status;
       L.timeout_ns = tmo;
-      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return run_gemm(L, ds, pair, s0, err); });
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, sl, [&] { return run_gemm(L, grid, pair, s0, err); });
       if (st != DOMINO_OK) return st;
       if (!reduce) {
         if (user_events) {
@@ -393,7 +423,7 @@ struct FwdSeq {
     q.P = s.P;
     q.f32 = s.partial == DOMINO_PARTIAL_F32;
     return timed(*T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
-                 [&] { return launch_shard_sum(q, ds->num_sms, sr, err); });
+                 [&] { return launch_shard_sum(q, grid.num_sms, sr, err); });
   }
 };
 
@@ -403,6 +433,7 @@ struct FwdSeq {
 struct BwdSeq {
   Shape s{};
   DeviceState* ds = nullptr;
+  Grid grid{};
   Timer* T = nullptr;
   cudaStream_t s0 = nullptr, sr = nullptr;
   bool pair = true;
@@ -464,7 +495,7 @@ struct BwdSeq {
     L.K = s.d;
     L.status = status;
     L.timeout_ns = tmo;
-    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DH, 0, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DH, 0, 0, [&] { return run_gemm(L, grid, pair, s0, err); });
   }
 
   domino_status_t dx_chunk(int k, std::string* err) const {
@@ -494,7 +525,7 @@ struct BwdSeq {
       L.status = status;
       L.timeout_ns = tmo;
       domino_status_t st =
-          timed(*T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return run_gemm(L, ds, pair, s0, err); });
+          timed(*T, s0, 0, DOMINO_KERNEL_BWD_DX, k, sl, [&] { return run_gemm(L, grid, pair, s0, err); });
       if (st != DOMINO_OK) return st;
       // ---- dX_k[:, s] = sum_p of the partials (the all-reduce of the input gradient)
       if (sr != s0) {
@@ -514,7 +545,7 @@ struct BwdSeq {
       q.P = s.P;
       q.f32 = s.partial == DOMINO_PARTIAL_F32;
       st = timed(*T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, sl,
-                 [&] { return launch_shard_sum(q, ds->num_sms, sr, err); });
+                 [&] { return launch_shard_sum(q, grid.num_sms, sr, err); });
       if (st != DOMINO_OK) return st;
     }
     return DOMINO_OK;
@@ -524,13 +555,14 @@ struct BwdSeq {
   // (tile-granular overlap, as in the fused forward).  Returns DOMINO_ERR_UNSUPPORTED with nothing launched
   // when the device cannot run it; the caller then issues dx_chunk() per chunk.
   domino_status_t dx_fused(uint8_t* ws, const WsLayout& W, std::string* err) const {
-    FusedDxLaunch F;
+    FusedGemm2Launch F;
     for (int p = 0; p < s.P; ++p) {
-      F.dG[p] = dG[p];
-      F.W[p] = A_shards[p];
+      F.A[p] = dG[p];
+      F.B[p] = A_shards[p];
       F.Z[p] = Z[p];
     }
-    F.dX = dX;
+    F.Y = dX;
+    F.b_mn = true;
     F.sync = reinterpret_cast<uint32_t*>(ws + W.sync_off);
     F.timeline = reinterpret_cast<uint64_t*>(ws + kTimelineOff);
     F.M = s.M;
@@ -541,14 +573,14 @@ struct BwdSeq {
     F.partial_f32 = s.partial == DOMINO_PARTIAL_F32;
     F.status = status;
     F.timeout_ns = tmo;
-    if (ds->fused_pair_clusters < 1) return DOMINO_ERR_UNSUPPORTED;
+    if (grid.fused_pair_clusters < 1) return DOMINO_ERR_UNSUPPORTED;
     cudaError_t e = cudaMemsetAsync(ws + kTimelineOff, 0, kSyncOff - kTimelineOff + W.sync_bytes, s0);
     if (e != cudaSuccess) {
       if (err) *err = std::string("counter reset: ") + cudaGetErrorString(e);
       return DOMINO_ERR_CUDA;
     }
     return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DX_FUSED, 0, 0,
-                 [&] { return launch_fused_dx(F, ds->fused_pair_clusters, s0, err); });
+                 [&] { return launch_fused_gemm2(F, grid.fused_pair_clusters, s0, err); });
   }
 
   // Weight gradients over all M (they run while the last shard-sum drains).
@@ -575,7 +607,7 @@ struct BwdSeq {
       L.status = status;
       L.timeout_ns = tmo;
       domino_status_t st =
-          timed(*T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+          timed(*T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 0, [&] { return run_gemm(L, grid, pair, s0, err); });
       if (st != DOMINO_OK) return st;
     }
     GemmLaunch L;  // dB_p = dY^T H_p : [d, Fp]
@@ -598,7 +630,7 @@ struct BwdSeq {
     L.K = s.M;
     L.status = status;
     L.timeout_ns = tmo;
-    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return run_gemm(L, ds, pair, s0, err); });
+    return timed(*T, s0, 0, DOMINO_KERNEL_BWD_DW, 0, 1, [&] { return run_gemm(L, grid, pair, s0, err); });
   }
 };
 
@@ -640,8 +672,8 @@ domino_status_t check_attn_desc(const domino_attn_desc_t* desc, AttnShape* s) {
   if (a.reserved != 0) return fail(DOMINO_ERR_INVALID_ARG, "reserved must be 0");
   if ((a.flags & ~(DOMINO_FLAG_KERNEL_TIMES | DOMINO_FLAG_ONE_CTA)) != 0)
     return fail(DOMINO_ERR_INVALID_ARG, "unknown flag bits");
-  if (a.schedule == DOMINO_SCHEDULE_FUSED)
-    return fail(DOMINO_ERR_UNSUPPORTED, "the attention block runs the SERIAL or STREAMS schedule");
+  if (a.schedule == DOMINO_SCHEDULE_FUSED && a.mu > kAttnFusedMaxChunks)
+    return fail(DOMINO_ERR_UNSUPPORTED, "the FUSED attention block takes at most 8 chunks (one timeline slot each)");
   if (a.dh != 128) return fail(DOMINO_ERR_UNSUPPORTED, "head width dh must be 128");
   if (a.S % 128) return fail(DOMINO_ERR_UNSUPPORTED, "S must be a multiple of 128");
   if (a.H % a.P) return fail(DOMINO_ERR_UNSUPPORTED, "P must divide H");
@@ -668,12 +700,16 @@ domino_status_t check_attn_desc(const domino_attn_desc_t* desc, AttnShape* s) {
 }
 
 struct AttnWs {
+  size_t sync_off, sync_bytes;  // FUSED: the counters of one chunk's output-projection + shard-sum launch
   size_t qkv_off, qkv_shard, o_off, o_shard, z_off, z_shard, total;
 };
 
 AttnWs attn_ws_layout(const AttnShape& s) {
   AttnWs W;
   size_t off = kHeaderBytes;
+  W.sync_off = off;
+  W.sync_bytes = fused_sync_bytes(s.Mc, s.d, s.P, 1);
+  off = align_up(off + W.sync_bytes, 256);
   W.qkv_shard = static_cast<size_t>(s.M) * s.qkv_cols() * 2;
   W.qkv_off = off;
   off = align_up(off + W.qkv_shard * s.P, 256);
@@ -692,6 +728,7 @@ AttnWs attn_ws_layout(const AttnShape& s) {
 struct AttnSeq {
   AttnShape s{};
   DeviceState* ds = nullptr;
+  Grid grid{};
   Timer* T = nullptr;
   cudaStream_t s0 = nullptr, sr = nullptr;
   bool pair = true;
@@ -704,6 +741,42 @@ struct AttnSeq {
   void* qkv[kMaxShards] = {};
   void* o[kMaxShards] = {};
   void* Z[kMaxShards] = {};
+  uint8_t* ws = nullptr;
+  AttnWs W{};
+
+  // FUSED, last chunk: its output projection and its shard-sum in one cooperative launch (each 128x256 tile
+  // of Y_k summed as soon as its P partials exist).  DOMINO_ERR_UNSUPPORTED with nothing launched if the device
+  // cannot run it.
+  domino_status_t out_proj_fused(int k, std::string* err) const {
+    if (grid.fused_pair_clusters < 1) return DOMINO_ERR_UNSUPPORTED;
+    const size_t row0 = static_cast<size_t>(k) * s.Mc;
+    FusedGemm2Launch F;
+    for (int p = 0; p < s.P; ++p) {
+      F.A[p] = static_cast<const uint8_t*>(o[p]) + row0 * s.o_cols() * 2;
+      F.B[p] = Wo[p];
+      F.Z[p] = static_cast<uint8_t*>(Z[p]) + row0 * s.d * s.psize;
+    }
+    F.Y = static_cast<uint8_t*>(Y) + row0 * s.d * 2;
+    F.sync = reinterpret_cast<uint32_t*>(ws + W.sync_off);
+    F.timeline = reinterpret_cast<uint64_t*>(ws + kAttnTimelineOff + 24 * static_cast<size_t>(k));
+    F.M = s.Mc;
+    F.d = s.d;
+    F.K2 = s.o_cols();
+    F.mu = 1;
+    F.P = s.P;
+    F.b_mn = false;
+    F.partial_f32 = s.partial == DOMINO_PARTIAL_F32;
+    F.status = status;
+    F.timeout_ns = tmo;
+    cudaError_t e = cudaMemsetAsync(F.timeline, 0, 24, s0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(F.sync, 0, W.sync_bytes, s0);
+    if (e != cudaSuccess) {
+      if (err) *err = std::string("counter reset: ") + cudaGetErrorString(e);
+      return DOMINO_ERR_CUDA;
+    }
+    return timed(*T, s0, 0, DOMINO_KERNEL_ATTN_OUT_FUSED, k, 0,
+                 [&] { return launch_fused_gemm2(F, grid.fused_pair_clusters, s0, err); });
+  }
 
   domino_status_t chunk(int k, std::string* err) const {
     const int32_t row0 = static_cast<int32_t>(k * s.Mc);
@@ -729,7 +802,7 @@ struct AttnSeq {
       L.K = s.d;
       L.status = status;
       L.timeout_ns = tmo;
-      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM1, k, 0, [&] { return run_gemm(L, grid, pair, s0, err); });
       if (st != DOMINO_OK) return st;
     }
     {  // ---- attention core of every (shard, sequence, head, query tile) of the chunk
@@ -747,8 +820,13 @@ struct AttnSeq {
       L.P = s.P;
       L.status = status;
       L.timeout_ns = tmo;
-      st = timed(*T, s0, 0, DOMINO_KERNEL_ATTN, k, 0, [&] { return launch_attn_fwd(L, ds->num_sms, s0, err); });
+      st = timed(*T, s0, 0, DOMINO_KERNEL_ATTN, k, 0, [&] { return launch_attn_fwd(L, grid.num_sms, s0, err); });
       if (st != DOMINO_OK) return st;
+    }
+    if (s.schedule == DOMINO_SCHEDULE_FUSED && k == s.mu - 1) {
+      // the last chunk's shard-sum has no next chunk to hide under: tile-granular inside its projection
+      st = out_proj_fused(k, err);
+      if (st != DOMINO_ERR_UNSUPPORTED) return st;  // else: the separate launches below
     }
     {  // ---- output projection of every shard into its partial buffer: O_p Wo_p
       GemmLaunch L;
@@ -771,7 +849,7 @@ struct AttnSeq {
       L.K = s.o_cols();
       L.status = status;
       L.timeout_ns = tmo;
-      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, 0, [&] { return run_gemm(L, ds, pair, s0, err); });
+      st = timed(*T, s0, 0, DOMINO_KERNEL_GEMM2, k, 0, [&] { return run_gemm(L, grid, pair, s0, err); });
       if (st != DOMINO_OK) return st;
     }
     // ---- Y_k = sum over p of the partials (the all-reduce of the row-parallel projection)
@@ -792,7 +870,7 @@ struct AttnSeq {
     q.P = s.P;
     q.f32 = s.partial == DOMINO_PARTIAL_F32;
     return timed(*T, sr, sr != s0, DOMINO_KERNEL_SHARD_SUM, k, 0,
-                 [&] { return launch_shard_sum(q, ds->num_sms, sr, err); });
+                 [&] { return launch_shard_sum(q, grid.num_sms, sr, err); });
   }
 };
 
@@ -875,6 +953,8 @@ domino_status_t mlp_fwd_impl(const domino_mlp_desc_t* desc, const void* X, const
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != DOMINO_OK) return st;
+  st = check_reserve(ds, desc->reserve_sms);
+  if (st != DOMINO_OK) return st;
 
   cudaStream_t s0 = static_cast<cudaStream_t>(stream);
   cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
@@ -891,6 +971,7 @@ domino_status_t mlp_fwd_impl(const domino_mlp_desc_t* desc, const void* X, const
   FwdSeq f;
   f.s = s;
   f.ds = ds;
+  f.grid = grid_for(ds, desc->reserve_sms);
   f.T = &T;
   f.s0 = s0;
   f.sr = sr;
@@ -911,7 +992,7 @@ domino_status_t mlp_fwd_impl(const domino_mlp_desc_t* desc, const void* X, const
   std::string err;
 
   if (s.schedule == DOMINO_SCHEDULE_FUSED) {
-    if (ds->fused_max_ctas < 1) return fail(DOMINO_ERR_DEVICE, "fused kernel cannot be resident on this device");
+    if (f.grid.fused_ctas < 1) return fail(DOMINO_ERR_DEVICE, "fused kernel cannot be resident on this device");
     FusedLaunch F;
     F.X = X;
     for (int p = 0; p < s.P; ++p) {
@@ -939,12 +1020,12 @@ domino_status_t mlp_fwd_impl(const domino_mlp_desc_t* desc, const void* X, const
     if (e != cudaSuccess) return fail(DOMINO_ERR_CUDA, std::string("counter reset: ") + cudaGetErrorString(e));
     F.pair = pair;
     st = timed(T, s0, 0, DOMINO_KERNEL_FUSED, 0, 0, [&] {
-      domino_status_t r = launch_fused_fwd(F, ds->fused_max_ctas, ds->fused_pair_clusters, s0, &err);
+      domino_status_t r = launch_fused_fwd(F, f.grid.fused_ctas, f.grid.fused_pair_clusters, s0, &err);
       if (r == DOMINO_ERR_UNSUPPORTED && F.pair) {
         // paired cooperative launches refused on this device: use one-CTA tiles from now on
         ds->fused_pair_clusters = 0;
         F.pair = false;
-        r = launch_fused_fwd(F, ds->fused_max_ctas, 0, s0, &err);
+        r = launch_fused_fwd(F, f.grid.fused_ctas, 0, s0, &err);
       }
       return r;
     });
@@ -1020,6 +1101,8 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != DOMINO_OK) return st;
+  st = check_reserve(ds, desc->reserve_sms);
+  if (st != DOMINO_OK) return st;
   // FUSED: dH, one cooperative launch for the partial input gradients of every chunk and their shard-sum, then
   // the weight gradients (STREAMS if the device cannot run the cooperative launch)
   cudaStream_t sr = s.schedule != DOMINO_SCHEDULE_SERIAL ? ds->reduce_stream : s0;
@@ -1035,6 +1118,7 @@ domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const void* X, con
   BwdSeq g;
   g.s = s;
   g.ds = ds;
+  g.grid = grid_for(ds, desc->reserve_sms);
   g.T = &T;
   g.s0 = s0;
   g.sr = sr;
@@ -1114,6 +1198,8 @@ domino_status_t domino_mlp_fwd_bwd_interleaved(const domino_mlp_desc_t* desc, co
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != DOMINO_OK) return st;
+  st = check_reserve(ds, desc->reserve_sms);
+  if (st != DOMINO_OK) return st;
   cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
   const uint64_t tmo = desc->timeout_ns ? desc->timeout_ns : kDefaultTimeoutNs;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1127,6 +1213,7 @@ domino_status_t domino_mlp_fwd_bwd_interleaved(const domino_mlp_desc_t* desc, co
   FwdSeq f;
   f.s = s;
   f.ds = ds;
+  f.grid = grid_for(ds, desc->reserve_sms);
   f.T = &T;
   f.s0 = s0;
   f.sr = sr;
@@ -1142,6 +1229,7 @@ domino_status_t domino_mlp_fwd_bwd_interleaved(const domino_mlp_desc_t* desc, co
   BwdSeq g;
   g.s = s;
   g.ds = ds;
+  g.grid = grid_for(ds, desc->reserve_sms);
   g.T = &T;
   g.s0 = s0;
   g.sr = sr;
@@ -1204,7 +1292,8 @@ domino_status_t domino_attn_fwd(const domino_attn_desc_t* desc, const void* X, c
   st = device_state(&ds);
   if (st != DOMINO_OK) return st;
   cudaStream_t s0 = static_cast<cudaStream_t>(stream);
-  cudaStream_t sr = s.schedule == DOMINO_SCHEDULE_STREAMS ? ds->reduce_stream : s0;
+  // STREAMS, and FUSED for every chunk but the last: the shard-sum on the reduction stream under the next chunk
+  cudaStream_t sr = s.schedule != DOMINO_SCHEDULE_SERIAL ? ds->reduce_stream : s0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Timer T;
   T.on = (desc->flags & DOMINO_FLAG_KERNEL_TIMES) != 0;
@@ -1214,6 +1303,7 @@ domino_status_t domino_attn_fwd(const domino_attn_desc_t* desc, const void* X, c
   AttnSeq a;
   a.s = s;
   a.ds = ds;
+  a.grid = grid_for(ds, 0);
   a.T = &T;
   a.s0 = s0;
   a.sr = sr;
@@ -1224,6 +1314,8 @@ domino_status_t domino_attn_fwd(const domino_attn_desc_t* desc, const void* X, c
   a.Wqkv = Wqkv_shards;
   a.Wo = Wo_shards;
   a.Y = Y;
+  a.ws = ws;
+  a.W = W;
   for (int p = 0; p < s.P; ++p) {
     a.qkv[p] = ws + W.qkv_off + W.qkv_shard * p;
     a.o[p] = ws + W.o_off + W.o_shard * p;

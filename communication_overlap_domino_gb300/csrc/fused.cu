@@ -768,10 +768,14 @@ void* fused_pair_ptr() {
   return reinterpret_cast<void*>(&fused_fwd_pair_kernel<A, B, false>);
 }
 
-// The backward's dX kernel: no GEMM1 phase, GEMM2 with the MN-major weight shard as B.
-void* fused_dx_kernel_for(bool f32) {
-  return f32 ? reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_F32, true>)
-             : reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_BF16, true>);
+// The GEMM2-only launches (no GEMM1 phase): with the MN-major weight shard as B (the backward's partial input
+// gradients) or K-major (the forward identity kernel's GEMM2 phase: a row-parallel projection).
+void* fused_gemm2_kernel_for(bool f32, bool b_mn) {
+  if (b_mn)
+    return f32 ? reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_F32, true>)
+               : reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_BF16, true>);
+  return f32 ? reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_F32, false>)
+             : reinterpret_cast<void*>(&fused_fwd_pair_kernel<EPI_H_IDENTITY, EPI_Z_BF16, false>);
 }
 
 void* fused_pair_kernel_for(int epi_a, bool f32) {
@@ -826,7 +830,7 @@ cudaError_t prepare_fused_kernels(int* max_ctas_per_sm, int* max_pair_clusters) 
     }
   }
   for (int f32 = 0; f32 < 2; ++f32) {
-    void* fn = fused_dx_kernel_for(f32 != 0);
+    void* fn = fused_gemm2_kernel_for(f32 != 0, true);
     cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (st != cudaSuccess) return st;
     cudaLaunchConfig_t cfg = {};
@@ -947,22 +951,25 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pai
 
 namespace domino {
 
-domino_status_t launch_fused_dx(const FusedDxLaunch& L, int max_pair_clusters, cudaStream_t stream, std::string* err) {
+domino_status_t launch_fused_gemm2(const FusedGemm2Launch& L, int max_pair_clusters, cudaStream_t stream,
+                                   std::string* err) {
   if (max_pair_clusters < 1) {
-    if (err) *err = "fused dX kernel: no paired cooperative launch on this device";
+    if (err) *err = "fused GEMM2 + shard-sum kernel: no paired cooperative launch on this device";
     return DOMINO_ERR_UNSUPPORTED;
   }
   FusedParams f;
   memset(&f, 0, sizeof f);
   for (int p = 0; p < L.P; ++p) {
-    // A: dG_p [M, K2] K-major, 128-row boxes; B: A_shards[p] [K2, d] MN-major, 64 x 64 boxes
-    if (!encode_bf16_sw128(&f.map_h[p], Operand2D{L.dG[p], L.M, L.K2, L.K2}, kBM, err)) return DOMINO_ERR_CUDA;
-    if (!encode_bf16_sw128(&f.map_w2[p], Operand2D{L.W[p], L.K2, L.d, L.d}, kBK, err)) return DOMINO_ERR_CUDA;
+    // A: [M, K2] K-major, 128-row boxes; B: [K2, d] MN-major in 64 x 64 boxes, or [d, K2] K-major in 128-row boxes
+    if (!encode_bf16_sw128(&f.map_h[p], Operand2D{L.A[p], L.M, L.K2, L.K2}, kBM, err)) return DOMINO_ERR_CUDA;
+    const bool ok = L.b_mn ? encode_bf16_sw128(&f.map_w2[p], Operand2D{L.B[p], L.K2, L.d, L.d}, kBK, err)
+                           : encode_bf16_sw128(&f.map_w2[p], Operand2D{L.B[p], L.d, L.K2, L.K2}, kBN / 2, err);
+    if (!ok) return DOMINO_ERR_CUDA;
     if (!encode_store_map(&f.map_zout[p], L.Z[p], L.M, L.d, L.d, L.partial_f32, L.partial_f32 ? 32 : 64, err))
       return DOMINO_ERR_CUDA;
     f.z[p] = L.Z[p];
   }
-  f.y = L.dX;
+  f.y = L.Y;
   f.Mc = static_cast<int32_t>(L.M / L.mu);
   f.tiles_m = (f.Mc + kBM - 1) / kBM;
   f.tiles_n2 = static_cast<int32_t>((L.d + kBN - 1) / kBN);
@@ -984,7 +991,7 @@ domino_status_t launch_fused_dx(const FusedDxLaunch& L, int max_pair_clusters, c
   f.status = L.status;
   f.timeout_ns = L.timeout_ns;
   if (f.num_pair_tiles == 0) return DOMINO_OK;
-  void* fn = fused_dx_kernel_for(L.partial_f32);
+  void* fn = fused_gemm2_kernel_for(L.partial_f32, L.b_mn);
   const int clusters = f.num_pair_tiles < max_pair_clusters ? f.num_pair_tiles : max_pair_clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
@@ -999,7 +1006,7 @@ domino_status_t launch_fused_dx(const FusedDxLaunch& L, int max_pair_clusters, c
   void* args[] = {&f};
   const cudaError_t st = cudaLaunchKernelExC(&cfg, fn, args);
   if (st == cudaSuccess) return DOMINO_OK;
-  if (err) *err = std::string("fused dX launch: ") + cudaGetErrorString(st);
+  if (err) *err = std::string("fused GEMM2 + shard-sum launch: ") + cudaGetErrorString(st);
   return DOMINO_ERR_UNSUPPORTED;
 }
 

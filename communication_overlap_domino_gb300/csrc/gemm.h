@@ -83,24 +83,28 @@ struct FusedLaunch {
   DeviceStatus* status = nullptr;
   uint64_t timeout_ns = 0;
 };
-// The backward's partial input gradients and their shard-sum in one cooperative launch (paired tiles):
-// Z_p = dG_p A_shards[p] for every chunk and shard (dG_p [M, K2] K-major, A_shards[p] [K2, d] read as the
-// MN-major B operand), each output tile's shard-sum as soon as its P partials exist, dX = bf16(sum_p Z_p).
-struct FusedDxLaunch {
-  const void* dG[kMaxShards] = {};
-  const void* W[kMaxShards] = {};  // A_shards[p]: [K2, d]
+// A row-parallel GEMM and its shard-sum in one cooperative launch of the paired fused kernel (no GEMM1
+// phase): Z_p = A_p B_p for every chunk and shard, each 128x256 output tile summed over the shards as soon as
+// its P partials exist, Y = bf16(sum_p Z_p).  A_p [M, K2] is K-major; B_p is [d, K2] (K-major, the forward
+// layout of a row-parallel weight) or, with b_mn, [K2, d] (MN-major: the backward's partial input gradients
+// dG_p A_shards[p]).
+struct FusedGemm2Launch {
+  const void* A[kMaxShards] = {};
+  const void* B[kMaxShards] = {};
   void* Z[kMaxShards] = {};
-  void* dX = nullptr;
-  uint32_t* sync = nullptr;
-  uint64_t* timeline = nullptr;
+  void* Y = nullptr;
+  uint32_t* sync = nullptr;      // fused_sync_bytes(M / mu, d, P, mu) of zeroed counters
+  uint64_t* timeline = nullptr;  // 3 words, zero before the launch
   int64_t M = 0, d = 0, K2 = 0;
   int mu = 1, P = 1;
+  bool b_mn = false;
   bool partial_f32 = true;
   DeviceStatus* status = nullptr;
   uint64_t timeout_ns = 0;
 };
 // Returns DOMINO_ERR_UNSUPPORTED (with nothing launched) if no paired cooperative launch is possible.
-domino_status_t launch_fused_dx(const FusedDxLaunch& L, int max_pair_clusters, cudaStream_t stream, std::string* err);
+domino_status_t launch_fused_gemm2(const FusedGemm2Launch& L, int max_pair_clusters, cudaStream_t stream,
+                                   std::string* err);
 size_t fused_sync_bytes(int64_t Mc, int64_t d, int P, int mu);
 cudaError_t prepare_fused_kernels(int* max_ctas_per_sm, int* max_pair_clusters);
 // Returns DOMINO_ERR_UNSUPPORTED (with nothing launched) if a paired launch is refused.

@@ -112,6 +112,8 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
   NoallocDevice* nd = nullptr;
   domino_status_t st = noalloc_setup(&nd);
   if (st != DOMINO_OK) return st;
+  const int sms = nd->num_sms - desc->reserve_sms;  // the SMs the persistent grids spread over
+  if (sms < 2) return noalloc_fail(DOMINO_ERR_INVALID_ARG, "reserve_sms must leave at least 2 SMs to the library");
 
   const int64_t Fp = F / P, Mc = M / mu, ds = d / S;
   const bool swiglu = desc->act == DOMINO_ACT_SWIGLU;
@@ -156,7 +158,7 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
     L1.K = d;
     L1.status = status;
     L1.timeout_ns = tmo;
-    st = launch_gemm(L1, nd->num_sms, s0, &err);
+    st = launch_gemm(L1, sms, s0, &err);
     if (st != DOMINO_OK) return noalloc_fail(st, err);
     for (int sl = 0; sl < S; ++sl) {
       const int32_t col0 = static_cast<int32_t>(sl * ds);
@@ -178,7 +180,7 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
       L2.K = Fp;
       L2.status = status;
       L2.timeout_ns = tmo;
-      st = launch_gemm(L2, nd->num_sms, s0, &err);
+      st = launch_gemm(L2, sms, s0, &err);
       if (st != DOMINO_OK) return noalloc_fail(st, err);
       ShardSumParams q;
       memset(&q, 0, sizeof q);
@@ -191,7 +193,7 @@ extern "C" DOMINO_API domino_status_t domino_mlp_fwd_noalloc(const domino_mlp_de
       q.y = static_cast<uint8_t*>(Y) + (static_cast<size_t>(row0) * d + col0) * 2;
       q.P = P;
       q.f32 = f32 ? 1 : 0;
-      st = launch_shard_sum(q, nd->num_sms, s0, &err);
+      st = launch_shard_sum(q, sms, s0, &err);
       if (st != DOMINO_OK) return noalloc_fail(st, err);
     }
   }

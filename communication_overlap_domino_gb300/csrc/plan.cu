@@ -69,7 +69,7 @@ domino_status_t domino_mlp_plan(const domino_mlp_desc_t* problem, const domino_p
   p.mu = 1;
   p.schedule = DOMINO_SCHEDULE_STREAMS;
   p.flags = 0;
-  p.reserved = 0;
+  p.reserve_sms = 0;
   const domino_status_t st = domino::validate_desc(&p);
   if (st != DOMINO_OK) return st;
 

@@ -126,7 +126,11 @@ typedef struct domino_mlp_desc {
   int32_t partial_dtype;  /* domino_partial_dtype_t                              */
   int32_t schedule;       /* domino_schedule_t                                   */
   uint32_t flags;         /* DOMINO_FLAG_*                                       */
-  uint32_t reserved;      /* must be 0                                           */
+  int32_t reserve_sms;    /* SMs the library's kernels leave free for work that  */
+                          /* runs beside them (a collective, another stream):    */
+                          /* persistent grids are sized for (SM count -          */
+                          /* reserve_sms) SMs; 0 = all; >= 0 and at most the SM  */
+                          /* count - 2 (else DOMINO_ERR_INVALID_ARG)              */
   uint64_t timeout_ns;    /* bound on each device-side wait; 0 = 2 seconds       */
 } domino_mlp_desc_t;
 
@@ -308,8 +312,10 @@ typedef enum domino_kernel_kind {
   DOMINO_KERNEL_BWD_DW = 5,    /* backward: weight gradients                           */
   DOMINO_KERNEL_FUSED = 6,     /* the fused forward kernel (whole call)                */
   DOMINO_KERNEL_ATTN = 7,      /* attention core of the attention block                */
-  DOMINO_KERNEL_BWD_DX_FUSED = 8 /* backward, FUSED schedule: the partial input gradients of
-                                    every chunk and their shard-sum in one launch          */
+  DOMINO_KERNEL_BWD_DX_FUSED = 8, /* backward, FUSED schedule: the partial input gradients of
+                                     every chunk and their shard-sum in one launch          */
+  DOMINO_KERNEL_ATTN_OUT_FUSED = 9 /* attention block, FUSED schedule: one chunk's output
+                                     projection and its shard-sum in one launch            */
 } domino_kernel_kind_t;
 
 typedef struct domino_kernel_time {
@@ -345,13 +351,17 @@ DOMINO_API void domino_kernel_times_reset(void);
  * tensor cores: scores and P V in tensor memory, online softmax, no score matrix
  * in global memory), the output projection of every shard into its partial
  * buffer (one launch), and the shard-sum of the chunk -- on the library's
- * reduction stream with DOMINO_SCHEDULE_STREAMS, so it overlaps chunk k+1.
+ * reduction stream with DOMINO_SCHEDULE_STREAMS, so it overlaps chunk k+1;
+ * DOMINO_SCHEDULE_FUSED does the same for every chunk but the last, whose output
+ * projection and shard-sum -- which no later chunk could hide -- are one
+ * cooperative launch in which each 128x256 tile of Y is summed as soon as its P
+ * partials are stored (the separate launches if the device cannot run it).
  * Weights, nn.Linear layout, per shard:
  *   Wqkv_shards[p]  [3 Hp dh, d]: shard p's query heads' rows, then its key
  *                   heads', then its value heads' (head h: rows h dh .. (h+1) dh)
  *   Wo_shards[p]    Wo_p^T [d, Hp dh]
- * Supported: dh = 128, S a multiple of 128, P | H, mu | B, d % 8 == 0;
- * DOMINO_SCHEDULE_SERIAL or STREAMS.  Other shapes: DOMINO_ERR_UNSUPPORTED
+ * Supported: dh = 128, S a multiple of 128, P | H, mu | B, d % 8 == 0; any
+ * schedule (FUSED: mu <= 8).  Other shapes: DOMINO_ERR_UNSUPPORTED
  * (ALIGNMENT for d).  Softmax in fp32; Q, K, V, P and O rounded to bf16. */
 typedef struct domino_attn_desc {
   int64_t B;              /* sequences, >= 0                                     */
@@ -362,15 +372,18 @@ typedef struct domino_attn_desc {
   int32_t P;              /* shards, 1..DOMINO_MAX_SHARDS                        */
   int32_t mu;             /* chunks of whole sequences, mu | B, <= DOMINO_MAX_PIECES */
   int32_t partial_dtype;  /* domino_partial_dtype_t                              */
-  int32_t schedule;       /* DOMINO_SCHEDULE_SERIAL or DOMINO_SCHEDULE_STREAMS   */
+  int32_t schedule;       /* domino_schedule_t                                   */
   uint32_t flags;         /* DOMINO_FLAG_KERNEL_TIMES, DOMINO_FLAG_ONE_CTA       */
   uint32_t reserved;      /* must be 0                                           */
   uint64_t timeout_ns;    /* bound on each device-side wait; 0 = 2 seconds       */
 } domino_attn_desc_t;
 
 /* Workspace bytes of domino_attn_fwd (0 for an invalid descriptor): a 256-byte
- * header (device status), Q|K|V per shard [P][B S][3 Hp dh] bf16, the attention
- * output per shard [P][B S][Hp dh] bf16, the partials [P][B S][d]. */
+ * header (device status at bytes 0-15; with DOMINO_SCHEDULE_FUSED, the last
+ * chunk k's timeline -- 3 words as in domino_read_timeline -- at byte 64 + 24 k), the
+ * counters of one fused output-projection launch, Q|K|V per shard
+ * [P][B S][3 Hp dh] bf16, the attention output per shard [P][B S][Hp dh] bf16,
+ * the partials [P][B S][d]. */
 DOMINO_API size_t domino_attn_workspace_size(const domino_attn_desc_t* desc);
 
 /* Forward pass: X [B S, d] -> Y [B S, d] bf16.  B == 0 returns DOMINO_OK having

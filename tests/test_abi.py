@@ -85,7 +85,7 @@ def test_descriptor_validation(lib, kw, status):
 
 
 def test_enum_validation(lib):
-    for field, bad in (("act", 9), ("partial_dtype", 5), ("schedule", 3), ("reserved", 1), ("flags", 0x80)):
+    for field, bad in (("act", 9), ("partial_dtype", 5), ("schedule", 3), ("reserve_sms", -1), ("flags", 0x80)):
         d = desc()
         setattr(d, field, bad)
         arr = b._ptr_array([0x20000] * 2)
@@ -154,7 +154,7 @@ def attn_desc(**kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(P=0), 1), (dict(H=0), 1), (dict(mu=0), 1), (dict(B=-1), 1),
-    (dict(S=200), 2), (dict(dh=64), 2), (dict(H=3), 2), (dict(mu=3), 2), (dict(schedule="fused"), 2),
+    (dict(S=200), 2), (dict(dh=64), 2), (dict(H=3), 2), (dict(mu=3), 2), (dict(schedule="fused", B=16, mu=16), 2),
     (dict(d=516), 3),
 ])
 def test_attention_descriptor_validation(lib, kw, status):
@@ -171,7 +171,9 @@ def test_attention_workspace_and_arguments(lib):
     o = 2 * M * Hp * dh * 2
     z = 2 * M * 512 * 4
     align = lambda x: (x + 255) // 256 * 256
-    assert b.attn_workspace_size(d) == align(align(align(256 + qkv) + o) + z)
+    tiles_m, tiles_n = 256 // 128, 512 // 256  # one chunk of 256 rows; d = 512
+    sync = 4 * (2 * tiles_m + tiles_m * tiles_n * 4 + 1)  # a fused output-projection launch's counters
+    assert b.attn_workspace_size(d) == align(align(align(align(256 + sync) + qkv) + o) + z)
     arr = b._ptr_array([0x20000] * 2)
     ws = b.attn_workspace_size(d)
     assert lib.domino_attn_fwd(ctypes.byref(d), None, arr, arr, 0x40000, 0x10000, ws, None) == 1

@@ -41,7 +41,7 @@ def _f64(t):
     return {k: v.to(torch.float64).numpy() for k, v in t.items()}
 
 
-@pytest.mark.parametrize("schedule", ["streams", "serial"])
+@pytest.mark.parametrize("schedule", ["streams", "serial", "fused"])
 @pytest.mark.parametrize("w", [
     wl.ATTN_WORKLOADS["tiny_attn_fwd"],
     wl.AttnWorkload("attn_4tiles", B=2, S=512, d=512, H=4, P=2, mu=2, partial="bf16"),
@@ -64,8 +64,9 @@ def test_attention_deterministic_and_schedule_independent():
     a = _run(w, t, "streams")
     b2 = _run(w, t, "serial")
     c = _run(w.with_(mu=1), t, "streams")
+    f = _run(w, t, "fused")  # each chunk's output projection and shard-sum in one cooperative launch
     torch.cuda.synchronize()
-    assert torch.equal(a, b2) and torch.equal(a, c)
+    assert torch.equal(a, b2) and torch.equal(a, c) and torch.equal(a, f)
 
 
 def test_attention_device_status_and_empty_batch():
@@ -92,12 +93,13 @@ def test_gpt_attention_full_size_sampled():
     assert np.isfinite(Y).all()
 
 
-def test_llama_attention_full_size_sampled():
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_llama_attention_full_size_sampled(schedule):
     # 4 sequences of 2048 tokens, d 4096, 32 heads on 8 shards, 4 chunks of one sequence each, bf16 partials:
     # the first and the last chunk's sequence against the oracle
     w = wl.ATTN_WORKLOADS["llama_attn_fwd"]
     t = wl.generate_attn(w, seed=0)
-    Y = _run(w, t).double().cpu().numpy()
+    Y = _run(w, t, schedule).double().cpu().numpy()
     f = _f64(t)
     for seq in (0, w.B - 1):
         rows = slice(seq * w.S, (seq + 1) * w.S)

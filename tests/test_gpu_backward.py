@@ -170,3 +170,21 @@ def test_llama_fwdbwd_full_size_sampled(schedule):
     assert oracle.max_rel_err(_f64(dB[units]), ref_cols["dB"]) <= TOL
     for g in (dX, dA[0], dA[1], dB):
         assert torch.isfinite(g).all()
+
+
+def test_fused_backward_with_reserved_sms():
+    # the cooperative dX launch on fewer clusters (reserve_sms) gives the same gradients
+    w = wl.Workload("reserve_bwd", M=1000, d=336, F=1968, P=3, mu=2, act="swiglu", partial="bf16", bwd=True)
+    t = wl.generate(w, 23, with_dy=True)
+    dev = torch.device("cuda:0")
+    A_sh, B_sh = b.shard_weights((t["Wg"].to(dev), t["Wu"].to(dev)), t["B"].to(dev), w.P)
+    X, dY = t["X"].to(dev), t["dY"].to(dev)
+    kw = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, schedule="fused")
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, 1, "fused")
+    saved = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device=dev)
+    b.mlp_fwd(X, A_sh, B_sh, saved=saved, **kw)
+    g0 = b.mlp_bwd(X, A_sh, B_sh, dY, saved, **kw)
+    g1 = b.mlp_bwd(X, A_sh, B_sh, dY, saved, reserve_sms=40, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(g0[0], g1[0])
+    assert all(torch.equal(a, c) for a, c in zip(g0[1], g1[1])) and all(torch.equal(a, c) for a, c in zip(g0[2], g1[2]))

@@ -258,3 +258,20 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert "gave up" in b.lib().domino_last_error().decode()
     assert b.query_device_status(ws) == 0  # cleared by the read
     _check_full(wl.WORKLOADS["tiny_gelu_fwd"], schedule="fused")
+
+
+@pytest.mark.parametrize("schedule", ["serial", "streams", "fused"])
+def test_reserve_sms_leaves_results_unchanged(schedule):
+    # the persistent grids shrink to (SMs - reserve_sms); every tile computes the same, so the result is equal
+    w = wl.Workload("reserve", M=1000, d=336, F=1968, P=3, mu=2, act="swiglu", partial="bf16", slices=2)
+    t = wl.generate(w, 19)
+    X, A_sh, B_sh = _device_inputs(w, t)
+    kw = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices, schedule=schedule)
+    y0 = b.mlp_fwd(X, A_sh, B_sh, **kw).clone()
+    y1 = b.mlp_fwd(X, A_sh, B_sh, reserve_sms=16, **kw).clone()
+    y2 = b.mlp_fwd(X, A_sh, B_sh, reserve_sms=torch.cuda.get_device_properties(0).multi_processor_count - 2, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(y0, y2)
+    with pytest.raises(b.DominoError) as e:
+        b.mlp_fwd(X, A_sh, B_sh, reserve_sms=torch.cuda.get_device_properties(0).multi_processor_count - 1, **kw)
+    assert e.value.status == 1  # DOMINO_ERR_INVALID_ARG
