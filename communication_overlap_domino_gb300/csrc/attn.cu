@@ -46,6 +46,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <type_traits>
 
 #include "attn.h"
 #include "ptx.cuh"
@@ -415,7 +416,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         // of those keys), then keys 0-63, reloaded (their probabilities overwrite scores 64-95, already read).
         float sum_even = 0.0f, sum_odd = 0.0f;
         const float nm = -m_run;
-        auto probs = [&](const uint32_t (&x0)[32], const uint32_t (&x1)[32], int kbase, uint32_t (&pk)[32]) {
+        // diag_c: std::true_type for the diagonal block (keys past the row masked), std::false_type for the
+        // others, so that the blocks below the diagonal carry no masking instructions
+        auto probs = [&](auto diag_c, const uint32_t (&x0)[32], const uint32_t (&x1)[32], int kbase,
+                         uint32_t (&pk)[32]) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int k0 = kbase + 2 * e, k1 = k0 + 32;
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
             fma2(y0, y1, __uint_as_float(x0[2 * e]), __uint_as_float(x0[2 * e + 1]), c, c, nm, nm);
             fma2(y2, y3, __uint_as_float(x1[2 * e]), __uint_as_float(x1[2 * e + 1]), c, c, nm, nm);
             float p0 = ex2_approx(y0), p1 = ex2_approx(y1), p2 = ex2_approx(y2), p3 = ex2_approx(y3);
-            if (diag) {
+            if constexpr (decltype(diag_c)::value) {
               p0 = k0 <= r ? p0 : 0.0f;
               p1 = k0 + 1 <= r ? p1 : 0.0f;
               p2 = k1 <= r ? p2 : 0.0f;
@@ -437,7 +441,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         };
         {
           uint32_t pk[32];
-          probs(w0, w1, 64, pk);
+          if (diag) probs(std::true_type{}, w0, w1, 64, pk);
+          else probs(std::false_type{}, w0, w1, 64, pk);
           tmem_st_32x32b_x32(ts + kPCol + 32, pk);
         }
         {
@@ -445,7 +450,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           tmem_ld_32x32b_x32(ts, v0);
           tmem_ld_32x32b_x32(ts + 32, v1);
           tmem_ld_wait();
-          probs(v0, v1, 0, pk);
+          if (diag) probs(std::true_type{}, v0, v1, 0, pk);
+          else probs(std::false_type{}, v0, v1, 0, pk);
           tmem_st_32x32b_x32(ts + kPCol, pk);
         }
         tmem_st_wait();
