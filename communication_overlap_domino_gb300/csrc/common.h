@@ -32,6 +32,7 @@ enum : uint32_t {
   kSiteSelfTest = 8,  // domino_selftest_wait_timeout
   kSiteAttnP = 9,     // attention: MMA waiting for the softmax's P tile
   kSiteAttnPV = 10,   // attention: softmax waiting for P V
+  kSiteAttnX = 11,    // attention: softmax waiting for the partner half of its row
 };
 
 // Epilogue of the tcgen05 GEMM: what is done with each fp32 accumulator tile.
