@@ -192,8 +192,10 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32], 
 // layout is the store map's swizzle: 128-byte rows (fp32) with the 128-byte
 // swizzle, or 64-byte rows (bf16, the backward dG outputs) with the 64-byte
 // swizzle, so the 16-byte writes of a warp spread over all banks.  Two buffers alternate; before one is
-// rewritten, lane 0 waits until the store that last read it is done reading.
-template <bool F32>
+// rewritten, lane 0 waits until the store that last read it is done reading.  kEvictFirst marks the written
+// lines first for eviction from L2 (the backward dG outputs, which no later step of the same launch reads), so
+// they do not push out the operands that the launch's other tiles read again.
+template <bool F32, bool kEvictFirst = false>
 __device__ __forceinline__ void stage_and_store(const EpiArgs& e, const float (&v)[32], int lane, int& sbuf,
                                                 int32_t x, int32_t y) {
   uint8_t* buf = e.stage + (sbuf & 1) * 4096;
@@ -220,7 +222,8 @@ __device__ __forceinline__ void stage_and_store(const EpiArgs& e, const float (&
   fence_proxy_async_shared();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(e.out_map, buf, x, y);
+    if constexpr (kEvictFirst) tma_store_2d_hint(e.out_map, buf, x, y, l2_policy_evict_first());
+    else tma_store_2d(e.out_map, buf, x, y);
     bulk_commit_group();
   }
   ++sbuf;
@@ -428,8 +431,8 @@ __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc
         swiglu_grad2(dg[j], dg[j + 1], du[j], du[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), g[j],
                      g[j + 1], u[j], u[j + 1]);
       if (tma) {
-        stage_and_store<false>(e, dg, lane, sbuf, col, y);
-        stage_and_store<false>(e, du, lane, sbuf, static_cast<int32_t>(e.out_u_off + col), y);
+        stage_and_store<false, true>(e, dg, lane, sbuf, col, y);
+        stage_and_store<false, true>(e, du, lane, sbuf, static_cast<int32_t>(e.out_u_off + col), y);
       } else if (row_ok) {
         store_row_bf16(dst_row + col, dg, n);
         store_row_bf16(dst_row + e.out_u_off + col, du, n);
@@ -439,7 +442,7 @@ __device__ __forceinline__ void epilogue_tile_dg(const EpiArgs& e, uint32_t tacc
 #pragma unroll
       for (int j = 0; j < 32; ++j) dgv[j] = __uint_as_float(r0[j]) * activate_grad<EPI>(g[j]);
       if (tma)
-        stage_and_store<false>(e, dgv, lane, sbuf, col, y);
+        stage_and_store<false, true>(e, dgv, lane, sbuf, col, y);
       else if (row_ok)
         store_row_bf16(dst_row + col, dgv, n);
     }
