@@ -47,6 +47,9 @@ def _f64(t):
     wl.AttnWorkload("attn_4tiles", B=2, S=512, d=512, H=4, P=2, mu=2, partial="bf16"),
     wl.AttnWorkload("attn_one_shard", B=1, S=1024, d=256, H=1, P=1, mu=1, partial="f32"),
     wl.AttnWorkload("attn_3shards", B=3, S=256, d=384, H=6, P=3, mu=3, partial="f32"),
+    # 5 query tiles per sequence (an odd count past one), 4 shards, 2 chunks: items of 1-5 key blocks dealt over
+    # several rounds
+    wl.AttnWorkload("attn_5tiles", B=2, S=640, d=512, H=4, P=4, mu=2, partial="bf16"),
 ], ids=lambda w: w.name if hasattr(w, "name") else w)
 def test_attention_block_matches_oracle(w, schedule):
     t = wl.generate_attn(w, seed=5)
