@@ -8,23 +8,24 @@
 // the output rescaled by exp2(m_old - m_new) when the maximum grows), so no
 // score matrix ever reaches global memory.
 //
-// Persistent kernel, one CTA per SM, one item at a time, with the scores
-// double-buffered in tensor memory: the tensor cores compute the scores of key
-// block j + 1 (and the P V product of block j - 1) while the softmax warps turn
-// the scores of block j into probabilities, so a key block costs the longer of
-// the two, not their sum.  14 warps:
+// Persistent kernel, one CTA per SM, one item at a time, with three score
+// buffers in tensor memory: the tensor cores compute the scores of the next key
+// blocks (and the P V products of the previous ones) while the softmax warps
+// turn the scores of block j into probabilities, so a key block costs the longer
+// of the two, not their sum.  14 warps:
 //   warp 0      TMA producer: the item's Q tile (two slots, so the next item's
 //               tile loads during the current item) and its key and value
 //               blocks through a 4-slot ring of 32 KB slots, in the order the
 //               MMAs consume them.
 //   warp 1      lane 0 issues the MMAs (the warp also allocates the 512
 //               tensor-memory columns), over the CTA's blocks in sequence s:
-//               S_0, S_1, then per s: O += P_s V_s, S_{s+2}.  S_s goes to score
-//               buffer s % 2; P_s overwrites it, and S_{s+2} is issued after
-//               the P V product that reads P_s: the tensor cores execute one
-//               thread's MMAs in issue order, so the product has read P_s
-//               before S_{s+2} overwrites it.  An item's products accumulate
-//               in output buffer (item % 2).
+//               S_0 .. S_2, then per s: O += P_s V_s, S_{s+3}.  S_s goes to
+//               score buffer s % 3; P_s overwrites it, and S_{s+3} is issued
+//               after the P V product that reads P_s: the tensor cores execute
+//               one thread's MMAs in issue order, so the product has read P_s
+//               before S_{s+3} overwrites it.  An item's products accumulate in
+//               the output accumulator, whose first product of the next item
+//               waits until the output warps have read it.
 //   warps 2-5   output: one thread per query row reads the item's finished
 //               output row from tensor memory, frees the buffer and stores
 //               O / l as bf16, while the softmax warps go on with the next item.
@@ -38,20 +39,21 @@
 //               row maximum exceeds it by more than 2^8 in the exp2 domain;
 //               both partners take the same decision from the same maximum and
 //               each rescales its half of the output row in tensor memory once
-//               the previous block's P V product has landed); its 64
+//               the previous block's P V product has landed, the only wait on
+//               the products); its 64
 //               probabilities p = exp2(s c - m) as bf16 pairs over the first 32
 //               of its own score columns, which it has already read.  After an
 //               item's last block the partners add their row sums and hand the
 //               sum to the output warps through shared memory.
-// Tensor memory: score buffers at columns 0 and 128 (keys 2q, 2q + 1 of half h
-// in column 64 h + q once they are probabilities), output buffers at 256 and
-// 384.
+// Tensor memory: score buffers at columns 0, 128 and 256 (keys 2q, 2q + 1 of
+// half h in column 64 h + q once they are probabilities), the output
+// accumulator at 384.
 //
 // Barriers (all waits bounded): ring full / empty per slot, q_full / q_empty
-// per Q slot, s_full / p_full per score buffer, o_full / o_empty per output
-// buffer, l_full per row-sum slot, pv (one phase per P V product), the four
-// row-quarter exchange barriers, final.  Warps arrive once per warp, after
-// __syncwarp.
+// per Q slot, s_full / p_full per score buffer, o_full / o_empty for the output
+// accumulator, l_full / l_empty per row-sum slot, pv for the P V products of
+// even and of odd index (one phase per product), the four row-quarter exchange
+// barriers, final.  Warps arrive once per warp, after __syncwarp.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -84,13 +86,15 @@ constexpr int kBarRingFull = 0;
 constexpr int kBarRingEmpty = kBarRingFull + kRing;
 constexpr int kBarQFull = kBarRingEmpty + kRing;
 constexpr int kBarQEmpty = kBarQFull + kQSlots;
+constexpr int kSBufs = 3;                         // score buffers in tensor memory
 constexpr int kBarSFull = kBarQEmpty + kQSlots;
-constexpr int kBarPFull = kBarSFull + 2;
-constexpr int kBarOFull = kBarPFull + 2;
-constexpr int kBarOEmpty = kBarOFull + 2;
-constexpr int kBarLFull = kBarOEmpty + 2;
-constexpr int kBarPV = kBarLFull + 2;
-constexpr int kBarX = kBarPV + 1;                 // 4: one per row quarter
+constexpr int kBarPFull = kBarSFull + kSBufs;
+constexpr int kBarOFull = kBarPFull + kSBufs;
+constexpr int kBarOEmpty = kBarOFull + 1;
+constexpr int kBarLFull = kBarOEmpty + 1;
+constexpr int kBarLEmpty = kBarLFull + 2;
+constexpr int kBarPV = kBarLEmpty + 2;            // 2: P V products of even and odd index
+constexpr int kBarX = kBarPV + 2;                 // 4: one per row quarter
 constexpr int kBarFinal = kBarX + 4;
 constexpr int kNumBars = kBarFinal + 1;
 
@@ -104,7 +108,7 @@ constexpr int kAttnSmemBytes = kLOff + 4 * 2 * kTile + 1024;  // + alignment sla
 static_assert(kAttnSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kAttnTmemCols = 512;
-constexpr uint32_t kOCol = 256;                   // output buffer b at kOCol + 128 b
+constexpr uint32_t kOCol = kSBufs * 128;          // output accumulator, after the score buffers
 constexpr float kRescaleLog2 = 8.0f;              // lazy rescaling threshold: the maximum may lag by 2^8
 
 struct AttnItem {
@@ -214,16 +218,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       mbar_init(&bars[kBarRingFull + s], 1);
       mbar_init(&bars[kBarRingEmpty + s], 1);
     }
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(&bars[kBarSFull + b], 1);
+      mbar_init(&bars[kBarPFull + b], kSoftWarps);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[kBarQFull + b], 1);
       mbar_init(&bars[kBarQEmpty + b], 1);
-      mbar_init(&bars[kBarSFull + b], 1);
-      mbar_init(&bars[kBarPFull + b], kSoftWarps);
-      mbar_init(&bars[kBarOFull + b], 1);
-      mbar_init(&bars[kBarOEmpty + b], 4);      // the output warps
       mbar_init(&bars[kBarLFull + b], 4);       // the softmax warps of key half 0
+      mbar_init(&bars[kBarLEmpty + b], 4);      // the output warps
+      mbar_init(&bars[kBarPV + b], 1);
     }
-    mbar_init(&bars[kBarPV], 1);
+    mbar_init(&bars[kBarOFull], 1);
+    mbar_init(&bars[kBarOEmpty], 4);            // the output warps
     for (int q = 0; q < 4; ++q) mbar_init(&bars[kBarX + q], 2);  // the row quarter's two softmax warps
     mbar_init(&bars[kBarFinal], 1);
     *abort_flag = 0;
@@ -247,6 +254,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   uint64_t* o_full = bars + kBarOFull;
   uint64_t* o_empty = bars + kBarOEmpty;
   uint64_t* l_full = bars + kBarLFull;
+  uint64_t* l_empty = bars + kBarLEmpty;
   uint64_t* pv_bar = bars + kBarPV;
   uint64_t* final_bar = bars + kBarFinal;
 
@@ -292,12 +300,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       ++g;
       return true;
     };
-    // the MMAs' order: S_0, S_1, then per s: P V_s, S_{s+2}
+    // the MMAs' order: S_0 .. S_2, then per s: P V_s, S_{s+3}
     BlockWalk ws, wv;
     ws.start(a);
     wv.start(a);
     bool ok = true;
-    for (int n = 0; n < 2 && ok && ws.valid(a); ++n) {
+    for (int n = 0; n < kSBufs && ok && ws.valid(a); ++n) {
       ok = load_block(true, ws);
       ws.next(a);
     }
@@ -320,13 +328,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
-    uint32_t g = 0, n_s = 0, n_pv = 0;  // ring slots consumed, S and P V steps issued
+    uint32_t g = 0, n_pv = 0;              // ring slots consumed, P V steps issued
+    uint32_t s_buf = 0, s_ph = 0;          // score buffer and its phase for the next S step
+    uint32_t p_buf = 0, p_ph = 0;          // the same for the next P V step
     BlockWalk ws, wp;
     ws.start(a);
     wp.start(a);
-    // S = Q K^T for the next S block into score buffer n_s % 2
+    // S = Q K^T for the next S block into score buffer s_buf
     auto issue_s = [&](bool ready) -> bool {
-      const uint32_t sb = n_s & 1;
       const int qs = ws.e & 1;
       const uint32_t st = g % kRing, ph = (g / kRing) & 1;
       if (!ready) {
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       tc_fence_after_sync();
       const uint32_t qa = smem_u32(sq + qs * kQBytes);
       const uint32_t ka = smem_u32(ring + st * kSlotBytes);
-      const uint32_t t_s = tmem_base + sb * kTile;
+      const uint32_t t_s = tmem_base + s_buf * kTile;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint64_t ad = smem_desc_k128(qa + (k >> 2) * kSub) + 2 * (k & 3);
@@ -345,54 +354,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         mma_bf16_ss(t_s, ad, bd, idesc_s, k != 0 ? 1u : 0u);
       }
       mma_commit(&ring_empty[st]);
-      mma_commit(&s_full[sb]);
+      mma_commit(&s_full[s_buf]);
       if (ws.j == ws.it.i) mma_commit(&q_empty[qs]);  // the item's last scores: its Q slot is free
       ++g;
-      ++n_s;
+      if (++s_buf == kSBufs) {
+        s_buf = 0;
+        s_ph ^= 1;
+      }
       ws.next(a);
       return true;
     };
     // O += P V for the next P V block, once its probabilities are written (and, for an item's first block,
-    // once the output buffer's previous item has been read)
+    // once the output warps have read the previous item's output)
     auto issue_pv = [&](bool ready) -> bool {
-      const uint32_t sb = n_pv & 1;
-      const int ob = wp.e & 1;
       const uint32_t st = g % kRing, ph = (g / kRing) & 1;
       if (!ready) {
-        if (wp.j == 0 &&
-            !mbar_wait(&o_empty[ob], ((wp.e >> 1) & 1) ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, wp.t))
+        if (wp.j == 0 && !mbar_wait(o_empty, (wp.e & 1) ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, wp.t))
           return false;
-        if (!mbar_wait(&p_full[sb], (n_pv >> 1) & 1, abort_flag, tmo, a.status, kSiteAttnP, wp.t)) return false;
+        if (!mbar_wait(&p_full[p_buf], p_ph, abort_flag, tmo, a.status, kSiteAttnP, wp.t)) return false;
         if (!mbar_wait(&ring_full[st], ph, abort_flag, tmo, a.status, kSiteMmaFull, wp.t)) return false;
       }
       tc_fence_after_sync();
       const uint32_t va = smem_u32(ring + st * kSlotBytes);
-      const uint32_t t_p = tmem_base + sb * kTile;
-      const uint32_t t_o = tmem_base + kOCol + ob * kTile;
+      const uint32_t t_p = tmem_base + p_buf * kTile;
+      const uint32_t t_o = tmem_base + kOCol;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {  // 16 keys per step: 8 columns of P (keys 0-63 at 0-31, 64-127 at 64-95)
         const uint64_t bd = smem_desc_mn128(va + (k >> 2) * kSub) + (2048 >> 4) * (k & 3);
         mma_bf16_ts(t_o, t_p + 64 * (k >> 2) + 8 * (k & 3), bd, idesc_pv, (wp.j | k) != 0 ? 1u : 0u);
       }
       mma_commit(&ring_empty[st]);
-      mma_commit(pv_bar);
-      if (wp.j == wp.it.i) mma_commit(&o_full[ob]);
+      mma_commit(&pv_bar[n_pv & 1]);
+      if (wp.j == wp.it.i) mma_commit(o_full);
       ++g;
       ++n_pv;
+      if (++p_buf == kSBufs) {
+        p_buf = 0;
+        p_ph ^= 1;
+      }
       wp.next(a);
       return true;
     };
     bool ok = true;
-    for (int n = 0; n < 2 && ok && ws.valid(a); ++n) ok = issue_s(false);
+    for (int n = 0; n < kSBufs && ok && ws.valid(a); ++n) ok = issue_s(false);
     while (ok && wp.valid(a)) {
-      // a step's barriers tested back to back, without blocking: a shared-memory access of this thread waits
-      // behind the tensor cores' operand reads, and independent tests overlap.  If any is not complete, the
-      // step's bounded waits run one by one.
+      // a step's barriers tested back to back, without blocking; if any is not complete, the step's bounded
+      // waits run one by one
       const bool has_s = ws.valid(a);
       const uint32_t g1 = g + 1;
       const bool ready =
-          mbar_test(&p_full[n_pv & 1], (n_pv >> 1) & 1) & mbar_test(&ring_full[g % kRing], (g / kRing) & 1) &
-          (wp.j != 0 || mbar_test(&o_empty[wp.e & 1], ((wp.e >> 1) & 1) ^ 1)) &
+          mbar_test(&p_full[p_buf], p_ph) & mbar_test(&ring_full[g % kRing], (g / kRing) & 1) &
+          (wp.j != 0 || mbar_test(o_empty, (wp.e & 1) ^ 1)) &
           (!has_s || (mbar_test(&ring_full[g1 % kRing], (g1 / kRing) & 1) &
                       (ws.j != 0 || mbar_test(&q_full[ws.e & 1], (ws.e >> 1) & 1))));
       ok = issue_pv(ready);
@@ -406,16 +418,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t to = tmem_base + lane_off + kOCol;
     for (int e = 0, t = attn_round_item(0); t < a.num_items && !*abort_flag; t = attn_round_item(++e)) {
       const AttnItem it = attn_item(a, t);
-      const int ob = e & 1;
-      const uint32_t ph = (e >> 1) & 1;
-      if (!mbar_wait(&l_full[ob], ph, abort_flag, tmo, a.status, kSiteAttnPV, t) ||
-          !mbar_wait(&o_full[ob], ph, abort_flag, tmo, a.status, kSiteAttnPV, t))
+      const int lb = e & 1;
+      if (!mbar_wait(&l_full[lb], (e >> 1) & 1, abort_flag, tmo, a.status, kSiteAttnPV, t) ||
+          !mbar_wait(o_full, e & 1, abort_flag, tmo, a.status, kSiteAttnPV, t))
         break;
       tc_fence_after_sync();
-      const float inv = 1.0f / lsum[ob * kTile + r];
-      const uint32_t to = tmem_base + lane_off + kOCol + ob * kTile;
+      const float inv = 1.0f / lsum[lb * kTile + r];
       const int64_t grow = a.row0 + static_cast<int64_t>(it.b) * a.S + it.i * kTile + r;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o[it.p]) + grow * a.ldo + it.h * kTile);
 #pragma unroll
@@ -424,10 +435,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         tmem_ld_32x32b_x32(to + hb * 64, o0);
         tmem_ld_32x32b_x32(to + hb * 64 + 32, o1);
         tmem_ld_wait();
-        if (hb == 1) {  // the output row and its sum are read: the buffer (and the sum's slot) are free
+        if (hb == 1) {  // the output row and its sum are read: the accumulator and the sum's slot are free
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&o_empty[ob]);
+          if (lane == 0) {
+            mbar_arrive(o_empty);
+            mbar_arrive(&l_empty[lb]);
+          }
         }
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
@@ -448,10 +462,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     const int r = quarter * 32 + lane;       // query row within the tile
     const int rr = r - 64 * h;               // on the diagonal block, keys 64 h + e with e <= rr are visible
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t to = tmem_base + lane_off + kOCol + 64 * h;  // this half of the output row
     uint64_t* xbar = bars + kBarX + quarter;
     float* xq = xslots + quarter * 64;       // + parity * 256 + half * 32 + row
     const float c = a.scale_log2;
     uint32_t s = 0, x_count = 0;             // the CTA's key blocks processed, exchanges made
+    uint32_t s_buf = 0, s_ph = 0;            // score buffer of block s and its phase
     // one value with the partner thread of the same row (the other half): both write their own slot, arrive
     // once per warp and read the other's slot.  Slots alternate by parity, so a slot is written again only
     // after the partner has arrived at the next exchange, i.e. after it has read this one.
@@ -467,14 +483,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     };
     for (int e = 0, t = attn_round_item(0); t < a.num_items && !*abort_flag; t = attn_round_item(++e)) {
       const AttnItem it = attn_item(a, t);
-      const uint32_t to = tmem_base + lane_off + kOCol + (e & 1) * kTile + 64 * h;  // this half of the output row
       float m_run = -INFINITY, l_run = 0.0f;
       bool ok = true;
       for (int j = 0; j <= it.i; ++j, ++s) {
-        const uint32_t sb = s & 1;
-        if (!mbar_wait(&s_full[sb], (s >> 1) & 1, abort_flag, tmo, a.status, kSiteEpilogueTmemFull, t)) {
+        const uint32_t sb = s_buf;
+        if (!mbar_wait(&s_full[sb], s_ph, abort_flag, tmo, a.status, kSiteEpilogueTmemFull, t)) {
           ok = false;
           break;
+        }
+        if (++s_buf == kSBufs) {
+          s_buf = 0;
+          s_ph ^= 1;
         }
         tc_fence_after_sync();
         const uint32_t ts = tmem_base + lane_off + sb * kTile + 64 * h;  // this half's scores / probabilities
@@ -507,8 +526,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           m_run = m_blk;
         }
         // the 64 probabilities as bf16 pairs (keys 64 h + 2q, 64 h + 2q + 1 -> column q of this half), over
-        // score columns this thread has read.  diag_c: std::true_type for the diagonal block (keys past the
-        // row masked), std::false_type for the others, so that the blocks below it carry no masking
+        // score columns this thread has read (the P V product that read this buffer's previous probabilities
+        // preceded these scores).  diag_c: std::true_type for the diagonal block (keys past the row masked),
+        // std::false_type for the others, so that the blocks below it carry no masking
         float sum_even = 0.0f, sum_odd = 0.0f;
         const float nm = -m_run;
         // x: 32 scores (keys 64 h + kb + e), packed into 16 columns
@@ -538,14 +558,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           else probs(std::false_type{}, v1, 32, pk);
           tmem_st_32x32b_x16(ts + 16, pk);
         }
-        // the previous block's P V product has landed (one phase per product, waited in order): only then may
-        // the output be rescaled.  Tensor-memory loads and stores are warp-wide: the whole warp rescales its
-        // half rows (alpha = 1 where the maximum stayed).
-        if (s > 0 && !mbar_wait(pv_bar, (s - 1) & 1, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
-          ok = false;
-          break;
-        }
+        // rescaling the output (rare) waits for the previous block's P V product.  Products of even and odd
+        // index complete on two barriers; the one of block s - 1 is the next phase of its barrier: the product
+        // of block s - 3 preceded these scores, and that of block s + 1 cannot start before this block's
+        // probabilities.  Tensor-memory loads and stores are warp-wide: the whole warp rescales its half rows
+        // (alpha = 1 where the maximum stayed).
         if (j > 0 && __any_sync(0xffffffffu, grow_m)) {
+          if (!mbar_wait(&pv_bar[(s - 1) & 1], ((s - 1) >> 1) & 1, abort_flag, tmo, a.status, kSiteAttnPV, t)) {
+            ok = false;
+            break;
+          }
           tc_fence_after_sync();
 #pragma unroll 1
           for (int cc = 0; cc < 2; ++cc) {
@@ -569,12 +591,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         l_run = l_run * alpha + (sum_even + sum_odd);
       }
       if (!ok) break;
-      // the row sum for the output warps: the slot of this item's parity is free once the output warps have
-      // read the item two back (their o_empty arrival)
+      // the row sum for the output warps, in the slot of this item's parity once they have read the item two back
       float l_other;
       if (!exchange(l_run, l_other, t)) break;
       if (h == 0) {
-        if (!mbar_wait(&o_empty[e & 1], ((e >> 1) & 1) ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, t)) break;
+        if (!mbar_wait(&l_empty[e & 1], ((e >> 1) & 1) ^ 1, abort_flag, tmo, a.status, kSiteMmaTmemEmpty, t)) break;
         lsum[(e & 1) * kTile + r] = l_run + l_other;
         __syncwarp();
         if (lane == 0) mbar_arrive(&l_full[e & 1]);
