@@ -50,6 +50,9 @@ def _f64(t):
     # 5 query tiles per sequence (an odd count past one), 4 shards, 2 chunks: items of 1-5 key blocks dealt over
     # several rounds
     wl.AttnWorkload("attn_5tiles", B=2, S=640, d=512, H=4, P=4, mu=2, partial="bf16"),
+    # 320 items of one key block each: every CTA runs several rounds and hands its output accumulator, row-sum
+    # slots and Q slots over on every block
+    wl.AttnWorkload("attn_many_short", B=160, S=128, d=256, H=2, P=2, mu=1, partial="f32"),
 ], ids=lambda w: w.name if hasattr(w, "name") else w)
 def test_attention_block_matches_oracle(w, schedule):
     t = wl.generate_attn(w, seed=5)
