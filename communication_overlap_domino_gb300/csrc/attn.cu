@@ -201,6 +201,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams a) {
+  grid_dependency_wait();  // launched as a dependent of the stream's previous kernel
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem;                              // Q slots
@@ -647,8 +648,8 @@ domino_status_t launch_attn_fwd(const AttnLaunch& L, int num_sms, cudaStream_t s
   if (a.num_items == 0) return DOMINO_OK;
   const int grid = a.num_items < num_sms ? a.num_items : num_sms;
   void* args[] = {&a};
-  const cudaError_t st = cudaLaunchKernel(reinterpret_cast<const void*>(&attn_fwd_kernel), dim3(grid),
-                                          dim3(kAttnThreads), args, kAttnSmemBytes, stream);
+  const cudaError_t st = launch_after_previous(reinterpret_cast<const void*>(&attn_fwd_kernel), dim3(grid),
+                                               dim3(kAttnThreads), kAttnSmemBytes, stream, args);
   if (st != cudaSuccess) {
     if (err) *err = std::string("attention launch: ") + cudaGetErrorString(st);
     return DOMINO_ERR_CUDA;

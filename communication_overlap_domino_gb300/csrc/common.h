@@ -142,4 +142,22 @@ struct ShardSumParams {
   int32_t f32;  // 1: fp32 partials, 0: bf16 partials
 };
 
+// Launches `fn` as a programmatic dependent of the stream's previous kernel, so that its launch overlaps that
+// kernel's end instead of following it; the kernel calls grid_dependency_wait() before its first
+// global-memory access.  Without a previous kernel (or after another stream operation) it is a plain launch.
+inline cudaError_t launch_after_previous(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                         void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 }  // namespace domino

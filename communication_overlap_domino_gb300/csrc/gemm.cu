@@ -50,6 +50,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& sha
 
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+  grid_dependency_wait();  // launched as a dependent of the stream's previous kernel
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smem_a = smem;
@@ -411,7 +412,7 @@ domino_status_t launch_gemm(const GemmLaunch& L, int max_ctas, cudaStream_t stre
     return DOMINO_ERR_INVALID_ARG;
   }
   void* args[] = {&p};
-  cudaError_t st = cudaLaunchKernel(fn, dim3(grid), dim3(kGemmThreads), args, kGemmSmemBytes, stream);
+  cudaError_t st = launch_after_previous(fn, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, stream, args);
   if (st != cudaSuccess) {
     if (err) *err = std::string("gemm launch: ") + cudaGetErrorString(st);
     return DOMINO_ERR_CUDA;

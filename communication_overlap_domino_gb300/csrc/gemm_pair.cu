@@ -257,6 +257,7 @@ __device__ __forceinline__ void gemm_pair_body(const GemmParams& p) {
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  grid_dependency_wait();  // launched as a dependent of the stream's previous kernel
   gemm_pair_body<EPI, A_MN, B_MN>(p);
 }
 
@@ -378,8 +379,7 @@ domino_status_t launch_gemm_pair(const GemmLaunch& L, int max_clusters, cudaStre
   }
   const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
   void* args[] = {&p};
-  cudaError_t st =
-      cudaLaunchKernel(fn, dim3(2 * clusters), dim3(kGemmThreads), args, kPairSmemBytes, stream);
+  cudaError_t st = launch_after_previous(fn, dim3(2 * clusters), dim3(kGemmThreads), kPairSmemBytes, stream, args);
   if (st != cudaSuccess) {
     if (err) *err = std::string("pair gemm launch: ") + cudaGetErrorString(st);
     return DOMINO_ERR_CUDA;

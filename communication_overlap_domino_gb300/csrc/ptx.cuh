@@ -15,6 +15,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Waits until the grid that precedes this one on its stream has completed and its memory operations are
+// visible (programmatic dependent launch: this grid may have been launched before that one finished).  A grid
+// launched with launch_after_previous() calls it before its first global-memory access.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

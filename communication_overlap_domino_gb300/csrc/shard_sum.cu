@@ -54,6 +54,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // NP > 0: P fixed at compile time; NP == 0: runtime P (<= kMaxShards).
 template <int NP, bool F32>
 __global__ void __launch_bounds__(256) shard_sum_kernel(const __grid_constant__ ShardSumParams p) {
+  grid_dependency_wait();  // launched as a dependent of the stream's previous kernel
   const int P = NP > 0 ? NP : p.P;
   const uint32_t vec_per_row = static_cast<uint32_t>(p.cols / 8);
   const uint32_t nvec = static_cast<uint32_t>(p.rows) * vec_per_row;
@@ -161,7 +162,7 @@ domino_status_t launch_shard_sum(const ShardSumParams& p, int num_sms, cudaStrea
   void* fn = p.f32 ? pick<true>(p.P) : pick<false>(p.P);
   ShardSumParams q = p;
   void* args[] = {&q};
-  cudaError_t st = cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, stream);
+  cudaError_t st = launch_after_previous(fn, dim3(grid), dim3(kThreads), 0, stream, args);
   if (st != cudaSuccess) {
     if (err) *err = std::string("shard_sum launch: ") + cudaGetErrorString(st);
     return DOMINO_ERR_CUDA;
