@@ -83,6 +83,16 @@ def ncu_traffic(kernel_kind, workload):
     return entry.get("dram_bytes_per_launch")
 
 
+def device_info(dev):
+    """The GPU the line was measured on: the L2 size and the SM count bear on how the kernels' DRAM re-reads and
+    grids come out, which differ between boxes."""
+    import torch
+
+    pr = torch.cuda.get_device_properties(dev)
+    return {"name": pr.name, "sms": pr.multi_processor_count, "l2_bytes": int(getattr(pr, "L2_cache_size", 0)),
+            "memory_bytes": int(pr.total_memory)}
+
+
 def tensor_peak_for(peaks, launch_s):
     """The bf16 denominator for a kernel whose launches last launch_s seconds: the burst figure (a GEMM
     timed alone, best of 10) for launches under a second, the sustained one (seconds back to back under
@@ -648,6 +658,7 @@ def run_ours(args, w, rank, world, local_rank):
             "frac_of_mma_probe": round(dom_tflops / probe["tflops"], 4),
         },
         "tensor_probe": probe,
+        "device": device_info(dev),
         "shard_sum": None if ss_gbs is None else {
             "bound": "hbm",
             "achieved": round(ss_gbs, 1),
@@ -825,6 +836,7 @@ def run_attn(args, w, rank, world, local_rank):
             "frac_of_mma_probe": round(a_tf / probe["tflops"], 4),
         },
         "tensor_probe": probe,
+        "device": device_info(dev),
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
                         "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["flops"] else None,
                         "share": round(v["total_ms"] / sum(x["total_ms"] for x in kinds.values()), 4)}
