@@ -1341,6 +1341,8 @@ domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t
     return fail(DOMINO_ERR_INVALID_ARG, "bad rows/cols/leading dimensions");
   if (cols % 8 || ld_partial % 8 || ld_y % 8)
     return fail(DOMINO_ERR_ALIGNMENT, "cols and leading dimensions must be multiples of 8");
+  if (rows > 0 && cols > 0 && rows * (cols / 8) >= (int64_t(1) << 32))
+    return fail(DOMINO_ERR_UNSUPPORTED, "rows * cols / 8 must be below 2^32");
   for (int p = 0; p < P; ++p) {
     if (!partials[p]) return fail(DOMINO_ERR_INVALID_ARG, "NULL partial pointer");
     if (!aligned16(partials[p])) return fail(DOMINO_ERR_ALIGNMENT, "partials must be 16-byte aligned");

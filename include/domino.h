@@ -218,7 +218,9 @@ DOMINO_API domino_status_t domino_mlp_bwd(const domino_mlp_desc_t* desc, const v
  * fp32 accumulation in shard order, one round-to-nearest-even at the end.
  * partials: HOST array of P device pointers to [rows, cols] matrices with leading
  * dimension ld_partial (elements) in `partial_dtype`; Y [rows, cols] bf16 with
- * leading dimension ld_y.  cols, ld_partial and ld_y must be multiples of 8. */
+ * leading dimension ld_y.  cols, ld_partial and ld_y must be multiples of 8
+ * (else DOMINO_ERR_ALIGNMENT), and rows * cols / 8 (the 16-byte vectors of Y,
+ * counted with 32-bit indices) below 2^32 (else DOMINO_ERR_UNSUPPORTED). */
 DOMINO_API domino_status_t domino_shard_sum(const void* const* partials, int32_t P, int32_t partial_dtype, int64_t rows,
                                  int64_t cols, int64_t ld_partial, void* Y, int64_t ld_y, void* stream);
 

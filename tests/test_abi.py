@@ -116,6 +116,10 @@ def test_shard_sum_validation(lib):
     assert lib.domino_shard_sum(b._ptr_array([0x20002, 0x20000]), 2, 0, 4, 8, 8, 0x40000, 8, None) == 3
     # empty problems are a no-op that needs no device
     assert lib.domino_shard_sum(arr, 2, 0, 0, 8, 8, 0x40000, 8, None) == 0
+    # 16-byte vectors of Y are counted with 32-bit indices: rows * cols / 8 must stay below 2^32
+    # (rejected before any device is touched)
+    assert lib.domino_shard_sum(arr, 2, 0, 1 << 29, 64, 64, 0x40000, 64, None) == 2
+    assert "2^32" in lib.domino_last_error().decode()
 
 
 def test_empty_batch_is_noop(lib):
