@@ -6,7 +6,7 @@ shard-sum for every chunk and slice), inputs resident in HBM.  Prints ONE JSON
 line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mu MU]
-                  [--schedule fused|streams|serial] [--impl ours|reference]
+                  [--schedule fused|streams|serial] [--plan] [--impl ours|reference]
 
 N > 1 runs under torch.distributed.run, one independent replica per GPU (the
 workload has no exchange between GPUs: weak scaling, no data-path collective;
@@ -67,8 +67,9 @@ def kernel_source_hash(kernel_kind):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_kind, workload):
-    """DRAM bytes per launch from a committed ncu capture, if it matches the kernel's current sources."""
+def ncu_traffic(kernel_kind, workload, mu):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken at the same number of chunks (a launch
+    covers one chunk, or all of them) and matches the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -76,7 +77,7 @@ def ncu_traffic(kernel_kind, workload):
     except (OSError, ValueError):
         return None
     entry = rec.get("kernels", {}).get(f"{workload}/{kernel_kind}")
-    if entry is None or kernel_kind not in KERNEL_SOURCES:
+    if entry is None or kernel_kind not in KERNEL_SOURCES or entry.get("mu") != mu:
         return None
     if entry.get("source_hash") != kernel_source_hash(kernel_kind):
         return None
@@ -654,7 +655,7 @@ def run_ours(args, w, rank, world, local_rank):
             "avg_launch_us": round(kinds[dominant]["avg_us"], 2),
             "frac_of_sustained": round(dom_tflops / sustained_tf, 4),
             "flops_per_launch": dom_flops_per_launch,
-            "traffic": ncu_traffic(dominant, w.name),
+            "traffic": ncu_traffic(dominant, w.name, w.mu),
             "frac_of_mma_probe": round(dom_tflops / probe["tflops"], 4),
         },
         "tensor_probe": probe,
@@ -666,7 +667,7 @@ def run_ours(args, w, rank, world, local_rank):
             "unit": "GB/s",
             "frac": round(ss_gbs / float(peaks.get("hbm_gbs")), 4),
             "bytes_per_launch": ss_bytes,
-            "traffic": ncu_traffic("shard_sum", w.name),
+            "traffic": ncu_traffic("shard_sum", w.name, w.mu),
         },
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_us"], 2),
                         "tflops": round(v["flops"] / (v["total_ms"] * 1e-3) / 1e12, 1) if v["flops"] else None,
@@ -871,7 +872,8 @@ def run_attn(args, w, rank, world, local_rank):
         "data": "synthetic: seeded N(0,1) activations, N(0,1/fan_in) weights, bf16",
         "config": {"workload": w.name, "B": w.B, "S": w.S, "d": w.d, "H": w.H, "dh": w.dh, "P": w.P, "mu": w.mu,
                    "partials": w.partial, "schedule": schedule, "causal": True,
-                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+                   "l2": "flushed between steps (256 MiB write outside the step events)",
+                   **({"plan": args.plan_result} if getattr(args, "plan_result", None) else {})},
         "pct_of_bf16_peak": round(100.0 * value / world / peak_tf, 2),
         "exposed_reduce_us_per_layer": round(1e3 * exposed_ms, 2),
         "exposed_reduce_frac": round(exposed_ms / span_ms, 4) if span_ms > 0 else None,
@@ -882,7 +884,7 @@ def run_attn(args, w, rank, world, local_rank):
             "bound": "tensor", "achieved": round(a_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
             "frac": round(a_tf / peak_tf, 4), "peak_source": f"{peak_src} {peak_key}",
             "avg_launch_us": round(kinds["attn"]["avg_us"], 2), "frac_of_sustained": round(a_tf / sustained_tf, 4),
-            "flops_per_launch": float(core_flops_chunk), "traffic": ncu_traffic("attn", w.name),
+            "flops_per_launch": float(core_flops_chunk), "traffic": ncu_traffic("attn", w.name, w.mu),
             "frac_of_mma_probe": round(a_tf / probe["tflops"], 4),
         },
         "tensor_probe": probe,
@@ -1006,9 +1008,11 @@ def main():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--mu", type=int, default=None)
     ap.add_argument("--schedule", choices=("streams", "serial", "fused"), default=None,
-                    help="default: fused for the MLP workloads, streams for the attention block (its faster schedule)")
+                    help="default: fused for the MLP workloads; for the attention block, with --mu not given "
+                         "either, domino_attn_plan's mu and schedule (streams, its faster schedule)")
     ap.add_argument("--plan", action="store_true",
-                    help="take mu and the schedule from domino_mlp_plan (overrides --mu and --schedule)")
+                    help="take mu and the schedule from domino_mlp_plan (domino_attn_plan for the attention "
+                         "block; overrides --mu and --schedule)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ab-pairs", type=int, default=30,
@@ -1023,6 +1027,8 @@ def main():
     if args.mu is not None:
         w = w.with_(mu=args.mu)
     attention = name in wl.ATTN_WORKLOADS
+    if attention and args.mu is None and args.schedule is None:
+        args.plan = True  # the attention block runs at domino_attn_plan's mu unless told otherwise
     if args.schedule is None:
         args.schedule = "streams" if attention else "fused"
 
@@ -1042,7 +1048,10 @@ def main():
         import torch
         from communication_overlap_domino_gb300 import binding as b
         torch.cuda.set_device(local_rank)
-        args.plan_result = b.plan(w.M, w.d, w.F, w.P, w.act, w.partial, w.slices)
+        if attention:
+            args.plan_result = b.plan_attn(w.B, w.S, w.d, w.H, w.P, w.partial, dh=w.dh)
+        else:
+            args.plan_result = b.plan(w.M, w.d, w.F, w.P, w.act, w.partial, w.slices)
         w = w.with_(mu=args.plan_result["mu"])
         args.schedule = args.plan_result["schedule"]
     if world > 1:

@@ -141,6 +141,7 @@ SIGNATURES = [
     ("domino_kernel_times", ctypes.c_int32, [ctypes.POINTER(KernelTime), ctypes.c_int32]),
     ("domino_kernel_times_reset", None, []),
     ("domino_mlp_plan", ctypes.c_int, [ctypes.POINTER(MlpDesc), ctypes.POINTER(PlanHw), ctypes.POINTER(Plan)]),
+    ("domino_attn_plan", ctypes.c_int, [ctypes.POINTER(AttnDesc), ctypes.POINTER(PlanHw), ctypes.POINTER(Plan)]),
     ("domino_mlp_interleaved_workspace_size", ctypes.c_size_t, [ctypes.POINTER(MlpDesc)]),
     ("domino_attn_workspace_size", ctypes.c_size_t, [ctypes.POINTER(AttnDesc)]),
     ("domino_attn_fwd", ctypes.c_int, [ctypes.POINTER(AttnDesc), _VP, _VPP, _VPP, _VP, _VP, ctypes.c_size_t, _VP]),
@@ -510,6 +511,20 @@ def plan(M: int, d: int, F: int, P: int, act: str, partial: str, out_slices: int
     sched = {v: k for k, v in SCHEDULE.items()}[out.schedule]
     return {"mu": out.mu, "schedule": sched, "reason": PLAN_REASON.get(out.reason, out.reason),
             "gemm1_tiles_per_chunk": out.gemm1_tiles_per_chunk, "chunk_h_bytes": out.chunk_h_bytes,
+            "l2_budget_bytes": out.l2_budget_bytes}
+
+
+def plan_attn(B: int, S: int, d: int, H: int, P: int, partial: str, *, dh: int = 128, num_sms: int = 0,
+              l2_bytes: int = 0) -> dict:
+    """domino_attn_plan: the number of sequence chunks and the schedule for this attention block.
+    Hardware figures left at 0 are read from the current CUDA device."""
+    desc = make_attn_desc(B, S, d, H, P, 1, partial, dh=dh)
+    hw = PlanHw(num_sms=num_sms, fused_available=0, l2_bytes=l2_bytes)
+    out = Plan()
+    _check(lib().domino_attn_plan(ctypes.byref(desc), ctypes.byref(hw), ctypes.byref(out)), "domino_attn_plan")
+    sched = {v: k for k, v in SCHEDULE.items()}[out.schedule]
+    return {"mu": out.mu, "schedule": sched, "reason": PLAN_REASON.get(out.reason, out.reason),
+            "proj_tiles_per_chunk": out.gemm1_tiles_per_chunk, "chunk_qkv_bytes": out.chunk_h_bytes,
             "l2_budget_bytes": out.l2_budget_bytes}
 
 

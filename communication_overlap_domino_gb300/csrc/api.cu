@@ -885,6 +885,10 @@ domino_status_t validate_desc(const domino_mlp_desc_t* desc) {
   Shape s;
   return check_desc(desc, &s);
 }
+domino_status_t validate_attn_desc(const domino_attn_desc_t* desc) {
+  AttnShape s;
+  return check_attn_desc(desc, &s);
+}
 }  // namespace domino
 
 // ====================================================================== ABI

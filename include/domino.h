@@ -465,6 +465,28 @@ typedef struct domino_plan {
 DOMINO_API domino_status_t domino_mlp_plan(const domino_mlp_desc_t* problem, const domino_plan_hw_t* hw,
                                            domino_plan_t* out);
 
+/* The same selection for the attention block (domino_attn_fwd), whose chunks
+ * are mu groups of B / mu whole sequences:
+ *   - schedule: always DOMINO_SCHEDULE_STREAMS (its output projection writes
+ *     the partials at close to the memory's rate, so a shard-sum folded into
+ *     that launch contends with it rather than hiding behind it);
+ *   - candidates: mu in {1, 2, 4, ...} with mu | B and mu <= DOMINO_MAX_PIECES;
+ *     a candidate fills the GPU when one chunk's Q|K|V projection has at least
+ *     one paired 256 x 256 tile per 2-CTA cluster;
+ *   - mu = the smallest filling candidate whose chunk of Q|K|V, (B / mu) S 3 H
+ *     dh 2 bytes, fits in 9/10 of the L2; else the largest filling candidate;
+ *     else mu = 1.  (The Q|K|V size stands in for how much work each chunk's
+ *     launches get against the shard-sum that chunking hides; on the GPT- and
+ *     Llama-style blocks it picks the fastest mu of 1, 2 and 4.)
+ * problem: as for domino_attn_fwd (mu, schedule and flags are ignored).  hw: as
+ * for domino_mlp_plan (fused_available is not consulted).  out: the choice,
+ * with gemm1_tiles_per_chunk = the projection's paired tiles of one chunk and
+ * chunk_h_bytes = one chunk's Q|K|V bytes.  Errors: as domino_attn_fwd would
+ * reject the problem with mu = 1, or DOMINO_ERR_CUDA when a device query fails.
+ * Launches nothing and allocates nothing. */
+DOMINO_API domino_status_t domino_attn_plan(const domino_attn_desc_t* problem, const domino_plan_hw_t* hw,
+                                            domino_plan_t* out);
+
 /* Tensor-core rate probe: the dense bf16 throughput of this GPU's tcgen05 MMAs
  * on their own, the ceiling the GEMM main loops approach.  Each 2-CTA cluster
  * (one CTA per SM) issues `mmas_per_cluster` back-to-back paired MMAs of

@@ -40,15 +40,17 @@ def test_traffic_record_entries_are_well_formed(bench):
         workload, kind = key.split("/")
         assert kind in bench.KERNEL_SOURCES, key
         assert entry["dram_bytes_per_launch"] > 0 and entry["algorithmic_bytes"] > 0
-        assert "source_hash" in entry
-        got = bench.ncu_traffic(kind, workload)
+        assert "source_hash" in entry and entry["mu"] >= 1
+        got = bench.ncu_traffic(kind, workload, entry["mu"])
         # a capture is reported exactly when its hash matches the kernel's current sources
         assert (got is not None) == (entry["source_hash"] == bench.kernel_source_hash(kind)), key
+        # and only at the number of chunks it was captured at (a launch covers one chunk, or all of them)
+        assert bench.ncu_traffic(kind, workload, 2 * entry["mu"]) is None, key
 
 
 def test_traffic_lookup_rejects_unknown(bench):
-    assert bench.ncu_traffic("no_such_kernel", "gpt_gelu_fwd") is None
-    assert bench.ncu_traffic("fused", "no_such_workload") is None
+    assert bench.ncu_traffic("no_such_kernel", "gpt_gelu_fwd", 2) is None
+    assert bench.ncu_traffic("fused", "no_such_workload", 2) is None
 
 
 def test_whole_job_throughput_counts_all_ranks(bench):

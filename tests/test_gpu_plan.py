@@ -1,5 +1,6 @@
-"""domino_mlp_plan on the GB300 itself: the hardware figures come from the
-device, and the planned configuration runs and matches the oracle."""
+"""domino_mlp_plan and domino_attn_plan on the GB300 itself: the hardware
+figures come from the device, and the planned configurations run and match the
+oracles."""
 import pytest
 import torch
 
@@ -40,4 +41,30 @@ def test_planned_configuration_runs():
     Y = b.mlp_fwd(t["X"].to(dev), A_sh, B_sh, F=w.F, mu=w.mu, act=w.act, partial=w.partial, schedule=p["schedule"])
     f = wl.to_float64(t)
     err = oracle.max_rel_err(Y.double().cpu().numpy(), oracle.mlp_fwd(f["X"], f["A"], f["B"], w.act))
+    assert err <= 1e-2
+
+
+def test_attn_plan_reads_the_device():
+    props = torch.cuda.get_device_properties(0)
+    w = wl.ATTN_WORKLOADS["llama_attn_fwd"]
+    p = b.plan_attn(w.B, w.S, w.d, w.H, w.P, w.partial)
+    explicit = b.plan_attn(w.B, w.S, w.d, w.H, w.P, w.partial, num_sms=props.multi_processor_count,
+                           l2_bytes=props.L2_cache_size)
+    assert p == explicit
+    assert p["l2_budget_bytes"] == props.L2_cache_size // 10 * 9
+    assert w.B % p["mu"] == 0 and p["schedule"] == "streams"
+
+
+def test_attn_planned_configuration_runs():
+    import oracle.attention as att
+    w0 = wl.AttnWorkload("attn_plan_small", B=4, S=512, d=512, H=4, P=2, mu=1, partial="f32")
+    p = b.plan_attn(w0.B, w0.S, w0.d, w0.H, w0.P, w0.partial, num_sms=16, l2_bytes=1 << 20)
+    assert p["mu"] > 1  # the small L2 forces chunking
+    w = w0.with_(mu=p["mu"])
+    t = wl.generate_attn(w, seed=23)
+    dev = torch.device("cuda:0")
+    qkv_sh, o_sh = b.shard_attn_weights(t["Wqkv"].to(dev), t["Wo"].to(dev), w.H, w.P)
+    Y = b.attn_fwd(t["X"].to(dev), qkv_sh, o_sh, S=w.S, H=w.H, mu=w.mu, partial=w.partial, schedule=p["schedule"])
+    f = {k: v.to(torch.float64).numpy() for k, v in t.items()}
+    err = oracle.max_rel_err(Y.double().cpu().numpy(), att.attn_fwd(f["X"], f["Wqkv"], f["Wo"], w.S, w.H))
     assert err <= 1e-2

@@ -1,5 +1,6 @@
-"""Schedule selection (domino_mlp_plan) on the host: the rule stated in
-include/domino.h, checked with explicit hardware figures (no device needed).
+"""Schedule selection (domino_mlp_plan, domino_attn_plan) on the host: the rules
+stated in include/domino.h, checked with explicit hardware figures (no device
+needed).
 
 The rule: schedule FUSED when the fused cooperative forward can be launched,
 else STREAMS; mu = the smallest power of two dividing M whose chunk of hidden
@@ -90,4 +91,65 @@ def test_plan_rejects_invalid_problems(lib, kw, status):
     args.update(kw)
     with pytest.raises(b.DominoError) as e:
         b.plan(**args, **GB300)
+    assert e.value.status == status
+
+
+# ------------------------------------------------------------ attention block
+# domino_attn_plan: the same rule over whole-sequence chunks, with one chunk's Q|K|V (B/mu * S * 3 H dh * 2
+# bytes) as the intermediate that must fit in 9/10 of the L2 and the Q|K|V projection's paired tiles as the
+# filling test; the schedule is always STREAMS.
+
+def attn_plan_for(w, **hw):
+    return b.plan_attn(w.B, w.S, w.d, w.H, w.P, w.partial, dh=w.dh,
+                       **{**dict(num_sms=GB300["num_sms"], l2_bytes=GB300["l2_bytes"]), **hw})
+
+
+def test_attn_plan_workloads(lib):
+    budget = 126 * 2**20 // 10 * 9
+    # GPT-style: all 4 sequences' Q|K|V, 4096 * 3 * 2560 * 2 = 62.9 MB, fit at mu = 1
+    p = attn_plan_for(wl.ATTN_WORKLOADS["gpt_attn_fwd"])
+    assert (p["mu"], p["schedule"], p["reason"]) == (1, "streams", "fits_l2")
+    assert p["chunk_qkv_bytes"] == 4096 * 3 * 2560 * 2 <= budget
+    # 16 row blocks x 8 column blocks (3 * 5 heads * 128 = 1920 columns per shard) x 4 shards
+    assert p["proj_tiles_per_chunk"] == 16 * 8 * 4
+    # Llama-style: 8192 * 3 * 4096 * 2 = 201 MB does not fit; two sequences (101 MB) do
+    p = attn_plan_for(wl.ATTN_WORKLOADS["llama_attn_fwd"])
+    assert (p["mu"], p["schedule"], p["reason"]) == (2, "streams", "fits_l2")
+    assert 8192 * 3 * 4096 * 2 > budget >= p["chunk_qkv_bytes"] == 4096 * 3 * 4096 * 2
+
+
+def test_attn_plan_small_and_empty(lib):
+    # 256 rows: 1 row block x 2 column blocks (384 columns) x 2 shards = 4 tiles < 76 clusters
+    p = attn_plan_for(wl.ATTN_WORKLOADS["tiny_attn_fwd"])
+    assert (p["mu"], p["reason"], p["proj_tiles_per_chunk"]) == (1, "small", 4)
+    p = b.plan_attn(0, 1024, 2560, 20, 4, "f32", num_sms=152, l2_bytes=126 * 2**20)
+    assert (p["mu"], p["reason"], p["chunk_qkv_bytes"]) == (1, "small", 0)
+
+
+def test_attn_plan_largest_filling_and_divisibility(lib):
+    # a tiny L2: nothing fits, so the finest whole-sequence chunking that still fills the GPU
+    p = b.plan_attn(16, 2048, 4096, 32, 8, "bf16", num_sms=152, l2_bytes=2**20)
+    tiles = lambda mu: -(-(16 // mu * 2048) // 256) * (3 * 4 * 128 // 256) * 8
+    assert p["reason"] == "largest_filling"
+    assert tiles(p["mu"]) >= 76 and (p["mu"] == 16 or tiles(2 * p["mu"]) < 76)
+    # B = 6: only mu = 1 and 2 divide it
+    p = b.plan_attn(6, 2048, 4096, 32, 8, "bf16", num_sms=152, l2_bytes=2**20)
+    assert (p["mu"], p["reason"]) == (2, "largest_filling")
+
+
+@pytest.mark.parametrize("S", [1024, 2048, 4096, 8192])
+def test_attn_plan_monotone_in_sequence_length(lib, S):
+    # longer sequences never ask for fewer chunks
+    mus = [b.plan_attn(8, s, 4096, 32, 8, "bf16", num_sms=152, l2_bytes=126 * 2**20)["mu"] for s in (S, 2 * S)]
+    assert mus[0] <= mus[1]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(P=0), 1), (dict(H=21), 2), (dict(dh=64), 2), (dict(S=1000), 2), (dict(d=2564), 3),
+])
+def test_attn_plan_rejects_invalid_problems(lib, kw, status):
+    args = dict(B=4, S=1024, d=2560, H=20, P=4, partial="f32")
+    args.update(kw)
+    with pytest.raises(b.DominoError) as e:
+        b.plan_attn(**args, num_sms=152, l2_bytes=126 * 2**20)
     assert e.value.status == status
