@@ -31,7 +31,7 @@ def cuda():
     torch.cuda.set_device(0)
 
 
-def _grid(lo, hi, seed):
+def _grid(lo, hi, seed, F=F):
     """d x F bf16 values covering [lo, hi], in a seeded order."""
     v = np.linspace(lo, hi, D * F)
     np.random.default_rng(seed).shuffle(v)
@@ -46,11 +46,23 @@ def _bf16_ulp(x: np.ndarray) -> np.ndarray:
 @pytest.mark.parametrize("schedule", ["fused", "streams"])
 @pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "swiglu", "identity"])
 def test_activation_epilogue_elementwise(act, schedule):
+    _check_elementwise(act, schedule, F)
+
+
+@pytest.mark.parametrize("schedule", ["fused", "streams"])
+def test_swiglu_ragged_column_block_elementwise(schedule):
+    # F / P = 1000 = 7 x 128 + 104: the last SwiGLU column block holds 104 valid columns of gate and of up (the
+    # rest of its gate and up boxes zero-filled), and every one of them must pair gate column c with up column c
+    _check_elementwise("swiglu", schedule, 2000)
+
+
+def _check_elementwise(act, schedule, F):
+    FP = F // P
     dev = torch.device("cuda:0")
     X = torch.zeros(M, D, dtype=torch.bfloat16)
     X[torch.arange(M), torch.arange(M) % D] = 1.0
-    Wg = _grid(-8.0, 8.0, 1)
-    Wu = _grid(-2.0, 2.0, 2)
+    Wg = _grid(-8.0, 8.0, 1, F)
+    Wu = _grid(-2.0, 2.0, 2, F)
     Bw = (0.02 * torch.randn(F, D, generator=torch.Generator().manual_seed(3))).to(torch.bfloat16)
     A = (Wg.to(dev), Wu.to(dev)) if act == "swiglu" else Wg.to(dev)
     A_sh, B_sh = b.shard_weights(A, Bw.to(dev), P)

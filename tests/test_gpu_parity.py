@@ -96,6 +96,14 @@ def test_ragged_shapes(act, partial, schedule):
     _check_full(w, seed=3, schedule=schedule)
 
 
+@pytest.mark.parametrize("h", [8, 40, 64, 96, 120, 0])
+def test_swiglu_ragged_last_column_block(h):
+    # F / P = 256 + h: the last SwiGLU column block holds h < 128 valid columns of gate and of up, the rest of
+    # each 128-row weight box zero-filled (h = 0: no ragged block)
+    w = wl.Workload(f"swiglu_ragged_{h}", M=512, d=256, F=2 * (256 + h), P=2, mu=2, act="swiglu", partial="bf16")
+    _check_full(w, seed=11, schedule="fused")
+
+
 @pytest.mark.parametrize("rows", [129, 200, 300, 700])
 @pytest.mark.parametrize("act,partial", [("gelu", "f32"), ("swiglu", "bf16")])
 @pytest.mark.parametrize("schedule", ["streams", "fused"])
