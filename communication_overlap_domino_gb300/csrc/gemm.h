@@ -115,8 +115,6 @@ domino_status_t launch_fused_fwd(const FusedLaunch& L, int max_ctas, int max_pai
 void set_last_error(const std::string& msg);
 // Validates a descriptor the way domino_mlp_fwd does (sets the last error on failure).
 domino_status_t validate_desc(const domino_mlp_desc_t* desc);
-// Validates an attention descriptor the way domino_attn_fwd does.
-domino_status_t validate_attn_desc(const domino_attn_desc_t* desc);
 
 // Bounded-wait self-test (shard_sum.cu).
 domino_status_t launch_selftest_wait(void* workspace, uint64_t timeout_ns, cudaStream_t stream, std::string* err);

@@ -18,6 +18,12 @@
 #include "domino.h"
 #include "gemm.h"
 
+namespace domino {
+// Validates an attention descriptor the way domino_attn_fwd does (api.cu; sets
+// the last error on failure).
+domino_status_t validate_attn_desc(const domino_attn_desc_t* desc);
+}  // namespace domino
+
 namespace {
 
 constexpr int kPairTileRows = 256;   // rows of a paired GEMM tile
