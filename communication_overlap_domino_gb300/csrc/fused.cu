@@ -13,7 +13,8 @@
 // Work, in one global order shared by all CTAs (static round-robin, tile t is
 // processed by CTA t mod gridDim.x, in increasing t):
 //   for each chunk k:  GEMM1 tiles, then GEMM2 tiles (shard, column block, row
-//                      block; the last chunk's GEMM2 in groups of 8 row blocks)
+//                      block; the last chunk's GEMM2 in groups of 8 row blocks,
+//                      its last group cut to 4)
 // Dependencies, through counters in the workspace (release/acquire at GPU scope):
 //   GEMM2 tile (k, m, n, p) needs H_{k,p}[row block m] complete: hcnt[k][p][m]
 //     counts finished 32-row quarters of GEMM1 tiles (target tiles_n1 * 4); the
@@ -82,7 +83,10 @@ struct FusedTile {
 // block of the weights is loaded once and reused by every row block while it is
 // in L2).  The last chunk's GEMM2 uses smaller groups, so the P partials of its
 // first output tiles are complete -- and their shard-sum runs -- while the rest
-// of the chunk is still being multiplied.
+// of the chunk is still being multiplied; and its last group is cut to G / 2
+// row blocks (the group before it takes the rest, so the weights are read as
+// often as with equal groups) and taken column block by column block, because
+// the shard-sum of that last group is the one reduction nothing overlaps.
 constexpr int kLastChunkGroupM = 8;
 
 __device__ __forceinline__ void grouped_coords(int r, int G, int P, int tiles_m, int tiles_n, int& p, int& m,
@@ -99,6 +103,42 @@ __device__ __forceinline__ void grouped_coords(int r, int G, int P, int tiles_m,
   m = g * G + (r3 - n * gm);
 }
 
+// The same order for the last chunk's GEMM2: with n = ceil(tiles_m / G) >= 2
+// groups, groups 0 .. n-3 hold G row blocks, group n-2 the rest but the last
+// L = G / 2, group n-1 those L.  The last group goes column block by column
+// block (for each n: for each shard: for each row block), so that its output
+// tiles get their P partials -- and their shard-sum starts -- one column block
+// after another instead of all during the last shard's pass; its rows of H
+// (L row blocks of every shard) stay in L2 across the column blocks.
+__device__ __forceinline__ void grouped_coords_tail(int r, int G, int P, int tiles_m, int tiles_n, int& p, int& m,
+                                                    int& n) {
+  const int ngroups = (tiles_m + G - 1) / G;
+  const int L = G / 2;
+  const int full = P * tiles_n * G;
+  const int uniform = (ngroups - 2) * full;
+  if (ngroups < 2 || L < 1 || r < uniform) {
+    grouped_coords(r, G, P, tiles_m, tiles_n, p, m, n);
+    return;
+  }
+  int r2 = r - uniform;
+  const int m0a = (ngroups - 2) * G;
+  const int size_a = tiles_m - m0a - L;
+  if (r2 < P * tiles_n * size_a) {
+    const int per_p = tiles_n * size_a;
+    p = r2 / per_p;
+    const int r3 = r2 - p * per_p;
+    n = r3 / size_a;
+    m = m0a + (r3 - n * size_a);
+    return;
+  }
+  r2 -= P * tiles_n * size_a;
+  const int per_n = P * L;
+  n = r2 / per_n;
+  const int r3 = r2 - n * per_n;
+  p = r3 / L;
+  m = tiles_m - L + (r3 - p * L);
+}
+
 __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
   FusedTile T;
   const int per_chunk = f.tiles_a + f.tiles_b;
@@ -109,8 +149,12 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
     grouped_coords(r, f.tiles_m, f.P, f.tiles_m, f.tiles_n1, T.p, T.m, T.n);
   } else {
     T.phase = 1;
-    const int G = T.k == f.mu - 1 ? (f.tiles_m < kLastChunkGroupM ? f.tiles_m : kLastChunkGroupM) : f.tiles_m;
-    grouped_coords(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+    if (T.k == f.mu - 1) {
+      const int G = f.tiles_m < kLastChunkGroupM ? f.tiles_m : kLastChunkGroupM;
+      grouped_coords_tail(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+    } else {
+      grouped_coords(r - f.tiles_a, f.tiles_m, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+    }
   }
   return T;
 }
@@ -128,8 +172,12 @@ __device__ __forceinline__ FusedTile fused_pair_tile(const FusedParams& f, int t
   } else {
     T.phase = 1;
     const int g2 = kLastChunkGroupM / 2;
-    const int G = T.k == f.mu - 1 ? (f.tiles_m2 < g2 ? f.tiles_m2 : g2) : f.tiles_m2;
-    grouped_coords(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
+    if (T.k == f.mu - 1) {
+      const int G = f.tiles_m2 < g2 ? f.tiles_m2 : g2;
+      grouped_coords_tail(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
+    } else {
+      grouped_coords(r - f.tiles_a2, f.tiles_m2, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
+    }
   }
   return T;
 }
