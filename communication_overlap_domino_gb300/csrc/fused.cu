@@ -83,10 +83,11 @@ struct FusedTile {
 // block of the weights is loaded once and reused by every row block while it is
 // in L2).  The last chunk's GEMM2 uses smaller groups, so the P partials of its
 // first output tiles are complete -- and their shard-sum runs -- while the rest
-// of the chunk is still being multiplied; and its last group is cut to G / 2
-// row blocks (the group before it takes the rest, so the weights are read as
-// often as with equal groups) and taken column block by column block, because
-// the shard-sum of that last group is the one reduction nothing overlaps.
+// of the chunk is still being multiplied; and (when it keeps two waves of
+// tiles) its last group is cut to G / 2 row blocks (the group before it takes
+// the rest, so the weights are read as often as with equal groups) and taken
+// column block by column block, because the shard-sum of that last group is
+// the one reduction nothing overlaps.
 constexpr int kLastChunkGroupM = 8;
 
 __device__ __forceinline__ void grouped_coords(int r, int G, int P, int tiles_m, int tiles_n, int& p, int& m,
@@ -139,6 +140,14 @@ __device__ __forceinline__ void grouped_coords_tail(int r, int G, int P, int til
   m = tiles_m - L + (r3 - p * L);
 }
 
+// The graded order pays only when the cut-down last group still has tiles
+// enough (two waves over the CTAs or clusters) for the shard-sum of the group
+// before it to hide behind: on the GPT-style layer, whose last group would be
+// about one wave, it made the layer 1.9% slower.
+__device__ __forceinline__ bool graded_tail(int last_group_tiles, int units) {
+  return last_group_tiles >= 2 * units;
+}
+
 __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
   FusedTile T;
   const int per_chunk = f.tiles_a + f.tiles_b;
@@ -151,7 +160,10 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
     T.phase = 1;
     if (T.k == f.mu - 1) {
       const int G = f.tiles_m < kLastChunkGroupM ? f.tiles_m : kLastChunkGroupM;
-      grouped_coords_tail(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+      if (graded_tail(f.P * f.tiles_n2 * (G / 2), static_cast<int>(gridDim.x)))
+        grouped_coords_tail(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+      else
+        grouped_coords(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
     } else {
       grouped_coords(r - f.tiles_a, f.tiles_m, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
     }
@@ -174,7 +186,10 @@ __device__ __forceinline__ FusedTile fused_pair_tile(const FusedParams& f, int t
     const int g2 = kLastChunkGroupM / 2;
     if (T.k == f.mu - 1) {
       const int G = f.tiles_m2 < g2 ? f.tiles_m2 : g2;
-      grouped_coords_tail(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
+      if (graded_tail(f.P * f.tiles_n2 * (G / 2), static_cast<int>(gridDim.x >> 1)))
+        grouped_coords_tail(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
+      else
+        grouped_coords(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
     } else {
       grouped_coords(r - f.tiles_a2, f.tiles_m2, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
     }
