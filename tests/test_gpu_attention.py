@@ -53,6 +53,8 @@ def _f64(t):
     # 320 items of one key block each: every CTA runs several rounds and hands its output accumulator, row-sum
     # slots and Q slots over on every block
     wl.AttnWorkload("attn_many_short", B=160, S=128, d=256, H=2, P=2, mu=1, partial="f32"),
+    # one work item in all: a grid of one CTA, one key block, no shard to sum with
+    wl.AttnWorkload("attn_single_item", B=1, S=128, d=128, H=1, P=1, mu=1, partial="f32"),
 ], ids=lambda w: w.name if hasattr(w, "name") else w)
 def test_attention_block_matches_oracle(w, schedule):
     t = wl.generate_attn(w, seed=5)

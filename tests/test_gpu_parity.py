@@ -137,6 +137,13 @@ def test_degenerate_slicings(P, mu, S, schedule):
     _check_full(w, seed=5, schedule=schedule)
 
 
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_single_row_chunks(schedule):
+    # mu = M: every chunk is one row (each GEMM tile and shard-sum piece holds a single valid row)
+    w = wl.Workload("single_rows", M=40, d=256, F=512, P=2, mu=40, act="gelu", partial="f32")
+    _check_full(w, seed=9, schedule=schedule)
+
+
 def test_empty_batch_leaves_output_untouched():
     w = wl.Workload("empty", M=0, d=512, F=1024, P=2, mu=1, act="gelu", partial="f32")
     t = wl.generate(w.with_(M=1))
