@@ -88,30 +88,58 @@ def test_attention_device_status_and_empty_batch():
     assert b.lib().domino_attn_fwd(empty, None, None, None, None, None, 0, None) == 0
 
 
-def test_gpt_attention_full_size_sampled():
-    w = wl.ATTN_WORKLOADS["gpt_attn_fwd"]
+def _full_size_refs(name):
+    # the workload's first and last sequence through the fp64 oracle, once per module
+    w = wl.ATTN_WORKLOADS[name]
     t = wl.generate_attn(w, seed=0)
-    Y = _run(w, t).double().cpu().numpy()
     f = _f64(t)
-    for seq in (0, w.B - 1):  # one sequence from each chunk
+    refs = {}
+    for seq in (0, w.B - 1):
         rows = slice(seq * w.S, (seq + 1) * w.S)
-        ref = att.attn_fwd(f["X"][rows], f["Wqkv"], f["Wo"], w.S, w.H)
+        refs[seq] = att.attn_fwd(f["X"][rows], f["Wqkv"], f["Wo"], w.S, w.H)
+    return w, t, refs
+
+
+@pytest.fixture(scope="module")
+def gpt_full():
+    return _full_size_refs("gpt_attn_fwd")
+
+
+@pytest.fixture(scope="module")
+def llama_full():
+    return _full_size_refs("llama_attn_fwd")
+
+
+def _check_sampled(w, t, refs, schedule):
+    Y = _run(w, t, schedule).double().cpu().numpy()
+    for seq, ref in refs.items():
+        rows = slice(seq * w.S, (seq + 1) * w.S)
         err = max_rel_err(Y[rows], ref)
-        assert err <= TOL, f"sequence {seq}: {err:.3e}"
+        assert err <= TOL, f"{w.name} mu {w.mu} {schedule}, sequence {seq}: {err:.3e}"
     assert np.isfinite(Y).all()
+
+
+@pytest.mark.parametrize("mu", [1, 2])  # 1: the planned chunking the bench times; 2: the layer's MLP chunking
+def test_gpt_attention_full_size_sampled(gpt_full, mu):
+    w, t, refs = gpt_full
+    _check_sampled(w.with_(mu=mu), t, refs, "streams")
 
 
 @pytest.mark.parametrize("schedule", ["streams", "fused"])
-def test_llama_attention_full_size_sampled(schedule):
-    # 4 sequences of 2048 tokens, d 4096, 32 heads on 8 shards, 4 chunks of one sequence each, bf16 partials:
-    # the first and the last chunk's sequence against the oracle
-    w = wl.ATTN_WORKLOADS["llama_attn_fwd"]
-    t = wl.generate_attn(w, seed=0)
-    Y = _run(w, t, schedule).double().cpu().numpy()
-    f = _f64(t)
-    for seq in (0, w.B - 1):
-        rows = slice(seq * w.S, (seq + 1) * w.S)
-        ref = att.attn_fwd(f["X"][rows], f["Wqkv"], f["Wo"], w.S, w.H)
-        err = max_rel_err(Y[rows], ref)
-        assert err <= TOL, f"sequence {seq}: {err:.3e}"
-    assert np.isfinite(Y).all()
+@pytest.mark.parametrize("mu", [2, 4])  # 2: the planned chunking the bench times; 4: the layer's MLP chunking
+def test_llama_attention_full_size_sampled(llama_full, schedule, mu):
+    # 4 sequences of 2048 tokens, d 4096, 32 heads on 8 shards, bf16 partials: the first and the last sequence
+    w, t, refs = llama_full
+    _check_sampled(w.with_(mu=mu), t, refs, schedule)
+
+
+@pytest.mark.parametrize("name,mus", [("gpt_attn_fwd", (1, 2)), ("llama_attn_fwd", (2, 4))])
+def test_attention_full_size_independent_of_chunking(name, mus):
+    # a sequence's output depends on nothing outside it, and every reduction runs in the same order whatever the
+    # chunking: the whole output is bit-identical across mu
+    w = wl.ATTN_WORKLOADS[name]
+    t = wl.generate_attn(w, seed=1)
+    a = _run(w.with_(mu=mus[0]), t)
+    c = _run(w.with_(mu=mus[1]), t)
+    torch.cuda.synchronize()
+    assert torch.equal(a, c)
