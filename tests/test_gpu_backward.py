@@ -95,6 +95,21 @@ def test_fused_backward_equals_streams(act, partial):
     assert all(torch.equal(a, b2) for a, b2 in zip(ga, ra)) and torch.equal(got[3], ref[3])
 
 
+def test_llama_fwdbwd_full_size_fused_equals_streams():
+    # the bench's fwd+bwd configuration at full size (8192 tokens, d 4096, F 11008, P 8, mu 4): the FUSED forward
+    # and backward against the per-chunk launches, every output bit for bit (the graded, column-ordered last row
+    # group of the fused launches included)
+    w = wl.WORKLOADS["llama_swiglu_fwdbwd"]
+    t = wl.generate(w, 3, with_dy=True)
+    ref = _run_fwd_bwd(w, t, "streams")
+    got = _run_fwd_bwd(w, t, "fused")
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], ref[0]), "Y differs"
+    assert torch.equal(got[1], ref[1]), "dX differs"
+    assert all(torch.equal(a, c) for a, c in zip(got[2], ref[2])), "dA differs"
+    assert torch.equal(got[3], ref[3]), "dB differs"
+
+
 @pytest.mark.parametrize("schedule", ["serial", "fused"])
 def test_backward_llama_tail_bf16_partials(schedule):
     w = wl.Workload("llama_tail_bwd", M=512, d=512, F=2752, P=2, mu=2, act="swiglu", partial="bf16", bwd=True)

@@ -261,6 +261,22 @@ def test_large_swiglu_mu_sweep(mu, schedule):
     _check_sampled(wl.WORKLOADS["large_swiglu_fwd"].with_(mu=mu), schedule)
 
 
+@pytest.mark.parametrize("name,mus", [("large_swiglu_fwd", (4, 2)), ("gpt_gelu_fwd", (2, 1)),
+                                      ("llama_swiglu_fwd", (4, 2))])
+def test_full_size_bit_identical_across_schedules_and_mu(name, mus):
+    # every output element is the same tiles' sums in the same order whatever the schedule and the chunking: the
+    # whole output of the bench's configuration (FUSED at the first mu) equals STREAMS at that mu and FUSED at the
+    # other bit for bit
+    w = wl.WORKLOADS[name]
+    t = wl.generate(w, 2)
+    y_fused = _run(w.with_(mu=mus[0]), t, "fused")
+    y_streams = _run(w.with_(mu=mus[0]), t, "streams")
+    y_other_mu = _run(w.with_(mu=mus[1]), t, "fused")
+    torch.cuda.synchronize()
+    assert torch.equal(y_fused, y_streams), "fused and stream schedules differ"
+    assert torch.equal(y_fused, y_other_mu), "result depends on mu"
+
+
 # ------------------------------------------------------- failure detection
 
 def test_bounded_wait_reports_timeout_and_context_survives():
