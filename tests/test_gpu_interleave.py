@@ -67,3 +67,28 @@ def test_interleaved_equals_separate_calls(w, schedule):
     else:
         errs["dA"] = oracle.max_rel_err(f64(dA_full), ref["dA"])
     assert all(v <= 1e-2 for v in errs.values()), errs
+
+
+@pytest.mark.parametrize("schedule", ["streams", "serial"])
+def test_interleaved_full_size_equals_separate_calls(schedule):
+    # the Llama-style layer at full size (8192 tokens, d 4096, F 11008, P 8, mu 4): every output of the one
+    # interleaved call bit for bit that of the separate forward and backward calls (whose own parity with the
+    # oracle is checked at this size on sampled rows and hidden units)
+    w = wl.WORKLOADS["llama_swiglu_fwdbwd"]
+    A_sh, B_sh, Xa, Xb, dYb, _, _ = _strands(w)
+    kw = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices)
+    desc = b.make_desc(w.M, w.d, w.F, w.P, w.mu, w.act, w.partial, w.slices, schedule)
+    saved_b = torch.zeros(b.saved_size(desc), dtype=torch.uint8, device=Xa.device)
+    b.mlp_fwd(Xb, A_sh, B_sh, schedule="streams", saved=saved_b, **kw)
+    saved_a_ref = torch.zeros_like(saved_b)
+    Ya_ref = b.mlp_fwd(Xa, A_sh, B_sh, schedule="streams", saved=saved_a_ref, **kw)
+    dXb_ref, dA_ref, dB_ref = b.mlp_bwd(Xb, A_sh, B_sh, dYb, saved_b, schedule="streams", **kw)
+    saved_a = torch.zeros_like(saved_b)
+    ws = torch.zeros(b.interleaved_workspace_size(desc), dtype=torch.uint8, device=Xa.device)
+    Ya, dXb, dA, dB = b.mlp_fwd_bwd_interleaved(A_sh, B_sh, Xa, Xb, dYb, saved_b, schedule=schedule,
+                                                saved_a=saved_a, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert b.query_device_status(ws) == 0
+    assert torch.equal(Ya, Ya_ref) and torch.equal(saved_a, saved_a_ref) and torch.equal(dXb, dXb_ref)
+    assert all(torch.equal(x, y) for x, y in zip(dA, dA_ref)) and all(torch.equal(x, y) for x, y in zip(dB, dB_ref))
+    assert torch.isfinite(Ya).all() and torch.isfinite(dXb).all()
