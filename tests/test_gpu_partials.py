@@ -66,6 +66,27 @@ def test_partials_match_oracle_and_sum_to_forward(w, schedule):
 
 
 @pytest.mark.parametrize("schedule", ["streams", "fused"])
+def test_partials_full_size_sum_to_forward(schedule):
+    # the bench's configuration (the large SwiGLU layer, the "without" side of its A/B measure): the library's
+    # shard-sum of the 8 partials gives the forward's Y bit for bit, and each partial on sampled rows matches the
+    # oracle's block with that shard's weights
+    w = wl.WORKLOADS["large_swiglu_fwd"]
+    t, X, A_sh, B_sh = _setup(w, 22)
+    kw = dict(F=w.F, mu=w.mu, act=w.act, partial=w.partial, out_slices=w.slices, schedule=schedule)
+    Z = b.mlp_fwd_partials(X, A_sh, B_sh, **kw)
+    Y = b.mlp_fwd(X, A_sh, B_sh, **kw)
+    Ys = torch.empty_like(Y)
+    b.shard_sum(Z, Ys)
+    torch.cuda.synchronize()
+    assert torch.equal(Ys, Y), "sum of the partials differs from the forward pass"
+    rows = torch.tensor([0, 127, 128, 255, 256, w.Mc - 1, w.Mc, w.M - 1])
+    f = {k: v[rows].to(torch.float64).numpy() if k == "X" else v.to(torch.float64).numpy() for k, v in t.items()}
+    for p in (0, w.P - 1):
+        err = oracle.max_rel_err(Z[p][rows].double().cpu().numpy(), _shard_ref(w, f, p))
+        assert err <= TOL, f"shard {p}: {err:.3e}"
+
+
+@pytest.mark.parametrize("schedule", ["streams", "fused"])
 def test_one_shard_rank_computes_its_partial(schedule):
     w = CASES[1]
     t, X, A_sh, B_sh = _setup(w, 22)
