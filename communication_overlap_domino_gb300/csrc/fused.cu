@@ -14,7 +14,8 @@
 // processed by CTA t mod gridDim.x, in increasing t):
 //   for each chunk k:  GEMM1 tiles, then GEMM2 tiles (shard, column block, row
 //                      block; the last chunk's GEMM2 in groups of 8 row blocks,
-//                      its last group cut to 4)
+//                      its last group column by column, and cut to 4 when that
+//                      leaves it two waves of tiles)
 // Dependencies, through counters in the workspace (release/acquire at GPU scope):
 //   GEMM2 tile (k, m, n, p) needs H_{k,p}[row block m] complete: hcnt[k][p][m]
 //     counts finished 32-row quarters of GEMM1 tiles (target tiles_n1 * 4); the
@@ -83,10 +84,10 @@ struct FusedTile {
 // block of the weights is loaded once and reused by every row block while it is
 // in L2).  The last chunk's GEMM2 uses smaller groups, so the P partials of its
 // first output tiles are complete -- and their shard-sum runs -- while the rest
-// of the chunk is still being multiplied; and (when it keeps two waves of
-// tiles) its last group is cut to G / 2 row blocks (the group before it takes
-// the rest, so the weights are read as often as with equal groups) and taken
-// column block by column block, because the shard-sum of that last group is
+// of the chunk is still being multiplied; its last group is taken column
+// block by column block, and (when it keeps two waves of tiles) cut to G / 2
+// row blocks (the group before it takes the rest, so the weights are read as
+// often as with equal groups), because the shard-sum of that last group is
 // the one reduction nothing overlaps.
 constexpr int kLastChunkGroupM = 8;
 
@@ -148,6 +149,25 @@ __device__ __forceinline__ bool graded_tail(int last_group_tiles, int units) {
   return last_group_tiles >= 2 * units;
 }
 
+// Without the grading: equal groups of G, the last one (whatever its size)
+// taken column block by column block.
+__device__ __forceinline__ void grouped_coords_last_cols(int r, int G, int P, int tiles_m, int tiles_n, int& p,
+                                                         int& m, int& n) {
+  const int ngroups = (tiles_m + G - 1) / G;
+  const int uniform = (ngroups - 1) * P * tiles_n * G;
+  if (r < uniform) {
+    grouped_coords(r, G, P, tiles_m, tiles_n, p, m, n);
+    return;
+  }
+  const int L = tiles_m - (ngroups - 1) * G;
+  const int r2 = r - uniform;
+  const int per_n = P * L;
+  n = r2 / per_n;
+  const int r3 = r2 - n * per_n;
+  p = r3 / L;
+  m = tiles_m - L + (r3 - p * L);
+}
+
 __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
   FusedTile T;
   const int per_chunk = f.tiles_a + f.tiles_b;
@@ -163,7 +183,7 @@ __device__ __forceinline__ FusedTile fused_tile(const FusedParams& f, int t) {
       if (graded_tail(f.P * f.tiles_n2 * (G / 2), static_cast<int>(gridDim.x)))
         grouped_coords_tail(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
       else
-        grouped_coords(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
+        grouped_coords_last_cols(r - f.tiles_a, G, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
     } else {
       grouped_coords(r - f.tiles_a, f.tiles_m, f.P, f.tiles_m, f.tiles_n2, T.p, T.m, T.n);
     }
@@ -189,7 +209,7 @@ __device__ __forceinline__ FusedTile fused_pair_tile(const FusedParams& f, int t
       if (graded_tail(f.P * f.tiles_n2 * (G / 2), static_cast<int>(gridDim.x >> 1)))
         grouped_coords_tail(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
       else
-        grouped_coords(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
+        grouped_coords_last_cols(r - f.tiles_a2, G, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
     } else {
       grouped_coords(r - f.tiles_a2, f.tiles_m2, f.P, f.tiles_m2, f.tiles_n2, T.p, T.m, T.n);
     }
